@@ -1,0 +1,462 @@
+"""Benchmark of the REINFORCE Zero learner step (fused logprob + unclipped
+token-level IS loss, forward and backward) on synthetic workloads shaped like
+the pages' runs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--impl ours|reference]
+
+One step = group advantages + rz_loss_fwd_bwd over one batch already resident
+in HBM (H, W, tokens, recorded log mu, cu_seqlens, rewards).  Inputs (H alone
+is 3.3-5.7 GB) are far larger than L2, so no flush is needed between steps.
+Rank 0 prints one JSON line.  Under torchrun each rank runs its own batch
+(weak scaling, no data-path collective) and the max time over ranks counts.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "action tokens/s, fused logprob+IS-loss fwd/bwd (1 GB300); % bf16 tensor roofline"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed
+    region (200 ms period)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+def oracle_sample(b, n_tokens, seed=7):
+    """A bounded sample of the workload for the CPU oracle: the first responses
+    whose total length reaches n_tokens (whole responses, so the per-response
+    means are the workload's own)."""
+    import numpy as np
+    import torch
+    cu = b["cu"].cpu().numpy()
+    B = cu.shape[0] - 1
+    k = 1
+    while k < B and cu[k] < n_tokens:
+        k += 1
+    T = int(cu[k])
+    if T > n_tokens:  # cut the last response short to bound the work
+        T = n_tokens
+    cu_s = np.minimum(cu[:k + 1], T)
+    f = lambda t: t.to("cpu", torch.float64).numpy()
+    return {"H": f(b["H"][:T]), "W": f(b["W"]), "tokens": b["tokens"][:T].cpu().numpy(),
+            "logmu": b["logmu"][:T].cpu().double().numpy(), "cu": cu_s,
+            "adv": b["adv"][:k].cpu().double().numpy(), "T": T}
+
+
+def time_oracle(sample, reps=1):
+    import oracle
+    import numpy as np
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.loss_fwd_bwd(sample["H"], sample["W"], sample["tokens"], sample["logmu"],
+                            sample["cu"], sample["adv"])
+    dt = (time.perf_counter() - t0) / reps
+    return sample["T"] / dt, dt
+
+
+def cpu_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------- workloads
+def build_learner_batch(name, dev, rank):
+    import torch
+    import invariant_logprobs_gb300 as rz
+    from invariant_logprobs_gb300 import synth
+    wl = synth.WORKLOADS[name]
+    b = synth.make_batch(wl, device=dev, seed=wl.seed + 7919 * rank)
+    # the rollout records log mu with its (lagged) weights: our own rollout path
+    b["logmu"], _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
+    b["adv"] = rz.rz_group_advantage(b["rewards"], b["G"])
+    torch.cuda.synchronize()
+    return wl, b
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import invariant_logprobs_gb300 as rz
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rz.load()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    if args.config == "moe30b_logits":
+        return run_logits(args, world, rank, dev, peaks, peak_src)
+
+    wl, b = build_learner_batch(args.config, dev, rank)
+    T, d, V, B = b["T"], b["d"], b["V"], b["B"]
+    ws = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
+    dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    d3 = torch.empty(1, dtype=torch.float32, device=dev)
+    adv = torch.empty(B, dtype=torch.float32, device=dev)
+    err = rz.new_err_flag(dev)
+
+    def step():
+        rz.rz_group_advantage(b["rewards"], b["G"], adv_out=adv)
+        rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
+                           logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
+                           err_flag=err)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for k in range(args.steps):
+        step()
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    per_step = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+
+    # dominant kernel, timed live: the LM-head logprob GEMM (rollout entry point,
+    # one tcgen05 GEMM launch + a tiny merge) over the same rows
+    lp2 = torch.empty(T, dtype=torch.float32, device=dev)
+    ws_r = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, dev)
+    rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], logprob_out=lp2, ws=ws_r)
+    torch.cuda.synchronize()
+    kr = max(2, min(args.steps, 5))
+    rev = [torch.cuda.Event(enable_timing=True) for _ in range(kr + 1)]
+    rev[0].record(stream)
+    for k in range(kr):
+        rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], logprob_out=lp2, ws=ws_r)
+        rev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    roll_ms = statistics.mean(rev[k].elapsed_time(rev[k + 1]) for k in range(kr))
+
+    # end to end through the public API from pinned host buffers
+    e2e = run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err)
+
+    ms = max_over_ranks(total_ms / args.steps, world)
+    value = T * world / (ms / 1e3)
+    flop_alg = 6.0 * d * V * T
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the workload, random-init weights)",
+        "config": {"workload": wl.name, "tokens_per_step": T, "responses": B, "group": wl.group,
+                   "d": d, "V": V, "lag_steps": wl.drift_steps,
+                   "l2": "inputs larger than L2 (H %.1f GB), no flush" % (T * d * 2 / 1e9),
+                   "parallelism": "dp%d replicas" % world},
+        "step_ms_median": statistics.median(per_step),
+        "algorithmic_tflops": flop_alg / (ms / 1e3) / 1e12,
+        "algorithmic_frac_of_sustained_bf16": flop_alg / (ms / 1e3) / 1e12 /
+        peaks["bf16_tflops_sustained"],
+        "roofline": {
+            "kernel": "gemm_kernel<EpiLsePartial> (LM-head logprob GEMM, timed via rz_token_logprob)",
+            "bound": "tensor", "achieved": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12,
+            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+            "peak_source": "%s bf16_tflops_sustained" % peak_src,
+            "traffic": None},
+        "rollout_tokens_per_s": T / (roll_ms / 1e3),
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step(T, V),
+        "device_err_flag": int(err.item()),
+        "loss": float(loss.item()), "d3": float(d3.item()),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        s = oracle_sample(b, args.cpu_tokens)
+        v, dt = time_oracle(s)
+        out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_threads(),
+                               "kind": "oracle",
+                               "sample": "%d tokens (first responses) of the same batch at full "
+                                         "d=%d, V=%d; fp64 numpy, %.1f s" % (s["T"], d, V, dt)}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+def launches_per_step(T, V):
+    chunk = 38912
+    n_chunks = (T + chunk - 1) // chunk
+    return 1 + 2 + 2 + 3 * n_chunks   # advantage; lse GEMM + merge; loss (2); per chunk 3
+
+
+def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err):
+    import torch
+    host = {k: b[k].cpu().pin_memory() for k in ("H", "tokens", "logmu", "cu", "rewards")}
+    dev_bufs = {k: torch.empty_like(b[k]) for k in host}
+    res = torch.empty(2, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = 8
+
+    def step():
+        for k in host:
+            dev_bufs[k].copy_(host[k], non_blocking=True)
+        rz.rz_group_advantage(dev_bufs["rewards"], b["G"], adv_out=adv)
+        rz.rz_loss_fwd_bwd(dev_bufs["H"], b["W"], dev_bufs["tokens"], dev_bufs["logmu"],
+                           dev_bufs["cu"], adv, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
+                           d3_out=d3, ws=ws, err_flag=err)
+        res[0:1].copy_(loss, non_blocking=True)
+        res[1:2].copy_(d3, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 3))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    return {"value": b["T"] / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def run_logits(args, world, rank, dev, peaks, peak_src):
+    import torch
+    import invariant_logprobs_gb300 as rz
+    from invariant_logprobs_gb300 import synth
+    wl = synth.WORKLOADS["moe30b_logits"]
+    b = synth.make_logits_batch(wl, device=dev, seed=wl.seed + 7919 * rank)
+    T, V, B = b["T"], b["V"], b["B"]
+    logpi = torch.empty(T, dtype=torch.float32, device=dev)
+    for s in range(0, T, 8192):
+        e = min(T, s + 8192)
+        z = torch.log_softmax(b["logits"][s:e].float(), dim=-1)
+        logpi[s:e] = z.gather(1, b["tokens"][s:e].long()[:, None])[:, 0]
+        del z
+    logmu = synth.logmu_near(logpi, synth.LOGMU_NOISE_STD, b["gen"])
+    adv = rz.rz_group_advantage(b["rewards"], b["G"])
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    d3 = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = rz.alloc_workspace(rz.RZ_OP_LOGITS_LOSS, T, 0, V, B, dev)
+    err = rz.new_err_flag(dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rz.rz_logits_loss_fwd_bwd(b["logits"], b["tokens"], logmu, b["cu"], adv,
+                                  logprob_out=lp, loss_out=loss, d3_out=d3, ws=ws, err_flag=err)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(dev.index)
+    clk.start()
+    time.sleep(0.3)
+    barrier(world)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for k in range(args.steps):
+        step()
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clk.stop()
+    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]) / args.steps, world)
+    alg_bytes = T * (4.0 * V + 12.0)
+    out = {
+        "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic bf16 logits ~N(0,3) (in place: later steps read the previous dz)",
+        "config": {"workload": wl.name, "tokens_per_step": T, "responses": B, "V": V,
+                   "l2": "inputs larger than L2 (%.0f GB), no flush" % (T * V * 2 / 1e9),
+                   "parallelism": "dp%d replicas" % world},
+        "roofline": {"kernel": "logits_row_kernel", "bound": "hbm",
+                     "achieved": alg_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": alg_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": "%s hbm_gbs" % peak_src, "traffic": None},
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+        "device_err_flag": int(err.item()),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as it stands, on the host cores, on a bounded sample of
+    the same workload; rank 0 only."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import torch
+    from invariant_logprobs_gb300 import synth
+    import oracle
+    if args.config == "moe30b_logits":
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "reference arm is defined for the hidden-state learner workloads"}))
+        return 0
+    wl = synth.WORKLOADS[args.config]
+    # draw the same distributions on the host (no GPU needed): a small batch
+    # of whole responses at full d and V
+    import dataclasses
+    n = args.cpu_tokens
+    small = dataclasses.replace(wl, n_prompts=1, group=2, len_lo=n // 2, len_hi=n // 2)
+    b = synth.make_batch(small, device="cpu")
+    f = lambda t: t.to(torch.float64).numpy()
+    lm, _ = oracle.token_logprob(f(b["H"]), f(b["W_mu"]), b["tokens"].numpy())
+    b["logmu"] = torch.tensor(lm)
+    b["adv"] = torch.tensor(oracle.group_advantage(f(b["rewards"]), b["G"]))
+    s = oracle_sample(b, args.cpu_tokens)
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_oracle(s)
+    times = []
+    for _ in range(args.steps):
+        _, dt = time_oracle(s)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    v = s["T"] / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)",
+           "config": {"workload": wl.name, "d": wl.d, "V": wl.V,
+                      "tokens_per_step": s["T"], "parallelism": "cpu oracle, rank 0"},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_threads(),
+                            "kind": "oracle",
+                            "sample": "%d tokens at full d=%d, V=%d per step" % (
+                                s["T"], wl.d, wl.V)},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="qwen4b_lag64",
+                    choices=["qwen4b_lag64", "qwen1p5b_lag2", "moe30b_logits", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

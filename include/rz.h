@@ -1,0 +1,191 @@
+/*
+ * rz.h -- C ABI of the batch-invariant logprob + REINFORCE Zero loss library
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (sources are web pages on REINFORCE Zero, cited by title
+ * and section):
+ *   [RZ-page]  "REINFORCE Zero: Kernel Alignment Unlocks Stable Asynchronous
+ *              RL with Importance Sampling", project page, section 02 "The
+ *              mechanism", block "A minimal REINFORCE objective":
+ *                L = -(1/B) sum_i (1/T_i) sum_t A_i pi(a_it|h_it)/mu_i(a_it|h_it),
+ *              T_i = valid action tokens of response i, mu = the behaviour
+ *              probability recorded at sampling time, gradient through the
+ *              numerator pi only.
+ *   [vLLM-zh]  "Zero Mismatch, Simple Async RL: REINFORCE Zero, DeepSeek-V4.1
+ *              and Kimi K3.1" (todayforai rendering): section 3 (D3 = mean
+ *              over all tokens of w - 1 - log w), section 4 items 1-3
+ *              (aligned logprobs, unclipped token-level ratio, advantage =
+ *              reward minus group mean), section 5 ("diff 0": bitwise-equal
+ *              logprob of every sampled token in rollout and trainer).
+ *
+ * Conventions shared by every entry point:
+ *   - Array arguments are DEVICE pointers owned by the caller; the library
+ *     never frees or keeps them.  Scalars are written to device pointers.
+ *   - The library allocates no device memory.  Scratch space is the caller's
+ *     `ws` buffer of at least rz_workspace_size(...) bytes (256-byte aligned).
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     never synchronise the host.  A return of RZ_OK means the work was
+ *     enqueued; faults found on the device are reported through `err_flag`.
+ *   - Layouts are row-major and contiguous.  bf16 arrays are raw 16-bit
+ *     bfloat16 values (rz_bf16).  H, W, dH and logits must be 16-byte
+ *     aligned; d must be a multiple of 8 (16-byte rows for the tensor-memory
+ *     copy engine).
+ *   - Sizes: 0 <= T < 2^31, 1 <= V <= 2^24, 8 <= d <= 65536, B >= 0.
+ *   - Return value: RZ_OK or an RZ_ERR_* code; nothing is enqueued when an
+ *     argument check fails.  rz_status_string() gives the text.
+ *   - err_flag (nullable, device int32): device-side problems are OR-ed
+ *     into it (RZ_DEVERR_*).  The caller zeroes it before the call and reads
+ *     it afterwards.  No kernel ever traps.
+ *   - Batch invariance: the logprob of a row depends only on that row's
+ *     hidden state, its token and W -- never on T, on the other rows or on
+ *     the row's position -- because the GEMM tile (128x256x64), the K order
+ *     and the vocab split (a function of V only) are fixed.
+ */
+#ifndef RZ_H_
+#define RZ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RZ_API __attribute__((visibility("default")))
+#else
+#define RZ_API
+#endif
+
+typedef uint16_t rz_bf16;                 /* raw bfloat16 bits */
+typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
+
+/* Return codes. */
+#define RZ_OK               0
+#define RZ_ERR_INVALID_ARG  1  /* null pointer, bad size, B % G != 0, ... */
+#define RZ_ERR_UNSUPPORTED  2  /* alignment, d % 8, no sm_103a device */
+#define RZ_ERR_WORKSPACE    3  /* ws == NULL or ws_bytes too small */
+#define RZ_ERR_CUDA         4  /* a CUDA runtime/driver call failed */
+
+/* Bits OR-ed into *err_flag by device code. */
+#define RZ_DEVERR_TOKEN_RANGE  1  /* a token id outside [0, V) */
+#define RZ_DEVERR_CU_SEQLENS   2  /* cu_seqlens not 0 = cu[0] <= ... <= cu[B] = T */
+#define RZ_DEVERR_TIMEOUT      4  /* a pipeline wait gave up (kernel returned early) */
+
+/* Operation ids for rz_workspace_size(). */
+#define RZ_OP_TOKEN_LOGPROB   0
+#define RZ_OP_LOSS_FWD_BWD    1
+#define RZ_OP_LOGITS_LOSS     2
+#define RZ_OP_IS_LOSS         3
+
+/*
+ * Bytes of scratch the operation needs for these sizes (0 if none).  Pure
+ * host function; arguments an operation does not use are ignored.
+ */
+RZ_API size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B);
+
+/* Static text for a return code (never NULL). */
+RZ_API const char* rz_status_string(int status);
+
+/*
+ * Rollout side: record log mu of every sampled token [vLLM-zh s.4 item 2;
+ * RZ-page s.02 "recorded behavior probability"].
+ *   H       [T, d] bf16   hidden state that predicts token t
+ *   W       [V, d] bf16   LM-head weight (the rollout's weights)
+ *   tokens  [T] int32     sampled token ids
+ *   logprob_out [T] fp32  log pi(a_t|h_t) = z_{t,a_t} - logsumexp_v z_tv,
+ *                         z = H W^T (fp32 accumulation, temperature 1)
+ *   lse_out [T] fp32      logsumexp_v z_tv (nullable)
+ * Rows whose token is out of range get NaN and set RZ_DEVERR_TOKEN_RANGE.
+ * The learner side (rz_loss_fwd_bwd) runs this very computation with the same
+ * kernels and launch shape, so both sides agree bit for bit at equal weights
+ * [vLLM-zh s.5 "diff 0"].
+ */
+RZ_API int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                     int64_t T, int32_t d, int32_t V,
+                     float* logprob_out, float* lse_out,
+                     void* ws, size_t ws_bytes, int32_t* err_flag,
+                     rz_stream_t stream);
+
+/*
+ * Group-mean advantage [vLLM-zh s.4 item 3]: A_i = r_i - (1/G) sum_{j in g(i)} r_j,
+ * groups are contiguous blocks of G responses.  rewards, adv_out: [B] fp32.
+ * B % G != 0 -> RZ_ERR_INVALID_ARG.  No workspace.
+ */
+RZ_API int rz_group_advantage(const float* rewards, int32_t B, int32_t G,
+                       float* adv_out, rz_stream_t stream);
+
+/*
+ * The importance-sampled loss on given logprobs [RZ-page s.02 objective]:
+ *   w_t = exp(logpi_t - logmu_t) (never clipped)
+ *   loss = -(1/B) sum_{i: T_i > 0} A_i (1/T_i) sum_{t in i} w_t
+ *   d3   = (1/T) sum_t (w_t - 1 - log w_t)           [vLLM-zh s.3]
+ *   coef_out[t] = A_i w_t / (B T_i) = -dloss/dlogpi_t (nullable)
+ * cu_seqlens [B+1] int64 (response i owns tokens cu[i] .. cu[i+1]-1),
+ * adv [B] fp32.  Deterministic (fixed-order reductions).  T = 0 gives
+ * loss = d3 = 0.  Workspace: rz_workspace_size(RZ_OP_IS_LOSS, T, 0, 0, B).
+ */
+RZ_API int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens,
+               const float* adv, int32_t B, int64_t T,
+               float* loss_out, float* d3_out, float* coef_out,
+               void* ws, size_t ws_bytes, int32_t* err_flag, rz_stream_t stream);
+
+/*
+ * D3 diagnostic alone [vLLM-zh s.3]: d3_out = (1/T) sum_t (w_t - 1 - log w_t),
+ * w_t = exp(logpi_t - logmu_t); 0 for T = 0.  One fixed-order reduction, no
+ * workspace.
+ */
+RZ_API int rz_d3(const float* logpi, const float* logmu, int64_t T, float* d3_out,
+          rz_stream_t stream);
+
+/*
+ * Learner side: the fused logprob + REINFORCE Zero loss, forward and backward
+ * [RZ-page s.02 objective and "differentiate through the numerator"].
+ *   H [T,d] bf16, W [V,d] bf16, tokens [T] int32, logmu [T] fp32 (recorded by
+ *   the rollout), cu_seqlens [B+1] int64, adv [B] fp32.
+ * Outputs: loss_out, d3_out (fp32 scalars), logprob_out [T] fp32 (nullable),
+ *   dH [T,d] bf16 = dz W, dW [V,d] fp32 = dz^T H (overwritten, not
+ *   accumulated), with dz_tv = A_i w_t/(B T_i) (softmax_v(z_t) - [v = a_t]).
+ * log pi is produced by exactly the rollout computation (bitwise equal to
+ * rz_token_logprob on the same H, W, tokens).  The backward pass recomputes
+ * logits tile by tile and never stores the [T, V] logits; dW is reduced over
+ * token chunks in a fixed order, so results are run-to-run deterministic.
+ * Workspace: rz_workspace_size(RZ_OP_LOSS_FWD_BWD, T, d, V, B).
+ */
+RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                    const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                    int32_t B, int64_t T, int32_t d, int32_t V,
+                    float* loss_out, float* d3_out, float* logprob_out,
+                    rz_bf16* dH, float* dW,
+                    void* ws, size_t ws_bytes, int32_t* err_flag,
+                    rz_stream_t stream);
+
+/*
+ * Given-logits variant: the same loss on precomputed logits, with the
+ * log-softmax, gather, ratio and dlogits done in place.
+ *   logits_inout [T, V] bf16: read as logits, overwritten with
+ *   dz_tv = A_i w_t/(B T_i) (softmax_v - onehot) in bf16.  V % 8 == 0.
+ *   logprob_out [T] fp32 (required), loss_out, d3_out as in rz_is_loss.
+ * Workspace: rz_workspace_size(RZ_OP_LOGITS_LOSS, T, 0, V, B).
+ */
+RZ_API int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens,
+                           const float* logmu, const int64_t* cu_seqlens,
+                           const float* adv, int32_t B, int64_t T, int32_t V,
+                           float* loss_out, float* d3_out, float* logprob_out,
+                           void* ws, size_t ws_bytes, int32_t* err_flag,
+                           rz_stream_t stream);
+
+/*
+ * LM-head logits z = H W^T as fp32 [T, V] (row-major), from the same
+ * tensor-core tile, K order and accumulation as the logprob path: every
+ * value equals the z the logprob kernels reduce.  No workspace.
+ */
+RZ_API int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32_t d,
+                     int32_t V, float* logits_out, int32_t* err_flag,
+                     rz_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RZ_H_ */

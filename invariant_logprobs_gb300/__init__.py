@@ -1,0 +1,272 @@
+"""Python binding of the rz C ABI (include/rz.h).
+
+Argument marshalling only: each function below checks dtypes/devices,
+allocates outputs and scratch with torch when the caller did not pass them,
+and calls the C entry point of the same name on the current CUDA stream.
+Every step of the computation runs in librz.so's CUDA kernels; there is no
+Python, torch or CPU implementation behind these names.  If the library is
+missing, load() raises -- it never falls back.
+
+Build the library with ``python -m invariant_logprobs_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librz.so")
+
+RZ_OK = 0
+RZ_ERR_INVALID_ARG = 1
+RZ_ERR_UNSUPPORTED = 2
+RZ_ERR_WORKSPACE = 3
+RZ_ERR_CUDA = 4
+
+RZ_DEVERR_TOKEN_RANGE = 1
+RZ_DEVERR_CU_SEQLENS = 2
+RZ_DEVERR_TIMEOUT = 4
+
+RZ_OP_TOKEN_LOGPROB = 0
+RZ_OP_LOSS_FWD_BWD = 1
+RZ_OP_LOGITS_LOSS = 2
+RZ_OP_IS_LOSS = 3
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "rz_workspace_size": (_SZ, [ctypes.c_int, _I64, _I32, _I32, _I32]),
+    "rz_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "rz_token_logprob": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
+    "rz_group_advantage": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
+    "rz_is_loss": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_d3": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+    "rz_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
+                                       _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_logits_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32,
+                                              _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_lmhead_logits": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
+}
+
+
+class RzError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__("%s failed: %s (status %d)" % (fn, status_string(status), status))
+        self.status = status
+
+
+def load(path=None):
+    """Load librz.so (raises OSError/RuntimeError if it is missing)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError("librz.so not built at %s: run invariant_logprobs_gb300.build" % p)
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().rz_status_string(int(status)).decode()
+
+
+def workspace_size(op, T, d, V, B):
+    return int(load().rz_workspace_size(int(op), int(T), int(d), int(V), int(B)))
+
+
+# ----------------------------------------------------------------- helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name, status):
+    if status != RZ_OK:
+        raise RzError(name, status)
+
+
+def _need(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CUDA tensor of %s" % (name, dtype))
+
+
+def alloc_workspace(op, T, d, V, B, device):
+    torch = _torch()
+    n = workspace_size(op, T, d, V, B)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def new_err_flag(device):
+    torch = _torch()
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+# ----------------------------------------------------------------- entry points
+def rz_token_logprob(H, W, tokens, logprob_out=None, lse_out=None, ws=None, err_flag=None,
+                     stream=None):
+    """Rollout-side per-token logprob (see include/rz.h).  Returns
+    (logprob [T] fp32, lse [T] fp32 or None)."""
+    torch = _torch()
+    lib = load()
+    _need(H, torch.bfloat16, "H")
+    _need(W, torch.bfloat16, "W")
+    _need(tokens, torch.int32, "tokens")
+    T, d = H.shape
+    V = W.shape[0]
+    if logprob_out is None:
+        logprob_out = torch.empty(T, dtype=torch.float32, device=H.device)
+    if ws is None:
+        ws = alloc_workspace(RZ_OP_TOKEN_LOGPROB, T, d, V, 0, H.device)
+    st = lib.rz_token_logprob(_ptr(H), _ptr(W), _ptr(tokens), T, d, V, _ptr(logprob_out),
+                              _ptr(lse_out), _ptr(ws), ws.numel(), _ptr(err_flag),
+                              _stream(stream))
+    _check("rz_token_logprob", st)
+    return logprob_out, lse_out
+
+
+def rz_group_advantage(rewards, G, adv_out=None, stream=None):
+    torch = _torch()
+    lib = load()
+    _need(rewards, torch.float32, "rewards")
+    B = rewards.shape[0]
+    if adv_out is None:
+        adv_out = torch.empty_like(rewards)
+    _check("rz_group_advantage",
+           lib.rz_group_advantage(_ptr(rewards), B, int(G), _ptr(adv_out), _stream(stream)))
+    return adv_out
+
+
+def rz_is_loss(logpi, logmu, cu_seqlens, adv, loss_out=None, d3_out=None, coef_out=None,
+               ws=None, err_flag=None, stream=None):
+    torch = _torch()
+    lib = load()
+    _need(cu_seqlens, torch.int64, "cu_seqlens")
+    B = cu_seqlens.shape[0] - 1
+    T = logpi.shape[0]
+    dev = cu_seqlens.device
+    if loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if d3_out is None:
+        d3_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(RZ_OP_IS_LOSS, T, 0, 0, B, dev)
+    st = lib.rz_is_loss(_ptr(logpi), _ptr(logmu), _ptr(cu_seqlens), _ptr(adv), B, T,
+                        _ptr(loss_out), _ptr(d3_out), _ptr(coef_out), _ptr(ws), ws.numel(),
+                        _ptr(err_flag), _stream(stream))
+    _check("rz_is_loss", st)
+    return loss_out, d3_out, coef_out
+
+
+def rz_d3(logpi, logmu, d3_out=None, stream=None):
+    torch = _torch()
+    lib = load()
+    _need(logpi, torch.float32, "logpi")
+    _need(logmu, torch.float32, "logmu")
+    if d3_out is None:
+        d3_out = torch.empty(1, dtype=torch.float32, device=logpi.device)
+    _check("rz_d3", lib.rz_d3(_ptr(logpi), _ptr(logmu), logpi.shape[0], _ptr(d3_out),
+                              _stream(stream)))
+    return d3_out
+
+
+def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=None, dW=None,
+                    loss_out=None, d3_out=None, ws=None, err_flag=None, stream=None,
+                    want_logprob=True):
+    """Learner-side fused logprob + loss forward/backward (see include/rz.h).
+    Returns dict(loss, d3, logprob, dH, dW) of device tensors."""
+    torch = _torch()
+    lib = load()
+    _need(H, torch.bfloat16, "H")
+    _need(W, torch.bfloat16, "W")
+    _need(tokens, torch.int32, "tokens")
+    _need(logmu, torch.float32, "logmu")
+    _need(cu_seqlens, torch.int64, "cu_seqlens")
+    _need(adv, torch.float32, "adv")
+    T, d = H.shape
+    V = W.shape[0]
+    B = cu_seqlens.shape[0] - 1
+    dev = H.device
+    if want_logprob and logprob_out is None:
+        logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
+    if dH is None:
+        dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    if loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if d3_out is None:
+        d3_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
+    st = lib.rz_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(cu_seqlens),
+                             _ptr(adv), B, T, d, V, _ptr(loss_out), _ptr(d3_out),
+                             _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                             _ptr(err_flag), _stream(stream))
+    _check("rz_loss_fwd_bwd", st)
+    return {"loss": loss_out, "d3": d3_out, "logprob": logprob_out, "dH": dH, "dW": dW}
+
+
+def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob_out=None,
+                           loss_out=None, d3_out=None, ws=None, err_flag=None, stream=None):
+    """Given-logits variant; overwrites logits_inout with dz (see include/rz.h)."""
+    torch = _torch()
+    lib = load()
+    _need(logits_inout, torch.bfloat16, "logits_inout")
+    _need(tokens, torch.int32, "tokens")
+    _need(logmu, torch.float32, "logmu")
+    _need(cu_seqlens, torch.int64, "cu_seqlens")
+    _need(adv, torch.float32, "adv")
+    T, V = logits_inout.shape
+    B = cu_seqlens.shape[0] - 1
+    dev = logits_inout.device
+    if logprob_out is None:
+        logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
+    if loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if d3_out is None:
+        d3_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(RZ_OP_LOGITS_LOSS, T, 0, V, B, dev)
+    st = lib.rz_logits_loss_fwd_bwd(_ptr(logits_inout), _ptr(tokens), _ptr(logmu),
+                                    _ptr(cu_seqlens), _ptr(adv), B, T, V, _ptr(loss_out),
+                                    _ptr(d3_out), _ptr(logprob_out), _ptr(ws), ws.numel(),
+                                    _ptr(err_flag), _stream(stream))
+    _check("rz_logits_loss_fwd_bwd", st)
+    return {"loss": loss_out, "d3": d3_out, "logprob": logprob_out}
+
+
+def rz_lmhead_logits(H, W, logits_out=None, err_flag=None, stream=None):
+    torch = _torch()
+    lib = load()
+    _need(H, torch.bfloat16, "H")
+    _need(W, torch.bfloat16, "W")
+    T, d = H.shape
+    V = W.shape[0]
+    if logits_out is None:
+        logits_out = torch.empty((T, V), dtype=torch.float32, device=H.device)
+    st = lib.rz_lmhead_logits(_ptr(H), _ptr(W), T, d, V, _ptr(logits_out), _ptr(err_flag),
+                              _stream(stream))
+    _check("rz_lmhead_logits", st)
+    return logits_out

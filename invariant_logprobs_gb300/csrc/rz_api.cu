@@ -1,0 +1,314 @@
+// rz_api.cu -- the C ABI declared in include/rz.h: argument checks,
+// workspace carving, tensor-map construction and the launch sequence of
+// each operation.  Every step of every operation runs in this library's own
+// kernels; there is no host or library fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/rz.h"
+#include "rz_internal.h"
+
+namespace rz {
+
+// ------------------------------------------------------------------ device facts
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+bool device_ok() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  return major == 10 && minor == 3;  // the library is built for sm_103a only
+}
+
+int64_t chunk_rows(int32_t V) {
+  // dz chunk of rows x round_up(V, 8) bf16, at most 16 GiB.
+  const int64_t per_row = dz_ld(V) * 2;
+  int64_t rows = kChunkRowsMax;
+  const int64_t cap = (int64_t(16) << 30) / (per_row > 0 ? per_row : 1);
+  if (rows > cap) rows = cap / kBM * kBM;
+  if (rows < kBM) rows = kBM;
+  return rows;
+}
+
+// ------------------------------------------------------------------ tensor maps
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (row_stride_bytes & 15u)) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+// ------------------------------------------------------------------ workspace
+inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct FwdLayout {  // logprob pass scratch
+  size_t part, zg, total;
+};
+FwdLayout fwd_layout(int64_t T, int32_t V) {
+  FwdLayout L{};
+  const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
+  L.part = 0;
+  L.zg = al256(t * vocab_splits(V) * sizeof(float2));
+  L.total = L.zg + al256(t * sizeof(float));
+  return L;
+}
+
+struct LearnLayout {
+  FwdLayout fwd;
+  size_t logpi, lse2, coef, resp, dz, total;
+};
+LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
+  LearnLayout L{};
+  const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
+  L.fwd = fwd_layout(T, V);
+  L.logpi = L.fwd.total;
+  L.lse2 = L.logpi + al256(t * 4);
+  L.coef = L.lse2 + al256(t * 4);
+  L.resp = L.coef + al256(t * 4);
+  L.dz = L.resp + is_loss_ws_bytes(B);
+  int64_t rows = chunk_rows(V);
+  if (T < rows) rows = (T + kBM - 1) / kBM * kBM;
+  L.total = L.dz + al256(static_cast<size_t>(rows) * static_cast<size_t>(dz_ld(V)) * 2);
+  return L;
+}
+
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool a256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+bool sizes_ok(int64_t T, int32_t d, int32_t V) {
+  return T >= 0 && T < (int64_t(1) << 31) && V >= 1 && V <= (1 << 24) && d >= 8 && d <= 65536;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RZ_OK : RZ_ERR_CUDA; }
+
+#define RZ_TRY(expr)                                  \
+  do {                                                \
+    cudaError_t _e = (expr);                          \
+    if (_e != cudaSuccess) return RZ_ERR_CUDA;        \
+  } while (0)
+
+// log pi for all T rows: identical launch sequence for rollout and learner.
+int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int64_t T, int32_t d,
+                 int32_t V, float* logprob, float* lse, float* lse2, uint8_t* ws, int* err,
+                 cudaStream_t st) {
+  if (T == 0) return RZ_OK;
+  CUtensorMap tmH, tmW;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
+  const FwdLayout L = fwd_layout(T, V);
+  float2* part = reinterpret_cast<float2*>(ws + L.part);
+  float* zg = reinterpret_cast<float*>(ws + L.zg);
+  RZ_TRY(launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err, st));
+  RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse2, err, st));
+  return RZ_OK;
+}
+
+}  // namespace
+}  // namespace rz
+
+using namespace rz;
+
+extern "C" {
+
+const char* rz_status_string(int status) {
+  switch (status) {
+    case RZ_OK: return "ok";
+    case RZ_ERR_INVALID_ARG: return "invalid argument";
+    case RZ_ERR_UNSUPPORTED: return "unsupported (alignment, d % 8, or device is not sm_103)";
+    case RZ_ERR_WORKSPACE: return "workspace missing or too small";
+    case RZ_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
+  (void)d;
+  if (T < 0) T = 0;
+  switch (op) {
+    case RZ_OP_TOKEN_LOGPROB: return fwd_layout(T, V > 0 ? V : 1).total;
+    case RZ_OP_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
+    case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B);
+    case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
+    default: return 0;
+  }
+}
+
+int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int64_t T,
+                     int32_t d, int32_t V, float* logprob_out, float* lse_out, void* ws,
+                     size_t ws_bytes, int32_t* err_flag, rz_stream_t stream) {
+  if (!sizes_ok(T, d, V)) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!H || !W || !tokens || !logprob_out)) return RZ_ERR_INVALID_ARG;
+  if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
+  if (T == 0) return RZ_OK;
+  if (!a16(H) || !a16(W)) return RZ_ERR_UNSUPPORTED;
+  const size_t need = rz_workspace_size(RZ_OP_TOKEN_LOGPROB, T, d, V, 0);
+  if (!ws || ws_bytes < need || !a256(ws)) return RZ_ERR_WORKSPACE;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  return logprob_pass(H, W, tokens, T, d, V, logprob_out, lse_out, nullptr,
+                      static_cast<uint8_t*>(ws), err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int rz_group_advantage(const float* rewards, int32_t B, int32_t G, float* adv_out,
+                       rz_stream_t stream) {
+  if (B < 0 || G <= 0 || (B % G) != 0) return RZ_ERR_INVALID_ARG;
+  if (B == 0) return RZ_OK;
+  if (!rewards || !adv_out) return RZ_ERR_INVALID_ARG;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  return cuda_status(
+      launch_group_advantage(rewards, B, G, adv_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens,
+               const float* adv, int32_t B, int64_t T, float* loss_out, float* d3_out,
+               float* coef_out, void* ws, size_t ws_bytes, int32_t* err_flag,
+               rz_stream_t stream) {
+  if (B < 0 || T < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
+  if (!loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
+  if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
+  const size_t need = rz_workspace_size(RZ_OP_IS_LOSS, T, 0, 0, B);
+  if (need > 0 && (!ws || ws_bytes < need || !a256(ws))) return RZ_ERR_WORKSPACE;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  return cuda_status(launch_is_loss(logpi, logmu, cu_seqlens, adv, B, T, loss_out, d3_out,
+                                    coef_out, ws, err_flag,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int rz_d3(const float* logpi, const float* logmu, int64_t T, float* d3_out, rz_stream_t stream) {
+  if (T < 0 || !d3_out) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  return cuda_status(launch_d3(logpi, logmu, T, d3_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, const float* logmu,
+                    const int64_t* cu_seqlens, const float* adv, int32_t B, int64_t T, int32_t d,
+                    int32_t V, float* loss_out, float* d3_out, float* logprob_out, rz_bf16* dH,
+                    float* dW, void* ws, size_t ws_bytes, int32_t* err_flag,
+                    rz_stream_t stream) {
+  if (!sizes_ok(T, d, V) || B < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
+  if (!W || !dW || !loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!H || !tokens || !logmu || !dH)) return RZ_ERR_INVALID_ARG;
+  if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
+  if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
+  if (!a16(W) || !a16(dW) || (T > 0 && (!a16(H) || !a16(dH)))) return RZ_ERR_UNSUPPORTED;
+  const LearnLayout L = learn_layout(T, V, B);
+  if (!ws || ws_bytes < L.total || !a256(ws)) return RZ_ERR_WORKSPACE;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+
+  if (T == 0) {
+    RZ_TRY(cudaMemsetAsync(dW, 0, size_t(V) * size_t(d) * sizeof(float), st));
+    RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, B, 0, loss_out, d3_out, nullptr,
+                          w8 + L.resp, err_flag, st));
+    return RZ_OK;
+  }
+
+  // 1. log pi for every row: the rollout's own launch sequence.
+  float* logpi = logprob_out ? logprob_out : reinterpret_cast<float*>(w8 + L.logpi);
+  float* lse2 = reinterpret_cast<float*>(w8 + L.lse2);
+  float* coef = reinterpret_cast<float*>(w8 + L.coef);
+  int s = logprob_pass(H, W, tokens, T, d, V, logpi, nullptr, lse2, w8, err_flag, st);
+  if (s != RZ_OK) return s;
+
+  // 2. loss, D3 and the per-token coefficient c_t = A_i w_t / (B T_i).
+  RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, B, T, loss_out, d3_out, coef, w8 + L.resp,
+                        err_flag, st));
+
+  // 3. backward, chunk by chunk in row order.
+  uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
+  const int64_t ldz = dz_ld(V);
+  const int64_t Tc = chunk_rows(V);
+  CUtensorMap tmH, tmW, tmWmn, tmHmn;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmWmn, W, d, V, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmHmn, H, d, T, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
+  for (int64_t r0 = 0; r0 < T; r0 += Tc) {
+    const int64_t rows = (T - r0) < Tc ? (T - r0) : Tc;
+    CUtensorMap tmDz, tmDzMn;
+    if (!make_tmap_bf16(&tmDz, dz, V, rows, uint64_t(ldz) * 2, kBK, kBM))
+      return RZ_ERR_UNSUPPORTED;
+    if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
+      return RZ_ERR_UNSUPPORTED;
+    RZ_TRY(launch_dlogits(tmH, tmW, r0, rows, d, V, tokens, lse2, coef, dz, ldz, err_flag, st));
+    RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
+    RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
+  }
+  return RZ_OK;
+}
+
+int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const float* logmu,
+                           const int64_t* cu_seqlens, const float* adv, int32_t B, int64_t T,
+                           int32_t V, float* loss_out, float* d3_out, float* logprob_out,
+                           void* ws, size_t ws_bytes, int32_t* err_flag, rz_stream_t stream) {
+  if (T < 0 || T >= (int64_t(1) << 31) || V < 1 || V > (1 << 24) || B < 0 || (B == 0 && T > 0))
+    return RZ_ERR_INVALID_ARG;
+  if (!loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!logits_inout || !tokens || !logmu || !logprob_out)) return RZ_ERR_INVALID_ARG;
+  if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
+  if (V % 8 != 0 || (T > 0 && !a16(logits_inout))) return RZ_ERR_UNSUPPORTED;
+  const size_t need = rz_workspace_size(RZ_OP_LOGITS_LOSS, T, 0, V, B);
+  if (need > 0 && (!ws || ws_bytes < need || !a256(ws))) return RZ_ERR_WORKSPACE;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, adv, B, logprob_out,
+                            err_flag, st));
+  RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, B, T, loss_out, d3_out, nullptr, ws,
+                        err_flag, st));
+  return RZ_OK;
+}
+
+int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32_t d, int32_t V,
+                     float* logits_out, int32_t* err_flag, rz_stream_t stream) {
+  if (!sizes_ok(T, d, V)) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!H || !W || !logits_out)) return RZ_ERR_INVALID_ARG;
+  if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
+  if (T == 0) return RZ_OK;
+  if (!a16(H) || !a16(W)) return RZ_ERR_UNSUPPORTED;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  CUtensorMap tmH, tmW;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
+  return cuda_status(launch_logits_f32(tmH, tmW, T, d, V, logits_out, err_flag,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// rz_internal.h -- host-side declarations shared by the library's
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "rz_gemm.cuh"
+
+namespace rz {
+
+// Vocabulary split of the logprob pass: a function of V only (never of the
+// number of rows), so the per-row reduction order is batch-invariant.
+inline int vocab_tiles(int V) { return (V + kBN - 1) / kBN; }
+inline int vocab_tiles_per_split(int V) {
+  const int nt = vocab_tiles(V);
+  const int s = nt < 8 ? nt : 8;
+  return (nt + s - 1) / s;
+}
+inline int vocab_splits(int V) {
+  const int nt = vocab_tiles(V);
+  const int tps = vocab_tiles_per_split(V);
+  return (nt + tps - 1) / tps;
+}
+
+// Rows per backward chunk: dz for one chunk lives in the workspace.
+constexpr int64_t kChunkRowsMax = 38912;  // 256 * 152
+int64_t chunk_rows(int32_t V);
+inline int64_t dz_ld(int32_t V) { return (static_cast<int64_t>(V) + 7) / 8 * 8; }
+
+int num_sms();
+bool device_ok();  // current device is sm_103 (or newer family member we compiled for)
+
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---- lm-head kernels (rz_lmhead.cu)
+cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
+                               int V, const int32_t* tokens, float2* part, float* zgather,
+                               int* err, cudaStream_t st);
+cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const float2* part,
+                             const float* zgather, float* logprob, float* lse, float* lse2,
+                             int* err, cudaStream_t st);
+cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
+                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse2,
+                           const float* coef, uint16_t* dz, int64_t ldz, int* err,
+                           cudaStream_t st);
+cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
+                              int V, float* out, int* err, cudaStream_t st);
+cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
+                      int64_t rows, int d, int V, uint16_t* dH, int* err, cudaStream_t st);
+cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t row0,
+                      int64_t rows, int d, int V, float* dW, bool accumulate, int* err,
+                      cudaStream_t st);
+
+// ---- loss kernels (rz_loss.cu)
+size_t is_loss_ws_bytes(int32_t B);
+cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cudaStream_t st);
+cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
+                           const float* adv, int B, int64_t T, float* loss, float* d3,
+                           float* coef, void* ws, int* err, cudaStream_t st);
+cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
+                      cudaStream_t st);
+
+// ---- given-logits kernel (rz_logits.cu)
+cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
+                               const float* logmu, const int64_t* cu, const float* adv, int B,
+                               float* logprob, int* err, cudaStream_t st);
+
+}  // namespace rz

@@ -1,0 +1,408 @@
+// rz_lmhead.cu -- the LM-head contractions and their fused epilogues.
+//
+//   lse_partial  (rollout + learner pass 1) z = H W^T per 128x256 tile in
+//                TMEM; the epilogue folds each row's logits into a running
+//                (max, sum of exp) over the tiles of its vocab split, in
+//                ascending vocab order, and picks out z[t, a_t].
+//   lse_merge    fixed-order merge of the splits -> logsumexp, log pi.
+//   dlogits      (learner pass 2) recomputes the same z tiles and writes
+//                dz = c_t (softmax - onehot) as bf16 for one token chunk.
+//   dH, dW       dz W and dz^T H on the same tensor-core pipeline.
+//   logits_f32   plain z = H W^T (same tiles) for callers that want logits.
+//
+// Formulas: log pi(a|h) = z_a - logsumexp_v z_v (the sampled token's
+// logprob, "REINFORCE Zero" project page s.02 and the vLLM post s.4 item 1);
+// dz from differentiating the loss through the numerator pi only (project
+// page s.02, "A minimal REINFORCE objective").
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "rz_gemm.cuh"
+#include "rz_internal.h"
+#include "rz_math.cuh"
+#include "rz_ptx.cuh"
+
+namespace rz {
+
+// ============================================================== epilogues
+// Online log-sum-exp in base 2: state (m2, s) with m2 = max z*log2(e) so far
+// and s = sum 2^(z*log2(e) - m2); the row's logsumexp is (m2 + log2 s) ln 2.
+struct EpiLsePartial {
+  struct Params {
+    const int32_t* tokens;
+    float2* part;    // [T, S]
+    float* zgather;  // [T]
+    long long T;
+    int V;
+    int S;
+  };
+  struct State {
+    float m2, s, za;
+    int a;
+    bool found;
+  };
+
+  static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk, int,
+                                                    int row) {
+    const long long g = static_cast<long long>(m_blk) * kBM + row;
+    st.m2 = -INFINITY;
+    st.s = 0.f;
+    st.za = 0.f;
+    st.found = false;
+    st.a = g < p.T ? __ldg(p.tokens + g) : -1;
+  }
+
+  static __device__ __forceinline__ void chunk(const Params& p, State& st, const uint32_t (&r)[32],
+                                               int cbase) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    if (cbase + 32 > p.V) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (cbase + j >= p.V) v[j] = -INFINITY;
+    }
+    float mx[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+    for (int j = 4; j < 32; j += 4) {
+      mx[0] = fmaxf(mx[0], v[j]);
+      mx[1] = fmaxf(mx[1], v[j + 1]);
+      mx[2] = fmaxf(mx[2], v[j + 2]);
+      mx[3] = fmaxf(mx[3], v[j + 3]);
+    }
+    const float cm2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kLog2e;
+    if (cm2 > st.m2) {
+      st.s *= ex2_approx(st.m2 - cm2);
+      st.m2 = cm2;
+    }
+    const float nm = -st.m2;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j & 3] += ex2_approx(fmaf(v[j], kLog2e, nm));
+    st.s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const unsigned rel = static_cast<unsigned>(st.a - cbase);
+    if (rel < 32u) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (rel == static_cast<unsigned>(j)) st.za = v[j];
+      st.found = true;
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, State& st, int, int n_tile,
+                                              uint32_t taddr, int) {
+    const int col0 = n_tile * kBN;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 64) {
+      if (col0 + c >= p.V) break;  // warp-uniform
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr + c, r0);
+      tmem_ld32(taddr + c + 32, r1);
+      tmem_ld_wait();
+      chunk(p, st, r0, col0 + c);
+      if (col0 + c + 32 < p.V) chunk(p, st, r1, col0 + c + 32);
+    }
+  }
+
+  static __device__ __forceinline__ void task_end(const Params& p, State& st, int m_blk, int grp,
+                                                  int row) {
+    const long long g = static_cast<long long>(m_blk) * kBM + row;
+    if (g >= p.T) return;
+    p.part[g * p.S + grp] = make_float2(st.m2, st.s);
+    if (st.found) p.zgather[g] = st.za;
+  }
+};
+
+// dz_tv = c_t (2^(z log2e - lse2_t) - [v = a_t]) in bf16, one chunk of rows.
+struct EpiDlogits {
+  struct Params {
+    const int32_t* tokens;
+    const float* lse2;
+    const float* coef;
+    uint16_t* dz;
+    long long ldz;
+    long long row0;
+    long long rows;
+    int V;
+  };
+  struct State {
+    float nl, c;
+    int a;
+    bool valid;
+  };
+
+  static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk, int,
+                                                    int row) {
+    const long long r = static_cast<long long>(m_blk) * kBM + row;
+    st.valid = r < p.rows;
+    if (st.valid) {
+      const long long g = p.row0 + r;
+      st.a = __ldg(p.tokens + g);
+      st.nl = -__ldg(p.lse2 + g);
+      st.c = __ldg(p.coef + g);
+    } else {
+      st.a = -1;
+      st.nl = 0.f;
+      st.c = 0.f;
+    }
+  }
+
+  static __device__ __forceinline__ void chunk(const Params& p, const State& st,
+                                               const uint32_t (&r)[32], int cbase,
+                                               uint16_t* out_row) {
+    float g[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      g[j] = st.c * ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, st.nl));
+    const unsigned rel = static_cast<unsigned>(st.a - cbase);
+    if (rel < 32u) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (rel == static_cast<unsigned>(j)) g[j] -= st.c;
+    }
+    if (!st.valid) return;
+    if (cbase + 32 <= p.V) {
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
+      uint16_t* dst = out_row + cbase;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_global_v4(dst + 8 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (cbase + j < p.V) {
+          const uint32_t b = pack_bf16x2(g[j], 0.f);
+          out_row[cbase + j] = static_cast<uint16_t>(b & 0xffffu);
+        }
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, State& st, int m_blk, int n_tile,
+                                              uint32_t taddr, int row) {
+    const int col0 = n_tile * kBN;
+    const long long r = static_cast<long long>(m_blk) * kBM + row;
+    uint16_t* out_row = p.dz + r * p.ldz;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 64) {
+      if (col0 + c >= p.V) break;
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr + c, r0);
+      tmem_ld32(taddr + c + 32, r1);
+      tmem_ld_wait();
+      chunk(p, st, r0, col0 + c, out_row);
+      if (col0 + c + 32 < p.V) chunk(p, st, r1, col0 + c + 32, out_row);
+    }
+  }
+
+  static __device__ __forceinline__ void task_end(const Params&, State&, int, int, int) {}
+};
+
+// Plain stores of the accumulator: bf16 (dH) or fp32 (logits), optionally
+// fp32 accumulate (dW over token chunks, in chunk order).
+template <int kMode>  // 0: bf16 store, 1: fp32 store, 2: fp32 accumulate-or-store
+struct EpiStore {
+  struct Params {
+    void* out;
+    long long ld;    // row stride in elements
+    long long row0;  // row offset into out
+    long long rows;  // valid rows (block-local numbering)
+    int cols;        // valid columns
+    int accumulate;  // mode 2 only
+  };
+  struct State {};
+
+  static __device__ __forceinline__ void task_begin(const Params&, State&, int, int, int) {}
+  static __device__ __forceinline__ void task_end(const Params&, State&, int, int, int) {}
+
+  static __device__ __forceinline__ void chunk(const Params& p, const uint32_t (&r)[32], long long rr,
+                                               int cbase) {
+    if (kMode == 0) {
+      uint16_t* dst = static_cast<uint16_t*>(p.out) + (p.row0 + rr) * p.ld + cbase;
+      if (cbase + 32 <= p.cols) {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          w[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_global_v4(dst + 8 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      } else {
+        for (int j = 0; j < 32; ++j)
+          if (cbase + j < p.cols)
+            dst[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xffffu);
+      }
+    } else {
+      float* dst = static_cast<float*>(p.out) + (p.row0 + rr) * p.ld + cbase;
+      const bool acc = (kMode == 2) && p.accumulate;
+      const bool vec = (cbase + 32 <= p.cols) && ((p.ld & 3) == 0);
+      if (vec) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          float4* d4 = reinterpret_cast<float4*>(dst) + q;
+          if (acc) {
+            const float4 o = *d4;
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+          }
+          *d4 = v;
+        }
+      } else {
+        for (int j = 0; j < 32; ++j)
+          if (cbase + j < p.cols) dst[j] = __uint_as_float(r[j]) + (acc ? dst[j] : 0.f);
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, State&, int m_blk, int n_tile,
+                                              uint32_t taddr, int row) {
+    const int col0 = n_tile * kBN;
+    const long long rr = static_cast<long long>(m_blk) * kBM + row;
+    const bool valid = rr < p.rows;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 64) {
+      if (col0 + c >= p.cols) break;
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr + c, r0);
+      tmem_ld32(taddr + c + 32, r1);
+      tmem_ld_wait();
+      if (valid) {
+        chunk(p, r0, rr, col0 + c);
+        if (col0 + c + 32 < p.cols) chunk(p, r1, rr, col0 + c + 32);
+      }
+    }
+  }
+};
+
+// ============================================================== merge kernel
+// One thread per row: merge the S split states in split order, then
+// log pi = z[t, a_t] - logsumexp.
+__global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __restrict__ tokens,
+                                 const float2* __restrict__ part,
+                                 const float* __restrict__ zgather, float* __restrict__ logprob,
+                                 float* __restrict__ lse, float* __restrict__ lse2_out, int* err) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const float2* pp = part + t * S;
+  float M = -INFINITY;
+  for (int g = 0; g < S; ++g) M = fmaxf(M, pp[g].x);
+  float sum = 0.f;
+  for (int g = 0; g < S; ++g) {
+    const float2 q = pp[g];
+    sum += q.y * exp2f(q.x - M);
+  }
+  float l2 = M + log2f(sum);
+  float l = l2 * kLn2;
+  const int a = tokens[t];
+  float lp;
+  if (a < 0 || a >= V) {
+    lp = __int_as_float(0x7fc00000);
+    l = lp;
+    l2 = lp;
+    if (err) atomicOr(err, 1);
+  } else {
+    lp = zgather[t] - l;
+  }
+  logprob[t] = lp;
+  if (lse) lse[t] = l;
+  if (lse2_out) lse2_out[t] = l2;
+}
+
+// ============================================================== launchers
+namespace {
+
+template <class Epi, bool kAMN, bool kBMN>
+cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmSched& s,
+                     const typename Epi::Params& p, cudaStream_t st) {
+  if (s.num_tasks <= 0) return cudaSuccess;
+  auto kern = gemm_kernel<Epi, kAMN, kBMN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = s.num_tasks < num_sms() ? s.num_tasks : num_sms();
+  kern<<<grid, kThreads, kSmemBytes, st>>>(a, b, s, p);
+  return cudaGetLastError();
+}
+
+GemmSched sched_of(long long m_rows, int n_cols, int n_groups, long long k_depth, int* err) {
+  GemmSched s{};
+  s.m_blocks = static_cast<int>((m_rows + kBM - 1) / kBM);
+  s.n_tiles = (n_cols + kBN - 1) / kBN;
+  s.n_groups = n_groups;
+  s.tiles_per_group = (s.n_tiles + n_groups - 1) / n_groups;
+  s.k_blocks = static_cast<int>((k_depth + kBK - 1) / kBK);
+  s.num_tasks = s.m_blocks * n_groups;
+  s.err = err;
+  return s;
+}
+
+}  // namespace
+
+cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
+                               int V, const int32_t* tokens, float2* part, float* zgather,
+                               int* err, cudaStream_t st) {
+  const int S = vocab_splits(V);
+  GemmSched s = sched_of(T, V, S, d, err);
+  s.tiles_per_group = vocab_tiles_per_split(V);
+  EpiLsePartial::Params p{tokens, part, zgather, static_cast<long long>(T), V, S};
+  return run_gemm<EpiLsePartial, false, false>(tmH, tmW, s, p, st);
+}
+
+cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const float2* part,
+                             const float* zgather, float* logprob, float* lse, float* lse2,
+                             int* err, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (T + threads - 1) / threads;
+  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      T, V, vocab_splits(V), tokens, part, zgather, logprob, lse, lse2, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
+                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse2,
+                           const float* coef, uint16_t* dz, int64_t ldz, int* err,
+                           cudaStream_t st) {
+  const int S = vocab_splits(V);
+  GemmSched s = sched_of(rows, V, S, d, err);
+  s.tiles_per_group = vocab_tiles_per_split(V);
+  s.a_m_off = static_cast<int>(row0);
+  EpiDlogits::Params p{tokens, lse2, coef, dz, ldz, row0, rows, V};
+  return run_gemm<EpiDlogits, false, false>(tmH, tmW, s, p, st);
+}
+
+cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
+                              int V, float* out, int* err, cudaStream_t st) {
+  const int S = vocab_splits(V);
+  GemmSched s = sched_of(T, V, S, d, err);
+  s.tiles_per_group = vocab_tiles_per_split(V);
+  EpiStore<1>::Params p{out, V, 0, T, V, 0};
+  return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
+}
+
+cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
+                      int64_t rows, int d, int V, uint16_t* dH, int* err, cudaStream_t st) {
+  const int nt = (d + kBN - 1) / kBN;
+  GemmSched s = sched_of(rows, d, nt, V, err);
+  EpiStore<0>::Params p{dH, d, row0, rows, d, 0};
+  return run_gemm<EpiStore<0>, false, true>(tmDz, tmWmn, s, p, st);
+}
+
+cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t row0,
+                      int64_t rows, int d, int V, float* dW, bool accumulate, int* err,
+                      cudaStream_t st) {
+  const int nt = (d + kBN - 1) / kBN;
+  GemmSched s = sched_of(V, d, nt, rows, err);
+  s.b_k_off = static_cast<int>(row0);
+  EpiStore<2>::Params p{dW, d, 0, V, d, accumulate ? 1 : 0};
+  return run_gemm<EpiStore<2>, true, true>(tmDzMn, tmHmn, s, p, st);
+}
+
+}  // namespace rz

@@ -1,0 +1,168 @@
+// rz_logits.cu -- the given-logits variant: per row of bf16 logits, the
+// log-softmax normaliser, the sampled token's logprob, the unclipped ratio
+// and the dlogits c_t (softmax - onehot), written back over the logits.
+//
+// Purely bandwidth-bound (no contraction): one CTA streams one row with
+// 16-byte loads.  Pass 1 computes (max, sum exp) online and keeps the first
+// part of the row in shared memory; pass 2 re-reads the rest (mostly from L2)
+// and overwrites the row with dz.  The loss and D3 over all rows are then
+// reduced by the same fixed-order kernels as the hidden-state path.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "rz_internal.h"
+#include "rz_math.cuh"
+#include "rz_ptx.cuh"
+
+namespace rz {
+
+namespace {
+
+constexpr int kRowThreads = 512;
+constexpr int kStashVec = 6144;  // 96 KB of the row kept in shared memory
+constexpr size_t kRowSmem = kStashVec * sizeof(uint4);
+
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+__device__ __forceinline__ void fold8(const uint4& q, float& m2, float& s) {
+  const float v[8] = {bf_lo(q.x), bf_hi(q.x), bf_lo(q.y), bf_hi(q.y),
+                      bf_lo(q.z), bf_hi(q.z), bf_lo(q.w), bf_hi(q.w)};
+  float cm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+                   fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+  const float cm2 = cm * kLog2e;
+  if (cm2 > m2) {
+    s *= ex2_approx(m2 - cm2);
+    m2 = cm2;
+  }
+  const float nm = -m2;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    a0 += ex2_approx(fmaf(v[j], kLog2e, nm));
+    a1 += ex2_approx(fmaf(v[j + 1], kLog2e, nm));
+  }
+  s += a0 + a1;
+}
+
+__device__ __forceinline__ uint4 dz8(const uint4& q, float nl, float c, int rel) {
+  const float v[8] = {bf_lo(q.x), bf_hi(q.x), bf_lo(q.y), bf_hi(q.y),
+                      bf_lo(q.z), bf_hi(q.z), bf_lo(q.w), bf_hi(q.w)};
+  float g[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) g[j] = c * ex2_approx(fmaf(v[j], kLog2e, nl));
+  if (static_cast<unsigned>(rel) < 8u) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (rel == j) g[j] -= c;
+  }
+  uint4 o;
+  o.x = pack_bf16x2(g[0], g[1]);
+  o.y = pack_bf16x2(g[2], g[3]);
+  o.z = pack_bf16x2(g[4], g[5]);
+  o.w = pack_bf16x2(g[6], g[7]);
+  return o;
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    logits_row_kernel(uint16_t* __restrict__ logits, long long T, int V,
+                      const int32_t* __restrict__ tokens, const float* __restrict__ logmu,
+                      const int64_t* __restrict__ cu, const float* __restrict__ adv, int B,
+                      float* __restrict__ logprob, int* err) {
+  extern __shared__ uint4 stash[];
+  __shared__ float red_m[kRowThreads / 32], red_s[kRowThreads / 32];
+  __shared__ float bc[3];
+  __shared__ int bci;
+  const long long row = blockIdx.x;
+  uint4* rowp = reinterpret_cast<uint4*>(logits + row * static_cast<long long>(V));
+  const int nvec = V >> 3;
+  const int nstash = nvec < kStashVec ? nvec : kStashVec;
+
+  // ---- pass 1: online (max, sum exp) in base 2
+  float m2 = -INFINITY, s = 0.f;
+  int i = threadIdx.x;
+  for (; i + kRowThreads < nvec; i += 2 * kRowThreads) {
+    const uint4 q0 = rowp[i];
+    const uint4 q1 = rowp[i + kRowThreads];
+    if (i < nstash) stash[i] = q0;
+    if (i + kRowThreads < nstash) stash[i + kRowThreads] = q1;
+    fold8(q0, m2, s);
+    fold8(q1, m2, s);
+  }
+  for (; i < nvec; i += kRowThreads) {
+    const uint4 q0 = rowp[i];
+    if (i < nstash) stash[i] = q0;
+    fold8(q0, m2, s);
+  }
+  // warp butterfly merge, then warps in order
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m2, o);
+    const float so = __shfl_xor_sync(0xffffffffu, s, o);
+    lse2_merge(m2, s, mo, so);
+  }
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red_m[warp] = m2;
+    red_s[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = red_m[0], S = red_s[0];
+    for (int w = 1; w < kRowThreads / 32; ++w) lse2_merge(M, S, red_m[w], red_s[w]);
+    const float l2 = M + log2f(S);
+    const float l = l2 * kLn2;
+    const int a = tokens[row];
+    float lp, c = 0.f;
+    if (a < 0 || a >= V) {
+      lp = __int_as_float(0x7fc00000);
+      if (err) atomicOr(err, 1);
+    } else {
+      const uint16_t zb = logits[row * static_cast<long long>(V) + a];
+      lp = __uint_as_float(static_cast<uint32_t>(zb) << 16) - l;
+      // response of this row: the last i with cu[i] <= row
+      int lo = 0, hi = B;  // invariant cu[lo] <= row < cu[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= row) lo = mid;
+        else hi = mid;
+      }
+      const long long Ti = cu[lo + 1] - cu[lo];
+      const float inv_bt = Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
+      c = adv[lo] * is_weight(lp, logmu[row]) * inv_bt;
+    }
+    logprob[row] = lp;
+    bc[0] = -l2;
+    bc[1] = c;
+    bci = a;
+  }
+  __syncthreads();
+  const float nl = bc[0];
+  const float c = bc[1];
+  const int a = bci;
+
+  // ---- pass 2: dz = c (softmax - onehot), in place
+  for (int j = threadIdx.x; j < nvec; j += kRowThreads) {
+    const uint4 q = j < nstash ? stash[j] : rowp[j];
+    rowp[j] = dz8(q, nl, c, a - 8 * j);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
+                               const float* logmu, const int64_t* cu, const float* adv, int B,
+                               float* logprob, int* err, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(logits_row_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kRowSmem));
+  if (e != cudaSuccess) return e;
+  logits_row_kernel<<<static_cast<unsigned>(T), kRowThreads, kRowSmem, st>>>(
+      logits, T, V, tokens, logmu, cu, adv, B, logprob, err);
+  return cudaGetLastError();
+}
+
+}  // namespace rz

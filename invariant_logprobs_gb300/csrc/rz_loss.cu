@@ -1,0 +1,148 @@
+// rz_loss.cu -- group advantages, the importance-sampled REINFORCE Zero loss
+// with its per-token gradient coefficient, and the D3 diagnostic.
+//
+//   A_i  = r_i - mean of the rewards of i's group          (vLLM post s.4 item 3)
+//   w_t  = exp(log pi_t - log mu_t), never clipped          (vLLM post s.4 item 2)
+//   L    = -(1/B) sum_i (A_i/T_i) sum_{t in i} w_t          (project page s.02)
+//   D3   = (1/T) sum_t (w_t - 1 - log w_t)                   (vLLM post s.3)
+//   c_t  = A_i w_t / (B T_i) = -dL/dlog pi_t
+//
+// Numerics: w = 1 + expm1(log pi - log mu), so the loss is evaluated as
+//   L = -(1/B) [ sum_i A_i  +  sum_i A_i (1/T_i) sum_t expm1(d_t) ]
+// over responses with T_i > 0; the first sum is exact for centred rewards
+// and the second keeps full relative precision of the (small) lag term.
+// All reductions run in a fixed order: results are bitwise reproducible.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "rz_internal.h"
+#include "rz_math.cuh"
+
+namespace rz {
+
+namespace {
+
+constexpr int kRespThreads = 256;
+constexpr int kFinalThreads = 1024;
+constexpr int kD3Threads = 1024;
+
+struct RespPart {
+  double lag;   // A_i (1/T_i) sum_t expm1(d_t)
+  double base;  // A_i if T_i > 0 else 0
+  double d3;    // sum_t (w_t - 1 - log w_t)
+};
+
+__global__ void __launch_bounds__(kRespThreads)
+    is_loss_resp_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu,
+                        const int64_t* __restrict__ cu, const float* __restrict__ adv, int B,
+                        long long T, float* __restrict__ coef, RespPart* __restrict__ part,
+                        int* err) {
+  __shared__ float red[kRespThreads / 32];
+  const int i = blockIdx.x;
+  long long s = cu[i];
+  long long e = cu[i + 1];
+  const bool bad = s < 0 || e < s || e > T || (i == 0 && s != 0) || (i == B - 1 && e != T);
+  if (bad) {
+    if (threadIdx.x == 0 && err) atomicOr(err, 2);
+    if (s < 0 || s > T) s = 0;
+    if (e < s || e > T) e = s;
+  }
+  const long long Ti = e - s;
+  const float A = adv[i];
+  const float inv_bt = Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
+  float em1 = 0.f, d3s = 0.f;
+  for (long long t = s + threadIdx.x; t < e; t += kRespThreads) {
+    const float dl = logpi[t] - logmu[t];
+    const float w = expf(dl);
+    if (coef) coef[t] = A * w * inv_bt;
+    em1 += expm1f(dl);
+    d3s += d3_term(dl);
+  }
+  const float em1_tot = block_sum<float, kRespThreads>(em1, red);
+  const float d3_tot = block_sum<float, kRespThreads>(d3s, red);
+  if (threadIdx.x == 0) {
+    RespPart r;
+    r.lag = Ti > 0 ? static_cast<double>(A) * static_cast<double>(em1_tot) / static_cast<double>(Ti)
+                   : 0.0;
+    r.base = Ti > 0 ? static_cast<double>(A) : 0.0;
+    r.d3 = static_cast<double>(d3_tot);
+    part[i] = r;
+  }
+}
+
+__global__ void __launch_bounds__(kFinalThreads)
+    is_loss_final_kernel(const RespPart* __restrict__ part, int B, long long T, float* loss,
+                         float* d3) {
+  __shared__ double red[kFinalThreads / 32];
+  double lag = 0.0, base = 0.0, dd = 0.0;
+  for (int i = threadIdx.x; i < B; i += kFinalThreads) {
+    lag += part[i].lag;
+    base += part[i].base;
+    dd += part[i].d3;
+  }
+  const double lag_t = block_sum<double, kFinalThreads>(lag, red);
+  const double base_t = block_sum<double, kFinalThreads>(base, red);
+  const double d3_t = block_sum<double, kFinalThreads>(dd, red);
+  if (threadIdx.x == 0) {
+    if (loss) *loss = B > 0 ? static_cast<float>(-(base_t + lag_t) / B) : 0.f;
+    if (d3) *d3 = T > 0 ? static_cast<float>(d3_t / static_cast<double>(T)) : 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(kD3Threads)
+    d3_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu, long long T,
+              float* d3) {
+  __shared__ double red[kD3Threads / 32];
+  float acc = 0.f;
+  for (long long t = threadIdx.x; t < T; t += kD3Threads) acc += d3_term(logpi[t] - logmu[t]);
+  const double tot = block_sum<double, kD3Threads>(static_cast<double>(acc), red);
+  if (threadIdx.x == 0) *d3 = T > 0 ? static_cast<float>(tot / static_cast<double>(T)) : 0.f;
+}
+
+__global__ void group_advantage_kernel(const float* __restrict__ r, int B, int G,
+                                       float* __restrict__ adv) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B) return;
+  const int g0 = (i / G) * G;
+  double sum = 0.0;
+  for (int j = 0; j < G; ++j) sum += static_cast<double>(r[g0 + j]);
+  adv[i] = static_cast<float>(static_cast<double>(r[i]) - sum / G);
+}
+
+}  // namespace
+
+size_t is_loss_ws_bytes(int32_t B) {
+  const size_t b = B > 0 ? static_cast<size_t>(B) : 0;
+  return (b * sizeof(RespPart) + 255) / 256 * 256;
+}
+
+cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  const int threads = 256;
+  group_advantage_kernel<<<(B + threads - 1) / threads, threads, 0, st>>>(r, B, G, adv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
+                           const float* adv, int B, int64_t T, float* loss, float* d3,
+                           float* coef, void* ws, int* err, cudaStream_t st) {
+  RespPart* part = static_cast<RespPart*>(ws);
+  if (B > 0) {
+    is_loss_resp_kernel<<<B, kRespThreads, 0, st>>>(logpi, logmu, cu, adv, B, T, coef, part,
+                                                    err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, T, loss, d3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
+                      cudaStream_t st) {
+  d3_kernel<<<1, kD3Threads, 0, st>>>(logpi, logmu, T, d3);
+  return cudaGetLastError();
+}
+
+}  // namespace rz

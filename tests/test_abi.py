@@ -1,0 +1,109 @@
+"""CPU checks of the C ABI boundary: the library builds and loads without a
+GPU, exports every function include/rz.h declares, and its host-side
+argument checks return the documented status codes before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rz.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_logprobs_gb300 import build
+    import invariant_logprobs_gb300 as rz
+    path = build.build()
+    return rz.load(path)
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"^RZ_API\s+[\w\s\*]+?\b(rz_\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    for n in ["rz_token_logprob", "rz_loss_fwd_bwd", "rz_group_advantage", "rz_d3",
+              "rz_is_loss", "rz_logits_loss_fwd_bwd", "rz_workspace_size", "rz_status_string",
+              "rz_lmhead_logits"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    import invariant_logprobs_gb300 as rz
+    assert rz.status_string(0) == "ok"
+    for s in range(1, 5):
+        assert rz.status_string(s) and rz.status_string(s) != "unknown status"
+    assert rz.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    import invariant_logprobs_gb300 as rz
+    V = 151936
+    # logprob pass: per row S=8 (max, sum) pairs + one gathered logit
+    s = rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 1000, 2560, V, 0)
+    assert s >= 1000 * (8 * 8 + 4)
+    # independent of d, monotone in T
+    assert s == rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 1000, 64, V, 0)
+    assert rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 2000, 64, V, 0) > s
+    # learner: one dz chunk of at most 38912 rows x V bf16
+    big = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, 1_114_112, 2560, V, 128)
+    assert 38912 * V * 2 < big < 38912 * V * 2 + 1_114_112 * 100 + 10**6
+    small = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, 300, 256, 1024, 8)
+    assert small < 1 << 20
+    assert rz.workspace_size(rz.RZ_OP_IS_LOSS, 10, 0, 0, 256) >= 256 * 24
+    assert rz.workspace_size(99, 10, 10, 10, 10) == 0
+
+
+def test_host_side_argument_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails validation first
+    null = None
+    # B % G != 0
+    assert lib.rz_group_advantage(fake, 10, 4, fake, null) == 1
+    assert lib.rz_group_advantage(fake, 8, 0, fake, null) == 1
+    # d not a multiple of 8
+    assert lib.rz_token_logprob(fake, fake, fake, 5, 12, 100, fake, null, fake, 1 << 20,
+                                null, null) == 2
+    # missing pointers
+    assert lib.rz_token_logprob(null, fake, fake, 5, 16, 100, fake, null, fake, 1 << 20,
+                                null, null) == 1
+    # V out of range
+    assert lib.rz_token_logprob(fake, fake, fake, 5, 16, 0, fake, null, fake, 1 << 20,
+                                null, null) == 1
+    # misaligned H
+    assert lib.rz_token_logprob(P((1 << 20) + 2), fake, fake, 5, 16, 100, fake, null, fake,
+                                1 << 20, null, null) == 2
+    # workspace too small / missing
+    assert lib.rz_token_logprob(fake, fake, fake, 5, 16, 100, fake, null, fake, 8,
+                                null, null) == 3
+    assert lib.rz_token_logprob(fake, fake, fake, 5, 16, 100, fake, null, null, 1 << 30,
+                                null, null) == 3
+    # B = 0 with tokens
+    assert lib.rz_loss_fwd_bwd(fake, fake, fake, fake, fake, fake, 0, 5, 16, 100, fake, fake,
+                               null, fake, fake, fake, 1 << 30, null, null) == 1
+    # logits variant needs V % 8 == 0
+    assert lib.rz_logits_loss_fwd_bwd(fake, fake, fake, fake, fake, 2, 10, 100, fake, fake,
+                                      fake, fake, 1 << 20, null, null) == 2
+    # is_loss: missing outputs
+    assert lib.rz_is_loss(fake, fake, fake, fake, 2, 10, null, fake, null, fake, 1 << 20,
+                          null, null) == 1
+    assert lib.rz_d3(fake, fake, -1, fake, null) == 1
+
+
+def test_valid_call_without_gpu_reports_unsupported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    fake = ctypes.c_void_p(1 << 20)
+    # valid arguments, but no sm_103 device: refused, nothing launched
+    assert lib.rz_d3(fake, fake, 10, fake, None) == 2

@@ -1,0 +1,175 @@
+"""GPU-vs-oracle parity through the C ABI (small and mid sizes, ragged tails,
+several tiles), plus the tensor-core GEMM against a plain fp32 matmul."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_logprobs_gb300 import synth
+from helpers import (TOL_GRAD_REL_L2, TOL_LOGPI, f64, rel_l2, scalar_close)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _rand_bf16(shape, std, g):
+    return (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("T,d,V", [(300, 256, 1000), (1, 64, 256), (129, 2048, 513),
+                                   (520, 1536, 4096), (257, 136, 300)])
+def test_lmhead_logits_matches_fp32_matmul(rz, T, d, V):
+    g = torch.Generator().manual_seed(T * 7 + d + V)
+    H = _rand_bf16((T, d), 1.0, g)
+    W = _rand_bf16((V, d), 0.05, g)
+    z = rz.rz_lmhead_logits(H.to(DEV), W.to(DEV))
+    torch.cuda.synchronize()
+    ref = H.double() @ W.double().T
+    err = (z.cpu().double() - ref).abs().max().item()
+    scale = (H.double().abs() @ W.double().abs().T).max().item()
+    assert err <= 1e-5 * scale, (err, scale)
+
+
+def _tiny_inputs(wl, device="cpu"):
+    b = synth.make_batch(wl, device=device)
+    logmu64, _ = oracle.token_logprob(f64(b["H"]), f64(b["W_mu"]), f64(b["tokens"]))
+    b["logmu"] = torch.tensor(logmu64, dtype=torch.float32)
+    b["adv"] = torch.tensor(oracle.group_advantage(f64(b["rewards"]), b["G"]),
+                            dtype=torch.float32)
+    return b
+
+
+def _run_learner(rz, b):
+    out = rz.rz_loss_fwd_bwd(b["H"].to(DEV), b["W"].to(DEV), b["tokens"].to(DEV),
+                             b["logmu"].to(DEV), b["cu"].to(DEV), b["adv"].to(DEV))
+    torch.cuda.synchronize()
+    return out
+
+
+def _check_learner(out, ref):
+    lp = f64(out["logprob"])
+    assert np.max(np.abs(lp - ref["logpi"])) <= TOL_LOGPI
+    loss = float(out["loss"].item())
+    d3 = float(out["d3"].item())
+    assert scalar_close(loss, ref["loss"]), (loss, ref["loss"])
+    assert scalar_close(d3, ref["d3"]), (d3, ref["d3"])
+    e_dh = rel_l2(f64(out["dH"]), ref["dH"])
+    e_dw = rel_l2(f64(out["dW"]), ref["dW"])
+    assert e_dh <= TOL_GRAD_REL_L2, e_dh
+    assert e_dw <= TOL_GRAD_REL_L2, e_dw
+    return e_dh, e_dw
+
+
+def test_token_logprob_tiny_vs_oracle(rz):
+    b = _tiny_inputs(synth.WORKLOADS["tiny"])
+    lp, lse = rz.rz_token_logprob(b["H"].to(DEV), b["W"].to(DEV), b["tokens"].to(DEV),
+                                  lse_out=torch.empty(b["T"], device=DEV))
+    torch.cuda.synchronize()
+    ref_lp, ref_lse = oracle.token_logprob(f64(b["H"]), f64(b["W"]), f64(b["tokens"]))
+    assert np.max(np.abs(f64(lp) - ref_lp)) <= TOL_LOGPI
+    assert np.max(np.abs(f64(lse) - ref_lse)) <= TOL_LOGPI
+    # much tighter in practice: fp32 accumulation of exact bf16 products
+    assert np.max(np.abs(f64(lp) - ref_lp)) <= 1e-4
+
+
+@pytest.mark.parametrize("V", [1024, 151936, 1000])
+def test_zero_weights_give_minus_log_v(rz, V):
+    T, d = 77, 64
+    H = torch.randn(T, d).to(torch.bfloat16).to(DEV)
+    W = torch.zeros(V, d, dtype=torch.bfloat16, device=DEV)
+    tok = torch.randint(0, V, (T,), dtype=torch.int32, device=DEV)
+    lp, _ = rz.rz_token_logprob(H, W, tok)
+    want = np.float32(-np.log(V))
+    got = lp.cpu().numpy()
+    ulp = np.spacing(np.abs(want))
+    assert np.all(np.abs(got - want) <= 2 * ulp), (got[:4], want)
+
+
+def test_learner_tiny_vs_oracle(rz):
+    b = _tiny_inputs(synth.WORKLOADS["tiny"])
+    out = _run_learner(rz, b)
+    ref = oracle.loss_fwd_bwd(f64(b["H"]), f64(b["W"]), f64(b["tokens"]), f64(b["logmu"]),
+                              f64(b["cu"]), f64(b["adv"]))
+    _check_learner(out, ref)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n_prompts=3, group=4, len_lo=1, len_hi=200, d=512, V=5000),      # ragged V tail
+    dict(n_prompts=2, group=8, len_lo=60, len_hi=90, d=1536, V=2304),     # d = 6 N-tiles
+    dict(n_prompts=1, group=5, len_lo=0, len_hi=40, d=200, V=777),        # empty responses, d % 64
+])
+def test_learner_midsize_vs_oracle(rz, shape):
+    wl = synth.Workload("mid", shape["n_prompts"], shape["group"], shape["len_lo"],
+                        shape["len_hi"], shape["d"], shape["V"], "bernoulli", 0.5, "uniform",
+                        4, 2e-3, 4242)
+    b = _tiny_inputs(wl)
+    out = _run_learner(rz, b)
+    ref = oracle.loss_fwd_bwd(f64(b["H"]), f64(b["W"]), f64(b["tokens"]), f64(b["logmu"]),
+                              f64(b["cu"]), f64(b["adv"]))
+    _check_learner(out, ref)
+
+
+def test_learner_multi_chunk_vs_oracle(rz):
+    # more rows than one backward chunk (38912): exercises chunked dz and the
+    # fixed-order dW accumulation over chunks.
+    wl = synth.Workload("chunks", 1, 3, 15000, 16000, 64, 384, "uniform", 0.0, "uniform",
+                        4, 3e-2, 777)
+    b = _tiny_inputs(wl)
+    assert b["T"] > 38912
+    out = _run_learner(rz, b)
+    ref = oracle.loss_fwd_bwd(f64(b["H"]), f64(b["W"]), f64(b["tokens"]), f64(b["logmu"]),
+                              f64(b["cu"]), f64(b["adv"]))
+    _check_learner(out, ref)
+
+
+def test_group_advantage_vs_oracle(rz):
+    g = torch.Generator().manual_seed(5)
+    for B, G, kind in [(256, 8, "bern"), (128, 8, "unif"), (12, 3, "unif"), (7, 1, "unif")]:
+        r = (torch.rand(B, generator=g) < 0.4).float() if kind == "bern" else torch.rand(B, generator=g)
+        A = rz.rz_group_advantage(r.to(DEV), G)
+        torch.cuda.synchronize()
+        ref = oracle.group_advantage(f64(r), G)
+        np.testing.assert_allclose(f64(A), ref, atol=1e-7)
+        if kind == "bern" and G in (1, 2, 4, 8):
+            assert np.all(f64(A).reshape(-1, G).sum(1) == 0.0)
+
+
+@pytest.mark.parametrize("T,B,spread", [(1_114_112, 128, 0.08), (5000, 256, 1.5), (3, 2, 0.0)])
+def test_is_loss_and_d3_vs_oracle(rz, T, B, spread):
+    g = torch.Generator().manual_seed(T + B)
+    cuts = torch.sort(torch.randint(0, T + 1, (B - 1,), generator=g)).values
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64), cuts, torch.full((1,), T, dtype=torch.int64)])
+    logpi = -torch.rand(T, generator=g) * 12
+    logmu = logpi + torch.randn(T, generator=g) * spread
+    adv = torch.randn(B, generator=g)
+    loss, d3, coef = rz.rz_is_loss(logpi.to(DEV), logmu.to(DEV), cu.to(DEV), adv.to(DEV),
+                                   coef_out=torch.empty(T, device=DEV))
+    d3b = rz.rz_d3(logpi.to(DEV), logmu.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.is_loss(f64(logpi), f64(logmu), f64(cu), f64(adv))
+    assert scalar_close(loss.item(), ref["loss"]), (loss.item(), ref["loss"])
+    assert scalar_close(d3.item(), ref["d3"]), (d3.item(), ref["d3"])
+    assert scalar_close(d3b.item(), ref["d3"]), (d3b.item(), ref["d3"])
+    np.testing.assert_allclose(f64(coef), ref["c"], rtol=1e-5, atol=1e-12)
+
+
+@pytest.mark.parametrize("T,V,B", [(600, 1024, 6), (1030, 151936, 4), (5, 8, 5)])
+def test_logits_variant_vs_oracle(rz, T, V, B):
+    g = torch.Generator().manual_seed(T + V)
+    logits = (torch.randn(T, V, generator=g) * 3.0).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    cu = torch.linspace(0, T, B + 1).round().to(torch.int64)
+    adv = torch.randn(B, generator=g)
+    lp64 = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), np.zeros(T), f64(cu), f64(adv))["logpi"]
+    logmu = torch.tensor(lp64, dtype=torch.float32) + torch.randn(T, generator=g) * 0.05
+    rows = np.unique(np.concatenate([np.arange(min(T, 8)), np.random.default_rng(0).integers(0, T, 32)]))
+    ref = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), f64(logmu), f64(cu), f64(adv), rows=rows)
+    buf = logits.to(DEV)
+    out = rz.rz_logits_loss_fwd_bwd(buf, tok.to(DEV), logmu.to(DEV), cu.to(DEV), adv.to(DEV))
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(out["logprob"]) - ref["logpi"])) <= TOL_LOGPI
+    assert scalar_close(out["loss"].item(), ref["loss"]), (out["loss"].item(), ref["loss"])
+    assert scalar_close(out["d3"].item(), ref["d3"]), (out["d3"].item(), ref["d3"])
+    dz = f64(buf[torch.as_tensor(rows, device=DEV)])
+    assert rel_l2(dz, ref["dz"]) <= TOL_GRAD_REL_L2
