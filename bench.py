@@ -442,6 +442,39 @@ def run_reference(args):
     return 0
 
 
+def run_profile(args):
+    """Small fixed cases for ncu captures (not a benchmark): one rollout
+    logprob call, then `--steps` learner steps (or given-logits steps) on
+    `--rows` tokens of the workload's d and V."""
+    import dataclasses
+    import torch
+    import invariant_logprobs_gb300 as rz
+    from invariant_logprobs_gb300 import synth
+    rz.load()
+    dev = torch.device("cuda", 0)
+    if args.profile == "logits":
+        wl = synth.WORKLOADS["moe30b_logits"]
+        b = synth.make_logits_batch(wl, device=dev, T=args.rows)
+        logmu = torch.full((b["T"],), -12.0, device=dev)
+        adv = rz.rz_group_advantage(b["rewards"], b["G"])
+        for _ in range(args.steps):
+            rz.rz_logits_loss_fwd_bwd(b["logits"], b["tokens"], logmu, b["cu"], adv)
+        torch.cuda.synchronize()
+        print("profile logits rows=%d ok" % b["T"])
+        return 0
+    wl = synth.WORKLOADS[args.config]
+    per = max(1, args.rows // wl.B)
+    wl = dataclasses.replace(wl, len_lo=per, len_hi=per, tokens="uniform")
+    b = synth.make_batch(wl, device=dev)
+    logmu, _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
+    adv = rz.rz_group_advantage(b["rewards"], b["G"])
+    for _ in range(args.steps):
+        rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv)
+    torch.cuda.synchronize()
+    print("profile learner rows=%d ok" % b["T"])
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,7 +485,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["learner", "logits"], default=None,
+                    help="small fixed case for ncu captures (no timing output)")
+    ap.add_argument("--rows", type=int, default=16384)
     args = ap.parse_args()
+    if args.profile:
+        return run_profile(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

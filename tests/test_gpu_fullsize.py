@@ -1,0 +1,87 @@
+"""Full-size parity at the benchmark's shapes and launch configuration
+(1.5B-shaped lag-2 and 4B-shaped lag-64 learner batches, ~1.1M tokens,
+V = 151936), checked on sampled rows the oracle computes one by one and on
+identities that hold at any size:
+
+  * log pi of 64 sampled rows vs the oracle;
+  * dH of the sampled rows vs the oracle's dz_t W (dz from the oracle's own
+    softmax of the row, the recorded log mu, A_i, B and T_i);
+  * <dW, W> == <dH, H> (both equal sum_t sum_v dz_tv z_tv), tying dW to the
+    row-checked dH;
+  * the loss/D3 of the fused call equal rz_is_loss on its own log pi bit for
+    bit, and D3 >= 0.
+
+log mu comes from torch's bf16 matmul + log_softmax with the lagged weights
+(the behaviour policy of the workload), never from this library.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_logprobs_gb300 import synth
+from helpers import TOL_GRAD_REL_L2, TOL_LOGPI, bits, f64, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _behaviour_logprob(H, W_mu, tokens, chunk=4096):
+    out = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
+    for s in range(0, H.shape[0], chunk):
+        e = min(H.shape[0], s + chunk)
+        z = torch.log_softmax((H[s:e] @ W_mu.t()).float(), dim=-1)
+        out[s:e] = z.gather(1, tokens[s:e].long()[:, None])[:, 0]
+    return out
+
+
+@pytest.mark.parametrize("name", ["qwen1p5b_lag2", "qwen4b_lag64"])
+def test_learner_full_size_sampled(rz, name):
+    wl = synth.WORKLOADS[name]
+    b = synth.make_batch(wl, device=DEV)
+    T, d, V, B = b["T"], b["d"], b["V"], b["B"]
+    logmu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
+    adv = rz.rz_group_advantage(b["rewards"], b["G"])
+    err = rz.new_err_flag(DEV)
+    out = rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv, err_flag=err)
+    loss2, d32, _ = rz.rz_is_loss(out["logprob"], logmu, b["cu"], adv)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(bits(loss2), bits(out["loss"]))
+    assert np.array_equal(bits(d32), bits(out["d3"]))
+    assert out["d3"].item() >= 0.0
+
+    rng = np.random.default_rng(123)
+    rows = np.sort(rng.choice(T, 64, replace=False))
+    rows[0] = 0
+    rows[-1] = T - 1
+    r_t = torch.as_tensor(rows, device=DEV)
+    Hs = f64(b["H"][r_t])
+    Wd = f64(b["W"])
+    tok = f64(b["tokens"][r_t])
+    lp_ref, lse_ref = oracle.token_logprob_rows(Hs, Wd, tok, np.arange(64))
+    lp_got = f64(out["logprob"][r_t])
+    assert np.max(np.abs(lp_got - lp_ref)) <= TOL_LOGPI
+
+    # dH rows: dz_t = c_t (softmax(z_t) - onehot(a_t)), c_t = A_i w_t / (B T_i)
+    cu = f64(b["cu"])
+    seg = np.searchsorted(cu, rows, side="right") - 1
+    Ti = cu[seg + 1] - cu[seg]
+    A = f64(adv)[seg]
+    w = np.exp(lp_ref - f64(logmu[r_t]))
+    c = A * w / (B * Ti)
+    z = Hs @ Wd.T
+    p = np.exp(z - lse_ref[:, None])
+    p[np.arange(64), tok] -= 1.0
+    dH_ref = (c[:, None] * p) @ Wd
+    assert rel_l2(f64(out["dH"][r_t]), dH_ref) <= TOL_GRAD_REL_L2
+
+    # <dW, W> == <dH, H>
+    lhs = float((out["dW"].double() * b["W"].double()).sum())
+    rhs = float((out["dH"].double() * b["H"].double()).sum())
+    assert abs(lhs - rhs) <= 2e-2 * max(abs(lhs), abs(rhs)), (lhs, rhs)
+    # sum over the vocabulary of dW is ~0 (each dz row sums to zero)
+    dW64 = out["dW"].double()
+    colsum = dW64.sum(0)
+    assert float(colsum.norm()) <= 1e-3 * float(dW64.abs().sum(0).norm())
