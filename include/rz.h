@@ -66,6 +66,7 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
 #define RZ_ERR_UNSUPPORTED  2  /* alignment, d % 8, no sm_103a device */
 #define RZ_ERR_WORKSPACE    3  /* ws == NULL or ws_bytes too small */
 #define RZ_ERR_CUDA         4  /* a CUDA runtime/driver call failed */
+#define RZ_ERR_TOO_LARGE    5  /* exceeds the built-in scratch of rz_token_logprob_noalloc */
 
 /* Bits OR-ed into *err_flag by device code. */
 #define RZ_DEVERR_TOKEN_RANGE  1  /* a token id outside [0, V) */
@@ -183,6 +184,36 @@ RZ_API int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens,
 RZ_API int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32_t d,
                      int32_t V, float* logits_out, int32_t* err_flag,
                      rz_stream_t stream);
+
+/*
+ * rz_token_logprob without a caller workspace, for callers that cannot
+ * allocate device memory: a sampler hook inside an inference engine whose
+ * memory pool is reserved up front, a plug-in whose host owns every
+ * allocation, or code running between captured graph segments.  The pages
+ * have no counterpart for this entry point; it is a deployment convenience.
+ *
+ * Same arguments and results as rz_token_logprob (bitwise the same output:
+ * it runs the same kernels with the same launch shape), minus ws/ws_bytes.
+ * Scratch is a fixed array inside the library of rz_noalloc_scratch_bytes()
+ * bytes (8 MiB) on every GPU that loads the library, held until the process
+ * exits.  It needs T * (8 * S + 4) bytes plus padding, S = min(8, ceil(V/256))
+ * vocab splits -- about 123,000 rows at V = 151936; larger T returns
+ * RZ_ERR_TOO_LARGE and enqueues nothing.
+ *   - It never calls cudaMalloc/cudaFree or any allocating library routine.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - All calls on a device share the array, and it keeps the last call's
+ *     contents (nothing in it needs zeroing).  Calls that overlap on the GPU
+ *     (different streams, or threads without ordering) race on it and give
+ *     undefined results: serialise them.
+ */
+RZ_API int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                                    int64_t T, int32_t d, int32_t V,
+                                    float* logprob_out, float* lse_out,
+                                    int32_t* err_flag, rz_stream_t stream);
+
+/* Size in bytes of the built-in scratch used by rz_token_logprob_noalloc. */
+RZ_API size_t rz_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 }

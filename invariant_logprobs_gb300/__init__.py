@@ -22,6 +22,7 @@ RZ_ERR_INVALID_ARG = 1
 RZ_ERR_UNSUPPORTED = 2
 RZ_ERR_WORKSPACE = 3
 RZ_ERR_CUDA = 4
+RZ_ERR_TOO_LARGE = 5
 
 RZ_DEVERR_TOKEN_RANGE = 1
 RZ_DEVERR_CU_SEQLENS = 2
@@ -51,6 +52,8 @@ _SIGNATURES = {
     "rz_logits_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32,
                                               _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_lmhead_logits": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
+    "rz_token_logprob_noalloc": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _P]),
+    "rz_noalloc_scratch_bytes": (_SZ, []),
 }
 
 
@@ -270,3 +273,29 @@ def rz_lmhead_logits(H, W, logits_out=None, err_flag=None, stream=None):
                               _stream(stream))
     _check("rz_lmhead_logits", st)
     return logits_out
+
+
+def rz_token_logprob_noalloc(H, W, tokens, logprob_out, lse_out=None, err_flag=None,
+                             stream=None):
+    """rz_token_logprob for callers that cannot allocate device memory: the
+    library's built-in scratch replaces the workspace, and nothing is
+    allocated here either -- the caller passes the output buffers.  See
+    include/rz.h for the size limit, first-call set-up and the rule that
+    overlapping calls race."""
+    torch = _torch()
+    lib = load()
+    _need(H, torch.bfloat16, "H")
+    _need(W, torch.bfloat16, "W")
+    _need(tokens, torch.int32, "tokens")
+    _need(logprob_out, torch.float32, "logprob_out")
+    T, d = H.shape
+    V = W.shape[0]
+    st = lib.rz_token_logprob_noalloc(_ptr(H), _ptr(W), _ptr(tokens), T, d, V,
+                                      _ptr(logprob_out), _ptr(lse_out), _ptr(err_flag),
+                                      _stream(stream))
+    _check("rz_token_logprob_noalloc", st)
+    return logprob_out, lse_out
+
+
+def noalloc_scratch_bytes():
+    return int(load().rz_noalloc_scratch_bytes())

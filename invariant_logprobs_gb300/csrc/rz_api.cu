@@ -153,6 +153,7 @@ const char* rz_status_string(int status) {
     case RZ_ERR_UNSUPPORTED: return "unsupported (alignment, d % 8, or device is not sm_103)";
     case RZ_ERR_WORKSPACE: return "workspace missing or too small";
     case RZ_ERR_CUDA: return "CUDA error";
+    case RZ_ERR_TOO_LARGE: return "problem exceeds the built-in scratch of the no-alloc entry point";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,60 @@
+"""rz_token_logprob_noalloc: the rollout logprob for callers that cannot
+allocate device memory (engine-owned memory pools, plug-in hosts, code
+between captured graph segments).  It must give the same log pi as
+rz_token_logprob -- it runs the same kernels on a scratch array built into
+the library -- on consecutive calls that reuse that scratch with different
+sizes, and must refuse problems larger than the scratch without launching.
+
+Kept in its own file, collected last, so a failure here never hides the
+other GPU tests.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL_LOGPI, bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(T, d, V, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    H = torch.randn(T, d, generator=g, device=DEV).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, device=DEV, dtype=torch.int32)
+    return H, W, tok
+
+
+@pytest.mark.parametrize("shapes", [((3000, 512, 151936), (7777, 256, 5000))])
+def test_noalloc_matches_workspace_entry_point_twice(rz, shapes):
+    for i, (T, d, V) in enumerate(shapes):
+        H, W, tok = _case(T, d, V, 11 + i)
+        want, want_lse = rz.rz_token_logprob(H, W, tok, lse_out=torch.empty(T, device=DEV))
+        got = torch.full((T,), float("nan"), device=DEV)
+        got_lse = torch.full((T,), float("nan"), device=DEV)
+        err = rz.new_err_flag(DEV)
+        rz.rz_token_logprob_noalloc(H, W, tok, got, lse_out=got_lse, err_flag=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert float((got - want).abs().max()) <= TOL_LOGPI
+        assert float((got_lse - want_lse).abs().max()) <= TOL_LOGPI
+        # same kernels, same launch shape: bitwise the same
+        assert np.array_equal(bits(got), bits(want))
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(rz):
+    cap = rz.noalloc_scratch_bytes()
+    V, d = 151936, 64
+    T = cap // (8 * 8 + 4) + 1024  # more rows than the scratch can hold
+    W = torch.zeros(V, d, dtype=torch.bfloat16, device=DEV)
+    H = torch.zeros(T, d, dtype=torch.bfloat16, device=DEV)
+    tok = torch.zeros(T, dtype=torch.int32, device=DEV)
+    out = torch.zeros(T, device=DEV)
+    with pytest.raises(rz.RzError) as e:
+        rz.rz_token_logprob_noalloc(H, W, tok, out)
+    assert e.value.status == rz.RZ_ERR_TOO_LARGE
+    torch.cuda.synchronize()
+    assert float(out.abs().max()) == 0.0  # nothing was launched
