@@ -1,0 +1,89 @@
+"""Data-parallel sharding of the learner step over responses, checked on CPU
+with two gloo ranks: each rank runs the oracle on its own responses with
+advantages rescaled to the global batch, the ranks sum dW and the two
+scalars, and the result must equal the unsharded step."""
+
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import oracle
+from invariant_logprobs_gb300 import shard
+
+
+def _problem(seed=3):
+    rng = np.random.default_rng(seed)
+    B, d, V = 10, 6, 17
+    L = rng.integers(0, 9, B)
+    cu = np.concatenate([[0], np.cumsum(L)]).astype(np.int64)
+    T = int(cu[-1])
+    H = rng.standard_normal((T, d))
+    W = rng.standard_normal((V, d)) * 0.5
+    tok = rng.integers(0, V, T)
+    lm = oracle.token_logprob(H, W + rng.standard_normal((V, d)) * 0.1, tok)[0]
+    A = oracle.group_advantage(rng.random(B), 5)
+    return H, W, tok, lm, cu, A
+
+
+def test_plan_covers_all_responses_in_order():
+    cu = np.array([0, 5, 5, 9, 30, 31, 40])
+    for world in (1, 2, 3, 4, 8):
+        p = shard.plan(cu, world)
+        assert p[0][0] == 0 and p[-1][1] == 6
+        assert all(p[i][1] == p[i + 1][0] for i in range(world - 1))
+        assert all(a <= b for a, b in p)
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out_dir):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    H, W, tok, lm, cu, A = _problem()
+    B = A.shape[0]
+    r0, r1 = shard.plan(cu, world)[rank]
+    t0, t1, cu_l = shard.local_batch(cu, (r0, r1))
+    Bl = r1 - r0
+    A_l = A[r0:r1] * shard.advantage_scale(Bl, B)
+    if Bl > 0:
+        res = oracle.loss_fwd_bwd(H[t0:t1], W, tok[t0:t1], lm[t0:t1], cu_l, A_l)
+        loss, d3, dW = res["loss"], res["d3"], res["dW"]
+        dH = res["dH"]
+    else:
+        loss, d3, dW, dH = 0.0, 0.0, np.zeros_like(W), np.zeros((0, W.shape[1]))
+    dW_t = torch.tensor(dW)
+    dist.all_reduce(dW_t)
+    scal = [None] * world
+    dist.all_gather_object(scal, (loss, d3, t1 - t0))
+    g_loss, g_d3 = shard.combine_scalars([s[0] for s in scal], [s[1] for s in scal],
+                                         [s[2] for s in scal])
+    np.save(os.path.join(out_dir, "dH_%d.npy" % rank), dH)
+    if rank == 0:
+        np.save(os.path.join(out_dir, "dW.npy"), dW_t.numpy())
+        np.save(os.path.join(out_dir, "scalars.npy"), np.array([g_loss, g_d3]))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2])
+def test_two_rank_gloo_shard_equals_unsharded(tmp_path, world):
+    mp.spawn(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    H, W, tok, lm, cu, A = _problem()
+    ref = oracle.loss_fwd_bwd(H, W, tok, lm, cu, A)
+    g_loss, g_d3 = np.load(tmp_path / "scalars.npy")
+    assert g_loss == pytest.approx(ref["loss"], abs=1e-13)
+    assert g_d3 == pytest.approx(ref["d3"], abs=1e-13)
+    np.testing.assert_allclose(np.load(tmp_path / "dW.npy"), ref["dW"], atol=1e-13)
+    dH = np.concatenate([np.load(tmp_path / ("dH_%d.npy" % r)) for r in range(world)])
+    np.testing.assert_allclose(dH, ref["dH"], atol=1e-13)
