@@ -50,6 +50,8 @@ struct GemmSched {
   int tiles_per_group;  // ceil(n_tiles / n_groups)
   int k_blocks;         // number of 64-deep K blocks
   int num_tasks;        // m_blocks * n_groups
+  int m_group;          // raster: m-blocks per group; inside a group tasks run
+                        // group-of-n-tiles major, m-block minor (1 = m-major)
   int a_m_off;          // added to the M coordinate of A loads
   int a_k_off;          // added to the K coordinate of MN-major A loads
   int b_k_off;          // added to the K coordinate of B loads
@@ -92,10 +94,20 @@ struct Operands {
   }
 };
 
+// Task -> (m-block, n-tile group).  Tasks come in groups of m_group m-blocks;
+// inside a group all m-blocks of n-group 0 come first, then n-group 1, ...,
+// so CTAs running at the same time share the same B tiles (the LM-head
+// weight) through L2.  The order never changes what a task computes.
 __device__ __forceinline__ void task_coords(const GemmSched& s, int task, int& m_blk, int& grp,
                                             int& n_begin, int& n_end) {
-  m_blk = task / s.n_groups;
-  grp = task - m_blk * s.n_groups;
+  const int G = s.m_group;
+  const int per = G * s.n_groups;
+  const int mg = task / per;
+  const int rem = task - mg * per;
+  const int full_groups = s.m_blocks / G;
+  const int Gl = mg < full_groups ? G : s.m_blocks - full_groups * G;
+  grp = rem / Gl;
+  m_blk = mg * G + (rem - grp * Gl);
   n_begin = grp * s.tiles_per_group;
   n_end = n_begin + s.tiles_per_group;
   if (n_end > s.n_tiles) n_end = s.n_tiles;

@@ -331,6 +331,13 @@ cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmSched
   return cudaGetLastError();
 }
 
+// m-blocks per raster group of the vocab-split GEMMs: half the SMs, so at
+// any time about two vocab splits are in flight, each shared by ~76 CTAs.
+int vocab_raster_group() {
+  const int g = num_sms() / 2;
+  return g > 0 ? g : 1;
+}
+
 GemmSched sched_of(long long m_rows, int n_cols, int n_groups, long long k_depth, int* err) {
   GemmSched s{};
   s.m_blocks = static_cast<int>((m_rows + kBM - 1) / kBM);
@@ -339,6 +346,7 @@ GemmSched sched_of(long long m_rows, int n_cols, int n_groups, long long k_depth
   s.tiles_per_group = (s.n_tiles + n_groups - 1) / n_groups;
   s.k_blocks = static_cast<int>((k_depth + kBK - 1) / kBK);
   s.num_tasks = s.m_blocks * n_groups;
+  s.m_group = 1;
   s.err = err;
   return s;
 }
@@ -351,6 +359,7 @@ cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, i
   const int S = vocab_splits(V);
   GemmSched s = sched_of(T, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
+  s.m_group = vocab_raster_group();
   EpiLsePartial::Params p{tokens, part, zgather, static_cast<long long>(T), V, S};
   return run_gemm<EpiLsePartial, false, false>(tmH, tmW, s, p, st);
 }
@@ -373,6 +382,7 @@ cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64
   const int S = vocab_splits(V);
   GemmSched s = sched_of(rows, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
+  s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
   EpiDlogits::Params p{tokens, lse2, coef, dz, ldz, row0, rows, V};
   return run_gemm<EpiDlogits, false, false>(tmH, tmW, s, p, st);
@@ -383,6 +393,7 @@ cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, in
   const int S = vocab_splits(V);
   GemmSched s = sched_of(T, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
+  s.m_group = vocab_raster_group();
   EpiStore<1>::Params p{out, V, 0, T, V, 0};
   return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
 }

@@ -64,18 +64,17 @@ def test_learner_full_size_sampled(rz, name):
     lp_got = f64(out["logprob"][r_t])
     assert np.max(np.abs(lp_got - lp_ref)) <= TOL_LOGPI
 
-    # dH rows: dz_t = c_t (softmax(z_t) - onehot(a_t)), c_t = A_i w_t / (B T_i)
+    # dH rows from the oracle: each sampled row becomes a one-token response
+    # whose advantage is rescaled so the oracle's c = A' w / (n * 1) equals
+    # the full batch's A_i w / (B T_i) (the loss is linear in A).
     cu = f64(b["cu"])
     seg = np.searchsorted(cu, rows, side="right") - 1
     Ti = cu[seg + 1] - cu[seg]
-    A = f64(adv)[seg]
-    w = np.exp(lp_ref - f64(logmu[r_t]))
-    c = A * w / (B * Ti)
-    z = Hs @ Wd.T
-    p = np.exp(z - lse_ref[:, None])
-    p[np.arange(64), tok] -= 1.0
-    dH_ref = (c[:, None] * p) @ Wd
-    assert rel_l2(f64(out["dH"][r_t]), dH_ref) <= TOL_GRAD_REL_L2
+    n = rows.shape[0]
+    A_rows = f64(adv)[seg] * n / (B * Ti)
+    sub = oracle.loss_fwd_bwd(Hs, Wd, tok, f64(logmu[r_t]), np.arange(n + 1), A_rows)
+    assert np.max(np.abs(sub["logpi"] - lp_ref)) <= 1e-12
+    assert rel_l2(f64(out["dH"][r_t]), sub["dH"]) <= TOL_GRAD_REL_L2
 
     # <dW, W> == <dH, H>
     lhs = float((out["dW"].double() * b["W"].double()).sum())
@@ -85,3 +84,38 @@ def test_learner_full_size_sampled(rz, name):
     dW64 = out["dW"].double()
     colsum = dW64.sum(0)
     assert float(colsum.norm()) <= 1e-3 * float(dW64.abs().sum(0).norm())
+
+
+def test_logits_variant_full_size_sampled(rz):
+    wl = synth.WORKLOADS["moe30b_logits"]
+    b = synth.make_logits_batch(wl, device=DEV)
+    T, V, B = b["T"], b["V"], b["B"]
+    rng = np.random.default_rng(321)
+    rows = np.sort(rng.choice(T, 64, replace=False))
+    rows[0], rows[-1] = 0, T - 1
+    r_t = torch.as_tensor(rows, device=DEV)
+    z_rows = f64(b["logits"][r_t])             # keep: the call overwrites logits
+    logpi = torch.empty(T, dtype=torch.float32, device=DEV)
+    for s0 in range(0, T, 8192):
+        e = min(T, s0 + 8192)
+        zz = torch.log_softmax(b["logits"][s0:e].float(), dim=-1)
+        logpi[s0:e] = zz.gather(1, b["tokens"][s0:e].long()[:, None])[:, 0]
+        del zz
+    logmu = synth.logmu_near(logpi, synth.LOGMU_NOISE_STD, b["gen"])
+    adv = rz.rz_group_advantage(b["rewards"], b["G"])
+    err = rz.new_err_flag(DEV)
+    out = rz.rz_logits_loss_fwd_bwd(b["logits"], b["tokens"], logmu, b["cu"], adv, err_flag=err)
+    loss2, d32, _ = rz.rz_is_loss(out["logprob"], logmu, b["cu"], adv)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(bits(loss2), bits(out["loss"]))
+    assert np.array_equal(bits(d32), bits(out["d3"]))
+    cu = f64(b["cu"])
+    seg = np.searchsorted(cu, rows, side="right") - 1
+    Ti = cu[seg + 1] - cu[seg]
+    n = rows.shape[0]
+    A_rows = f64(adv)[seg] * n / (B * Ti)
+    ref = oracle.logits_loss_fwd_bwd(z_rows, f64(b["tokens"][r_t]), f64(logmu[r_t]),
+                                     np.arange(n + 1), A_rows)
+    assert np.max(np.abs(f64(out["logprob"][r_t]) - ref["logpi"])) <= TOL_LOGPI
+    assert rel_l2(f64(b["logits"][r_t]), ref["dz"]) <= TOL_GRAD_REL_L2
