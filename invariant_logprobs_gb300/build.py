@@ -16,8 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librz.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
-              "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
+              "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]
 
 
 def _nvcc():

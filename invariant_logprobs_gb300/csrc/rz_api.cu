@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/rz.h"
+#include "rz.h"
 #include "rz_internal.h"
 
 namespace rz {

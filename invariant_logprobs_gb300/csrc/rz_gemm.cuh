@@ -41,7 +41,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kErrTimeout = 4;                    // RZ_DEVERR_TIMEOUT
 
 constexpr uint32_t kSmemRing = kStages * (kTileABytes + kTileBBytes);
-constexpr uint32_t kSmemBytes = kSmemRing + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint32_t kEpiStageBytes = 32 * 128;  // per epilogue warp: 32 rows x 128 B
+constexpr uint32_t kSmemBytes =
+    kSmemRing + 1024 /*align*/ + 256 /*barriers*/ + 4 * kEpiStageBytes;
 
 struct GemmSched {
   int m_blocks;         // number of 128-row blocks
@@ -121,10 +123,12 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, int* err) {
 // Epi must provide:
 //   struct Params;  struct State;
 //   static void task_begin(const Params&, State&, int m_blk, int grp, int row);
-//   static void tile(const Params&, State&, int m_blk, int n_tile, uint32_t taddr, int row);
+//   static void tile(const Params&, State&, int m_blk, int n_tile, uint32_t taddr, int row,
+//                    uint8_t* stage);
 //   static void task_end(const Params&, State&, int m_blk, int grp, int row);
 // `row` is the thread's row inside the 128-row block; `taddr` the TMEM
-// address of (this warp's 32 lanes, column 0) of the tile's accumulator.
+// address of (this warp's 32 lanes, column 0) of the tile's accumulator;
+// `stage` a private 4 KB shared-memory buffer of the warp (128 B per row).
 template <class Epi, bool kAMN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* issued_ring = reinterpret_cast<int*>(tmem_slot + 2);  // [0] issued, [1] consumed
+  uint8_t* epi_stage = smem + kSmemRing + 256;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -284,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        Epi::tile(ep, st, m_blk, n, lane_addr + buf * kBN, row);
+        Epi::tile(ep, st, m_blk, n, lane_addr + buf * kBN, row,
+                  epi_stage + (warp - 2) * kEpiStageBytes);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);

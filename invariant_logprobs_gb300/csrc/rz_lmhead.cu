@@ -92,7 +92,7 @@ struct EpiLsePartial {
   }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, int, int n_tile,
-                                              uint32_t taddr, int) {
+                                              uint32_t taddr, int, uint8_t*) {
     const int col0 = n_tile * kBN;
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 64) {
@@ -149,9 +149,9 @@ struct EpiDlogits {
     }
   }
 
-  static __device__ __forceinline__ void chunk(const Params& p, const State& st,
-                                               const uint32_t (&r)[32], int cbase,
-                                               uint16_t* out_row) {
+  // 32 columns of this thread's row -> 16 packed bf16 pairs.
+  static __device__ __forceinline__ void chunk(const State& st, const uint32_t (&r)[32],
+                                               int cbase, uint32_t* w) {
     float g[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
@@ -162,39 +162,55 @@ struct EpiDlogits {
       for (int j = 0; j < 32; ++j)
         if (rel == static_cast<unsigned>(j)) g[j] -= st.c;
     }
-    if (!st.valid) return;
-    if (cbase + 32 <= p.V) {
-      uint32_t w[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
-      uint16_t* dst = out_row + cbase;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_global_v4(dst + 8 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (cbase + j < p.V) {
-          const uint32_t b = pack_bf16x2(g[j], 0.f);
-          out_row[cbase + j] = static_cast<uint16_t>(b & 0xffffu);
-        }
-    }
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
   }
 
+  // Each 64-column slab goes through the warp's shared-memory stage so that
+  // every global store instruction writes four whole 128-byte lines (4 rows
+  // x 64 columns) instead of 32 scattered 16-byte pieces.  Staging layout:
+  // row r at r*128, 16-byte piece j at position j ^ (r & 7) (conflict-free
+  // both when each thread writes its row and when 8 threads read a row).
   static __device__ __forceinline__ void tile(const Params& p, State& st, int m_blk, int n_tile,
-                                              uint32_t taddr, int row) {
+                                              uint32_t taddr, int row, uint8_t* stage) {
     const int col0 = n_tile * kBN;
-    const long long r = static_cast<long long>(m_blk) * kBM + row;
-    uint16_t* out_row = p.dz + r * p.ldz;
+    const int lane = row & 31;
+    const long long rbase = static_cast<long long>(m_blk) * kBM + (row & ~31);
+    uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 64) {
-      if (col0 + c >= p.V) break;
+      if (col0 + c >= p.V) break;  // warp-uniform
       uint32_t r0[32], r1[32];
       tmem_ld32(taddr + c, r0);
       tmem_ld32(taddr + c + 32, r1);
       tmem_ld_wait();
-      chunk(p, st, r0, col0 + c, out_row);
-      if (col0 + c + 32 < p.V) chunk(p, st, r1, col0 + c + 32, out_row);
+      uint32_t w[32];
+      chunk(st, r0, col0 + c, w);
+      chunk(st, r1, col0 + c + 32, w + 16);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mine[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = 4 * k + (lane >> 3);
+        const int j = lane & 7;
+        const uint4 v = reinterpret_cast<const uint4*>(stage + r * 128)[j ^ (r & 7)];
+        const long long gr = rbase + r;
+        const int col = col0 + c + 8 * j;
+        if (gr < p.rows && col < p.V) {
+          uint16_t* dst = p.dz + gr * p.ldz + col;
+          if (col + 8 <= p.V) {
+            st_global_v4(dst, v.x, v.y, v.z, v.w);
+          } else {
+            for (int e = 0; col + e < p.V; ++e) {
+              const uint32_t word = e < 2 ? v.x : (e < 4 ? v.y : (e < 6 ? v.z : v.w));
+              dst[e] = static_cast<uint16_t>((word >> (16 * (e & 1))) & 0xffffu);
+            }
+          }
+        }
+      }
+      __syncwarp();
     }
   }
 
@@ -262,7 +278,7 @@ struct EpiStore {
   }
 
   static __device__ __forceinline__ void tile(const Params& p, State&, int m_blk, int n_tile,
-                                              uint32_t taddr, int row) {
+                                              uint32_t taddr, int row, uint8_t*) {
     const int col0 = n_tile * kBN;
     const long long rr = static_cast<long long>(m_blk) * kBM + row;
     const bool valid = rr < p.rows;

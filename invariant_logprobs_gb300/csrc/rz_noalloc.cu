@@ -23,7 +23,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/rz.h"
+#include "rz.h"
 #include "rz_internal.h"
 
 namespace rz {
