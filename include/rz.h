@@ -140,6 +140,30 @@ RZ_API int rz_d3(const float* logpi, const float* logmu, int64_t T, float* d3_ou
           rz_stream_t stream);
 
 /*
+ * Per-update importance-sampling diagnostics over the T sampled tokens
+ * (d_t = logpi_t - logmu_t, w_t = e^{d_t}), one fixed-order reduction:
+ *   stats_out[0] D3 = mean(w - 1 - log w)     [vLLM-zh s.3]; for tokens drawn
+ *                from mu this is also the "k3" estimator of KL(mu || pi)
+ *   stats_out[1] k1 = mean(-d), the plain estimator of KL(mu || pi)
+ *   stats_out[2] k2 = mean(d^2 / 2)
+ *   stats_out[3..6] mean w, max w, min w, max |d|
+ * The pages plot a "sampled rollout-to-learner KL" without defining it
+ * [RZ-page Figure 1]; k1 and k3 are the two readings offered.  stats_out is
+ * 7 device floats; all zero for T = 0.  No workspace.
+ */
+RZ_API int rz_is_stats(const float* logpi, const float* logmu, int64_t T, float* stats_out,
+                       rz_stream_t stream);
+
+/*
+ * Peak-to-median ratio max(x)/median(x) of a per-update series held in HOST
+ * memory (the pages report it for D3 across updates: 1.50x with aligned
+ * kernels vs 442.54x with standard kernels [vLLM-zh s.3 Figure 1]).  The
+ * median of an even count is the mean of the two middle values.  Pure host
+ * function; n >= 1.
+ */
+RZ_API int rz_peak_to_median(const float* series, int64_t n, double* ratio_out);
+
+/*
  * Learner side: the fused logprob + REINFORCE Zero loss, forward and backward
  * [RZ-page s.02 objective and "differentiate through the numerator"].
  *   H [T,d] bf16, W [V,d] bf16, tokens [T] int32, logmu [T] fp32 (recorded by

@@ -54,6 +54,8 @@ _SIGNATURES = {
     "rz_lmhead_logits": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
     "rz_token_logprob_noalloc": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _P]),
     "rz_noalloc_scratch_bytes": (_SZ, []),
+    "rz_is_stats": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+    "rz_peak_to_median": (ctypes.c_int, [_P, _I64, _P]),
 }
 
 
@@ -299,3 +301,30 @@ def rz_token_logprob_noalloc(H, W, tokens, logprob_out, lse_out=None, err_flag=N
 
 def noalloc_scratch_bytes():
     return int(load().rz_noalloc_scratch_bytes())
+
+
+IS_STATS_FIELDS = ("d3", "k1", "k2", "w_mean", "w_max", "w_min", "absd_max")
+
+
+def rz_is_stats(logpi, logmu, stats_out=None, stream=None):
+    """Per-update IS diagnostics (see include/rz.h): a [7] fp32 device tensor
+    in the order of IS_STATS_FIELDS."""
+    torch = _torch()
+    lib = load()
+    _need(logpi, torch.float32, "logpi")
+    _need(logmu, torch.float32, "logmu")
+    if stats_out is None:
+        stats_out = torch.empty(7, dtype=torch.float32, device=logpi.device)
+    _check("rz_is_stats", lib.rz_is_stats(_ptr(logpi), _ptr(logmu), logpi.shape[0],
+                                          _ptr(stats_out), _stream(stream)))
+    return stats_out
+
+
+def rz_peak_to_median(series):
+    """max/median of a host sequence of per-update values (host function)."""
+    import array
+    buf = (ctypes.c_float * len(series))(*[float(x) for x in series])
+    out = ctypes.c_double(0.0)
+    _check("rz_peak_to_median", load().rz_peak_to_median(
+        ctypes.cast(buf, ctypes.c_void_p), len(series), ctypes.byref(out)))
+    return out.value

@@ -6,9 +6,11 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "rz.h"
 #include "rz_internal.h"
@@ -216,6 +218,24 @@ int rz_d3(const float* logpi, const float* logmu, int64_t T, float* d3_out, rz_s
   if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   return cuda_status(launch_d3(logpi, logmu, T, d3_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int rz_is_stats(const float* logpi, const float* logmu, int64_t T, float* stats_out,
+                rz_stream_t stream) {
+  if (T < 0 || !stats_out) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  return cuda_status(
+      launch_is_stats(logpi, logmu, T, stats_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int rz_peak_to_median(const float* series, int64_t n, double* ratio_out) {
+  if (!series || !ratio_out || n <= 0) return RZ_ERR_INVALID_ARG;
+  std::vector<double> v(series, series + n);
+  std::sort(v.begin(), v.end());
+  const double med = (n % 2) ? v[n / 2] : 0.5 * (v[n / 2 - 1] + v[n / 2]);
+  *ratio_out = v.back() / med;
+  return RZ_OK;
 }
 
 int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, const float* logmu,

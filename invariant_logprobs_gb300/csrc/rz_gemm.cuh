@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One lane waits; the verdict is shared so the warp stays converged
         // for the .sync.aligned TMEM loads that follow.
         int got = 1;
-        if (lane == 0) got = mbar_wait(&tfull[buf], use & 1u, abort, kWaitLimitNs) ? 1 : 0;
+        if (lane == 0) got = mbar_wait<true>(&tfull[buf], use & 1u, abort, kWaitLimitNs) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           if (lane == 0) raise_abort(abort, sched.err);

@@ -63,6 +63,8 @@ cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t
                            float* coef, void* ws, int* err, cudaStream_t st);
 cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
                       cudaStream_t st);
+cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, float* out,
+                            cudaStream_t st);
 
 // ---- given-logits kernel (rz_logits.cu)
 cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,

@@ -101,6 +101,46 @@ __global__ void __launch_bounds__(kD3Threads)
   if (threadIdx.x == 0) *d3 = T > 0 ? static_cast<float>(tot / static_cast<double>(T)) : 0.f;
 }
 
+// Per-update diagnostics over all T tokens, one block, fixed order:
+// out = {D3 (= k3), k1 = mean(-d), k2 = mean(d^2/2), mean w, max w, min w,
+// max |d|}.
+__global__ void __launch_bounds__(kD3Threads)
+    is_stats_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu,
+                    long long T, float* out) {
+  __shared__ double red[kD3Threads / 32];
+  __shared__ float redf[kD3Threads / 32];
+  float s3 = 0.f, s1 = 0.f, s2 = 0.f, sw = 0.f;
+  float wmax = 0.f, wmin = INFINITY, dmax = 0.f;
+  for (long long t = threadIdx.x; t < T; t += kD3Threads) {
+    const float d = logpi[t] - logmu[t];
+    const float w = expf(d);
+    s3 += d3_term(d);
+    s1 -= d;
+    s2 += 0.5f * d * d;
+    sw += w;
+    wmax = fmaxf(wmax, w);
+    wmin = fminf(wmin, w);
+    dmax = fmaxf(dmax, fabsf(d));
+  }
+  const double t3 = block_sum<double, kD3Threads>(static_cast<double>(s3), red);
+  const double t1 = block_sum<double, kD3Threads>(static_cast<double>(s1), red);
+  const double t2 = block_sum<double, kD3Threads>(static_cast<double>(s2), red);
+  const double tw = block_sum<double, kD3Threads>(static_cast<double>(sw), red);
+  const float mx = block_extreme<kD3Threads, true>(wmax, redf);
+  const float mn = block_extreme<kD3Threads, false>(wmin, redf);
+  const float dm = block_extreme<kD3Threads, true>(dmax, redf);
+  if (threadIdx.x == 0) {
+    const double inv = T > 0 ? 1.0 / static_cast<double>(T) : 0.0;
+    out[0] = static_cast<float>(t3 * inv);
+    out[1] = static_cast<float>(t1 * inv);
+    out[2] = static_cast<float>(t2 * inv);
+    out[3] = static_cast<float>(tw * inv);
+    out[4] = T > 0 ? mx : 0.f;
+    out[5] = T > 0 ? mn : 0.f;
+    out[6] = T > 0 ? dm : 0.f;
+  }
+}
+
 __global__ void group_advantage_kernel(const float* __restrict__ r, int B, int G,
                                        float* __restrict__ adv) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -136,6 +176,12 @@ cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t
     if (e != cudaSuccess) return e;
   }
   is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, T, loss, d3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, float* out,
+                            cudaStream_t st) {
+  is_stats_kernel<<<1, kD3Threads, 0, st>>>(logpi, logmu, T, out);
   return cudaGetLastError();
 }
 

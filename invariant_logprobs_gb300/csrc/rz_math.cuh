@@ -52,6 +52,26 @@ __device__ __forceinline__ Tv block_sum(Tv v, Tv* scratch /* >= kThreadsPerBlock
   return tot;
 }
 
+// Block max / min (thread 0 holds the result).
+template <int kThreadsPerBlock, bool kMax>
+__device__ __forceinline__ float block_extreme(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = kMax ? fmaxf(v, u) : fminf(v, u);
+  }
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) scratch[warp] = v;
+  __syncthreads();
+  float r = scratch[0];
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kThreadsPerBlock / 32; ++w)
+      r = kMax ? fmaxf(r, scratch[w]) : fminf(r, scratch[w]);
+  }
+  __syncthreads();
+  return r;
+}
+
 // Merge two (max in log2 units, sum of 2^(x - max)) pairs.
 __device__ __forceinline__ void lse2_merge(float& m, float& s, float m_o, float s_o) {
   if (m_o > m) {

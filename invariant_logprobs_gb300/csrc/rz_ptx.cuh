@@ -50,15 +50,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// Same test, but the hardware may suspend the waiting thread until the phase
+// completes (or `hint_ns` pass) instead of letting it spin: for waits that
+// are long and off the critical path (the epilogue waiting for a tile).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Every pipeline wait is bounded: it gives up after `limit_ns` of wall time
 // (or as soon as another role raised *abort) and returns false.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (kSleep ? mbar_try_wait_sleep(a, parity, 100000u) : mbar_try_wait(a, parity))
+      return true;
     if ((it & 31u) == 0u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) return false;

@@ -107,3 +107,15 @@ def test_valid_call_without_gpu_reports_unsupported(lib):
     fake = ctypes.c_void_p(1 << 20)
     # valid arguments, but no sm_103 device: refused, nothing launched
     assert lib.rz_d3(fake, fake, 10, fake, None) == 2
+
+
+def test_peak_to_median_host_function(lib):
+    import numpy as np
+    import invariant_logprobs_gb300 as rz
+    import oracle
+    rng = np.random.default_rng(4)
+    for n in (1, 2, 7, 100):
+        x = (rng.random(n) + 0.1).astype(np.float32)
+        assert rz.rz_peak_to_median(list(x)) == pytest.approx(oracle.peak_to_median(x), rel=1e-12)
+    out = ctypes.c_double(0)
+    assert lib.rz_peak_to_median(None, 3, ctypes.byref(out)) == 1

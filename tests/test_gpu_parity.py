@@ -173,3 +173,22 @@ def test_logits_variant_vs_oracle(rz, T, V, B):
     assert scalar_close(out["d3"].item(), ref["d3"]), (out["d3"].item(), ref["d3"])
     dz = f64(buf[torch.as_tensor(rows, device=DEV)])
     assert rel_l2(dz, ref["dz"]) <= TOL_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("T,spread", [(1_114_112, 0.08), (777, 2.0), (1, 0.3)])
+def test_is_stats_vs_oracle(rz, T, spread):
+    g = torch.Generator().manual_seed(T)
+    logpi = -torch.rand(T, generator=g) * 12
+    logmu = logpi + torch.randn(T, generator=g) * spread
+    st = rz.rz_is_stats(logpi.to(DEV), logmu.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.is_stats(f64(logpi), f64(logmu))
+    got = dict(zip(rz.IS_STATS_FIELDS, st.cpu().double().tolist()))
+    for k in ("d3", "k1", "k2", "w_mean"):
+        assert scalar_close(got[k], ref[k]), (k, got[k], ref[k])
+    for k in ("w_max", "w_min", "absd_max"):
+        assert abs(got[k] - ref[k]) <= 1e-6 * max(1.0, abs(ref[k])), (k, got[k], ref[k])
+    # D3 of the diagnostics equals rz_d3 bit for bit? (different reduction
+    # layouts are allowed to differ by rounding; both must match the oracle)
+    d3b = rz.rz_d3(logpi.to(DEV), logmu.to(DEV)).item()
+    assert scalar_close(d3b, got["d3"])

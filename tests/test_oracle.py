@@ -398,3 +398,38 @@ def test_log_gap_decomposition_zero_kernel_term():
     pi_v = oracle.token_logprob(H, Wv, tok)[0]
     assert np.all(pi_v - mu_v == 0.0)
     assert oracle.d3(pi_v, mu_v) == 0.0
+
+
+# ---------------------------------------------------------------- diagnostics
+
+def test_is_stats_closed_forms():
+    lp = np.array([-3.0, -5.0, -1.0])
+    r = oracle.is_stats(lp, lp - 0.25)            # d = 0.25 everywhere
+    assert r["k1"] == pytest.approx(-0.25, abs=1e-15)
+    assert r["k2"] == pytest.approx(0.03125, abs=1e-15)
+    assert r["d3"] == pytest.approx(math.exp(0.25) - 1.25, abs=1e-15)
+    assert r["w_max"] == r["w_min"] == pytest.approx(math.exp(0.25))
+    assert r["absd_max"] == pytest.approx(0.25)
+    z = oracle.is_stats(np.array([]), np.array([]))
+    assert all(v == 0.0 for v in z.values())
+
+
+def test_kl_estimators_by_enumeration():
+    """Weighting tokens by mu instead of sampling them: both k1 and k3 (= D3
+    per token) have expectation KL(mu || pi) (scipy rel_entr)."""
+    rng = _rng(21)
+    V = 9
+    pi = rng.random(V); pi /= pi.sum()
+    mu = rng.random(V); mu /= mu.sum()
+    kl = float(np.sum(scipy.special.rel_entr(mu, pi)))
+    lp, lm = np.log(pi), np.log(mu)
+    k1 = sum(mu[a] * oracle.is_stats(lp[a:a + 1], lm[a:a + 1])["k1"] for a in range(V))
+    k3 = sum(mu[a] * oracle.is_stats(lp[a:a + 1], lm[a:a + 1])["d3"] for a in range(V))
+    assert k1 == pytest.approx(kl, abs=1e-14)
+    assert k3 == pytest.approx(kl, abs=1e-14)
+
+
+def test_peak_to_median():
+    assert oracle.peak_to_median([1.0, 2.0, 3.0, 100.0]) == pytest.approx(40.0)
+    assert oracle.peak_to_median([2.0, 2.0, 2.0]) == 1.0
+    assert oracle.peak_to_median([3.0, 1.0, 2.0]) == pytest.approx(1.5)
