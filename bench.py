@@ -240,8 +240,21 @@ def run_ours(args):
         rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], logprob_out=lp2, ws=ws_r)
         rev[k + 1].record(stream)
     torch.cuda.synchronize()
-    clocks = clk.stop()
     roll_ms = statistics.mean(rev[k].elapsed_time(rev[k + 1]) for k in range(kr))
+    # rollout with the sampling fused into the same GEMM pass
+    tok_s = torch.empty(T, dtype=torch.int32, device=dev)
+    ws_s = rz.alloc_workspace(rz.RZ_OP_SAMPLE, T, d, V, 0, dev)
+    rz.rz_sample_logprob(b["H"], b["W_mu"], 1234, tokens_out=tok_s, logprob_out=lp2, ws=ws_s)
+    torch.cuda.synchronize()
+    rev[0].record(stream)
+    for k in range(kr):
+        rz.rz_sample_logprob(b["H"], b["W_mu"], 1234 + k, tokens_out=tok_s, logprob_out=lp2,
+                             ws=ws_s)
+        rev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    samp_ms = statistics.mean(rev[k].elapsed_time(rev[k + 1]) for k in range(kr))
+    del ws_s, tok_s
+    clocks = clk.stop()
 
     # end to end through the public API from pinned host buffers
     e2e = run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err)
@@ -270,6 +283,7 @@ def run_ours(args):
             "peak_source": "%s bf16_tflops_sustained" % peak_src,
             "traffic": None},
         "rollout_tokens_per_s": T / (roll_ms / 1e3),
+        "rollout_sample_tokens_per_s": T / (samp_ms / 1e3),
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step(T, V),

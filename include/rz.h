@@ -78,6 +78,7 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
 #define RZ_OP_LOSS_FWD_BWD    1
 #define RZ_OP_LOGITS_LOSS     2
 #define RZ_OP_IS_LOSS         3
+#define RZ_OP_SAMPLE          4
 
 /*
  * Bytes of scratch the operation needs for these sizes (0 if none).  Pure
@@ -107,6 +108,31 @@ RZ_API int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* t
                      float* logprob_out, float* lse_out,
                      void* ws, size_t ws_bytes, int32_t* err_flag,
                      rz_stream_t stream);
+
+/*
+ * Rollout side with the sampling fused in: draws a_t ~ softmax(z_t),
+ * z = H W^T at temperature 1, and records log mu(a_t) in the same pass over
+ * the logits [vLLM-zh s.4 item 2: the rollout records the logprob of every
+ * token it samples; the pages do not say how it samples].
+ * Sampling rule (a reading, exact in law): Gumbel-max,
+ *   a_t = argmax_v z_tv + G_tv,  G = -log(-log U),  ties -> smaller v,
+ * with U_tv = ((x >> 9) + 1/2) 2^-23 and x = word (v mod 4) of
+ * Philox4x32-10 (Salmon et al., SC 2011) at counter
+ * (v / 4, row_id low 32 bits, row_id high 32 bits, 0) under key
+ * (seed low, seed high).  row_ids [T] int64 (nullable: the row index t)
+ * makes a row's sample depend only on its own id, hidden state and W --
+ * never on the batch it sits in.
+ *   tokens_out [T] int32, logprob_out [T] fp32 (log mu of the sampled
+ *   token), lse_out [T] fp32 (nullable).
+ * logprob_out is bitwise equal to what rz_token_logprob (and the learner in
+ * rz_loss_fwd_bwd) computes for the same H, W and the sampled tokens.
+ * Workspace: rz_workspace_size(RZ_OP_SAMPLE, T, d, V, 0).
+ */
+RZ_API int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids,
+                             int64_t T, int32_t d, int32_t V, uint64_t seed,
+                             int32_t* tokens_out, float* logprob_out, float* lse_out,
+                             void* ws, size_t ws_bytes, int32_t* err_flag,
+                             rz_stream_t stream);
 
 /*
  * Group-mean advantage [vLLM-zh s.4 item 3]: A_i = r_i - (1/G) sum_{j in g(i)} r_j,

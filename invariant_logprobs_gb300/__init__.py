@@ -32,6 +32,7 @@ RZ_OP_TOKEN_LOGPROB = 0
 RZ_OP_LOSS_FWD_BWD = 1
 RZ_OP_LOGITS_LOSS = 2
 RZ_OP_IS_LOSS = 3
+RZ_OP_SAMPLE = 4
 
 _lib = None
 
@@ -55,6 +56,8 @@ _SIGNATURES = {
     "rz_token_logprob_noalloc": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _P]),
     "rz_noalloc_scratch_bytes": (_SZ, []),
     "rz_is_stats": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+    "rz_sample_logprob": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, ctypes.c_uint64,
+                                         _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_peak_to_median": (ctypes.c_int, [_P, _I64, _P]),
 }
 
@@ -328,3 +331,29 @@ def rz_peak_to_median(series):
     _check("rz_peak_to_median", load().rz_peak_to_median(
         ctypes.cast(buf, ctypes.c_void_p), len(series), ctypes.byref(out)))
     return out.value
+
+
+def rz_sample_logprob(H, W, seed, row_ids=None, tokens_out=None, logprob_out=None,
+                      lse_out=None, ws=None, err_flag=None, stream=None):
+    """Rollout with fused sampling (see include/rz.h): returns (tokens [T]
+    int32, log mu [T] fp32)."""
+    torch = _torch()
+    lib = load()
+    _need(H, torch.bfloat16, "H")
+    _need(W, torch.bfloat16, "W")
+    if row_ids is not None:
+        _need(row_ids, torch.int64, "row_ids")
+    T, d = H.shape
+    V = W.shape[0]
+    if tokens_out is None:
+        tokens_out = torch.empty(T, dtype=torch.int32, device=H.device)
+    if logprob_out is None:
+        logprob_out = torch.empty(T, dtype=torch.float32, device=H.device)
+    if ws is None:
+        ws = alloc_workspace(RZ_OP_SAMPLE, T, d, V, 0, H.device)
+    st = lib.rz_sample_logprob(_ptr(H), _ptr(W), _ptr(row_ids), T, d, V,
+                               ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
+                               _ptr(tokens_out), _ptr(logprob_out), _ptr(lse_out), _ptr(ws),
+                               ws.numel(), _ptr(err_flag), _stream(stream))
+    _check("rz_sample_logprob", st)
+    return tokens_out, logprob_out

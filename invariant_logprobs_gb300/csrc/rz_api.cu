@@ -91,6 +91,18 @@ FwdLayout fwd_layout(int64_t T, int32_t V) {
   return L;
 }
 
+struct SampleLayout {
+  size_t part, idx, total;
+};
+SampleLayout sample_layout(int64_t T, int32_t V) {
+  SampleLayout L{};
+  const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
+  L.part = 0;
+  L.idx = al256(t * vocab_splits(V) * sizeof(float4));
+  L.total = L.idx + al256(t * vocab_splits(V) * sizeof(int));
+  return L;
+}
+
 struct LearnLayout {
   FwdLayout fwd;
   size_t logpi, lse2, coef, resp, dz, total;
@@ -168,6 +180,7 @@ size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
     case RZ_OP_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
     case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B);
     case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
+    case RZ_OP_SAMPLE: return sample_layout(T, V > 0 ? V : 1).total;
     default: return 0;
   }
 }
@@ -185,6 +198,28 @@ int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, 
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   return logprob_pass(H, W, tokens, T, d, V, logprob_out, lse_out, nullptr,
                       static_cast<uint8_t*>(ws), err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids, int64_t T,
+                      int32_t d, int32_t V, uint64_t seed, int32_t* tokens_out,
+                      float* logprob_out, float* lse_out, void* ws, size_t ws_bytes,
+                      int32_t* err_flag, rz_stream_t stream) {
+  if (!sizes_ok(T, d, V)) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!H || !W || !tokens_out || !logprob_out)) return RZ_ERR_INVALID_ARG;
+  if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
+  if (T == 0) return RZ_OK;
+  if (!a16(H) || !a16(W)) return RZ_ERR_UNSUPPORTED;
+  const SampleLayout L = sample_layout(T, V);
+  if (!ws || ws_bytes < L.total || !a256(ws)) return RZ_ERR_WORKSPACE;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  CUtensorMap tmH, tmW;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  return cuda_status(launch_sample(tmH, tmW, T, d, V, row_ids, seed,
+                                   reinterpret_cast<float4*>(w8 + L.part),
+                                   reinterpret_cast<int*>(w8 + L.idx), tokens_out, logprob_out,
+                                   lse_out, err_flag, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int rz_group_advantage(const float* rewards, int32_t B, int32_t G, float* adv_out,

@@ -21,6 +21,7 @@
 
 #include "rz_gemm.cuh"
 #include "rz_internal.h"
+#include "rz_lse.cuh"
 #include "rz_math.cuh"
 #include "rz_ptx.cuh"
 
@@ -64,24 +65,7 @@ struct EpiLsePartial {
       for (int j = 0; j < 32; ++j)
         if (cbase + j >= p.V) v[j] = -INFINITY;
     }
-    float mx[4] = {v[0], v[1], v[2], v[3]};
-#pragma unroll
-    for (int j = 4; j < 32; j += 4) {
-      mx[0] = fmaxf(mx[0], v[j]);
-      mx[1] = fmaxf(mx[1], v[j + 1]);
-      mx[2] = fmaxf(mx[2], v[j + 2]);
-      mx[3] = fmaxf(mx[3], v[j + 3]);
-    }
-    const float cm2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * kLog2e;
-    if (cm2 > st.m2) {
-      st.s *= ex2_approx(st.m2 - cm2);
-      st.m2 = cm2;
-    }
-    const float nm = -st.m2;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j & 3] += ex2_approx(fmaf(v[j], kLog2e, nm));
-    st.s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    lse_fold32(st.m2, st.s, v);
     const unsigned rel = static_cast<unsigned>(st.a - cbase);
     if (rel < 32u) {
 #pragma unroll
@@ -112,6 +96,130 @@ struct EpiLsePartial {
     if (g >= p.T) return;
     p.part[g * p.S + grp] = make_float2(st.m2, st.s);
     if (st.found) p.zgather[g] = st.za;
+  }
+};
+
+// Philox4x32 with 10 rounds (Salmon et al., "Parallel Random Numbers: As
+// Easy as 1, 2, 3", SC 2011): each round multiplies c0 and c2 by fixed odd
+// constants, mixes the 64-bit products' halves with c1, c3 and the key, and
+// the key is bumped by two fixed increments between rounds.
+__device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                              uint32_t k0, uint32_t k1, uint32_t (&out)[4]) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c0;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Fused sampling in the rollout's logprob GEMM: besides the log-sum-exp state
+// (the very same arithmetic as EpiLsePartial) each row keeps the running
+// Gumbel-max winner over its split: key = z log2(e) - log2(-log2 U), which
+// orders tokens exactly as z + Gumbel noise does (the two differ by the
+// constant log2(ln 2) and the factor log2(e)).  U for (row, v) is word
+// v mod 4 of Philox4x32-10 at counter (v / 4, row id lo, row id hi, 0) under
+// the caller's 64-bit seed, mapped to ((x >> 9) + 1/2) 2^-23 in (0, 1).  Ties
+// go to the smaller vocabulary index.
+struct EpiSample {
+  struct Params {
+    const int64_t* row_ids;  // nullable: row index
+    float4* part;            // [T, S]: m2, s, best key, z at best
+    int* part_idx;           // [T, S]: best vocabulary index
+    long long T;
+    int V;
+    int S;
+    uint32_t k0, k1;
+  };
+  struct State {
+    float m2, s, bk, bz;
+    int bi;
+    uint32_t r_lo, r_hi;
+  };
+
+  static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk, int,
+                                                    int row) {
+    const long long g = static_cast<long long>(m_blk) * kBM + row;
+    st.m2 = -INFINITY;
+    st.s = 0.f;
+    st.bk = -INFINITY;
+    st.bz = 0.f;
+    st.bi = -1;
+    const long long rid = g < p.T ? (p.row_ids ? __ldg(p.row_ids + g) : g) : 0;
+    st.r_lo = static_cast<uint32_t>(static_cast<unsigned long long>(rid) & 0xffffffffull);
+    st.r_hi = static_cast<uint32_t>(static_cast<unsigned long long>(rid) >> 32);
+  }
+
+  static __device__ __forceinline__ void chunk(const Params& p, State& st, const uint32_t (&r)[32],
+                                               int cbase) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    if (cbase + 32 > p.V) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (cbase + j >= p.V) v[j] = -INFINITY;
+    }
+    lse_fold32(st.m2, st.s, v);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t x[4];
+      philox4x32_10(static_cast<uint32_t>(cbase >> 2) + q, st.r_lo, st.r_hi, 0u, p.k0, p.k1, x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * q + e;
+        const float u = __fmul_rn(__fadd_rn(__uint2float_rn(x[e] >> 9), 0.5f), 1.1920928955078125e-7f);
+        // -log2 U must be accurate relative to itself, also for U next to 1
+        // where it is tiny (and where the winning, largest Gumbel draws come
+        // from): the accurate log2f there, the fast approximation outside.
+        const float key = fmaf(v[j], kLog2e, -lg2_approx(-log2f(u)));
+        if (key > st.bk) {  // -inf (masked) never wins
+          st.bk = key;
+          st.bz = v[j];
+          st.bi = cbase + j;
+        }
+      }
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, State& st, int, int n_tile,
+                                              uint32_t taddr, int, uint8_t*) {
+    const int col0 = n_tile * kBN;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 64) {
+      if (col0 + c >= p.V) break;  // warp-uniform
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr + c, r0);
+      tmem_ld32(taddr + c + 32, r1);
+      tmem_ld_wait();
+      chunk(p, st, r0, col0 + c);
+      if (col0 + c + 32 < p.V) chunk(p, st, r1, col0 + c + 32);
+    }
+  }
+
+  static __device__ __forceinline__ void task_end(const Params& p, State& st, int m_blk, int grp,
+                                                  int row) {
+    const long long g = static_cast<long long>(m_blk) * kBM + row;
+    if (g >= p.T) return;
+    p.part[g * p.S + grp] = make_float4(st.m2, st.s, st.bk, st.bz);
+    p.part_idx[g * p.S + grp] = st.bi;
   }
 };
 
@@ -306,16 +414,8 @@ __global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __res
                                  float* __restrict__ lse, float* __restrict__ lse2_out, int* err) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
-  const float2* pp = part + t * S;
-  float M = -INFINITY;
-  for (int g = 0; g < S; ++g) M = fmaxf(M, pp[g].x);
-  float sum = 0.f;
-  for (int g = 0; g < S; ++g) {
-    const float2 q = pp[g];
-    sum += q.y * exp2f(q.x - M);
-  }
-  float l2 = M + log2f(sum);
-  float l = l2 * kLn2;
+  float l2 = lse2_of_splits(part + t * S, S);
+  float l = __fmul_rn(l2, kLn2);
   const int a = tokens[t];
   float lp;
   if (a < 0 || a >= V) {
@@ -324,11 +424,35 @@ __global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __res
     l2 = lp;
     if (err) atomicOr(err, 1);
   } else {
-    lp = zgather[t] - l;
+    lp = logprob_from(zgather[t], l2);
   }
   logprob[t] = lp;
   if (lse) lse[t] = l;
   if (lse2_out) lse2_out[t] = l2;
+}
+
+// One thread per row: log-sum-exp exactly as lse_merge_kernel, and the
+// Gumbel-max winner over the splits in split order (ties: earlier split,
+// i.e. smaller vocabulary index).
+__global__ void sample_merge_kernel(long long T, int S, const float4* __restrict__ part,
+                                    const int* __restrict__ part_idx, int32_t* __restrict__ tokens,
+                                    float* __restrict__ logprob, float* __restrict__ lse) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const float4* pp = part + t * S;
+  const float l2 = lse2_of_splits(pp, S);
+  float bk = -INFINITY, bz = 0.f;
+  int bi = 0;
+  for (int g = 0; g < S; ++g) {
+    if (pp[g].z > bk) {
+      bk = pp[g].z;
+      bz = pp[g].w;
+      bi = part_idx[t * S + g];
+    }
+  }
+  tokens[t] = bi;
+  logprob[t] = logprob_from(bz, l2);
+  if (lse) lse[t] = __fmul_rn(l2, kLn2);
 }
 
 // ============================================================== launchers
@@ -388,6 +512,25 @@ cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const floa
   const long long blocks = (T + threads - 1) / threads;
   lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
       T, V, vocab_splits(V), tokens, part, zgather, logprob, lse, lse2, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
+                          const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
+                          int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st) {
+  const int S = vocab_splits(V);
+  GemmSched s = sched_of(T, V, S, d, err);
+  s.tiles_per_group = vocab_tiles_per_split(V);
+  s.m_group = vocab_raster_group();
+  EpiSample::Params p{row_ids, part, part_idx, static_cast<long long>(T), V, S,
+                      static_cast<uint32_t>(seed & 0xffffffffull),
+                      static_cast<uint32_t>(seed >> 32)};
+  cudaError_t e = run_gemm<EpiSample, false, false>(tmH, tmW, s, p, st);
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  const long long blocks = (T + threads - 1) / threads;
+  sample_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(T, S, part, part_idx,
+                                                                         tokens, logprob, lse);
   return cudaGetLastError();
 }
 
