@@ -480,6 +480,12 @@ def run_profile(args):
     per = max(1, args.rows // wl.B)
     wl = dataclasses.replace(wl, len_lo=per, len_hi=per, tokens="uniform")
     b = synth.make_batch(wl, device=dev)
+    if args.profile == "sample":
+        for k in range(args.steps):
+            rz.rz_sample_logprob(b["H"], b["W_mu"], 77 + k)
+        torch.cuda.synchronize()
+        print("profile sample rows=%d ok" % b["T"])
+        return 0
     logmu, _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
     adv = rz.rz_group_advantage(b["rewards"], b["G"])
     for _ in range(args.steps):
@@ -499,7 +505,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["learner", "logits"], default=None,
+    ap.add_argument("--profile", choices=["learner", "logits", "sample"], default=None,
                     help="small fixed case for ncu captures (no timing output)")
     ap.add_argument("--rows", type=int, default=16384)
     args = ap.parse_args()

@@ -167,8 +167,29 @@ struct EpiSample {
     st.r_hi = static_cast<uint32_t>(static_cast<unsigned long long>(rid) >> 32);
   }
 
+  // -log2(U) to full relative precision for U = (m + 1/2) 2^-23.  Next to 1
+  // (1 - U < 2^-6), where -log2 U is tiny and the largest Gumbel draws come
+  // from, the fast hardware log2 has only absolute accuracy, so the Taylor
+  // series -ln(1 - v) = v (1 + v/2 + v^2/3 + v^3/4 + v^4/5 + ...) is used
+  // (truncation < 2^-26 relative); elsewhere the hardware log2 is accurate
+  // to ~1e-5 relative or better.
+  static __device__ __forceinline__ float neg_log2_uniform(uint32_t bits) {
+    const uint32_t m = bits >> 9;
+    const float u = __fmul_rn(__fadd_rn(__uint2float_rn(m), 0.5f), 1.1920928955078125e-7f);
+    const float v = __fmul_rn(__fsub_rn(__uint2float_rn(8388608u - m), 0.5f),
+                              1.1920928955078125e-7f);  // 1 - u, exact
+    float ser = fmaf(v, 0.2f, 0.25f);
+    ser = fmaf(v, ser, 0.33333334f);
+    ser = fmaf(v, ser, 0.5f);
+    ser = fmaf(v, ser, 1.0f);
+    const float near1 = __fmul_rn(__fmul_rn(v, kLog2e), ser);
+    return v < 0.015625f ? near1 : -lg2_approx(u);
+  }
+
+  // 32 columns of this thread's row; `words` holds the row's 32 Philox
+  // words (8 pieces of 16 B, piece q at position q ^ (lane & 7)).
   static __device__ __forceinline__ void chunk(const Params& p, State& st, const uint32_t (&r)[32],
-                                               int cbase) {
+                                               int cbase, const uint4* words, int sw) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -180,17 +201,13 @@ struct EpiSample {
     lse_fold32(st.m2, st.s, v);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      uint32_t x[4];
-      philox4x32_10(static_cast<uint32_t>(cbase >> 2) + q, st.r_lo, st.r_hi, 0u, p.k0, p.k1, x);
+      const uint4 x4 = words[q ^ sw];
+      const uint32_t x[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = 4 * q + e;
-        const float u = __fmul_rn(__fadd_rn(__uint2float_rn(x[e] >> 9), 0.5f), 1.1920928955078125e-7f);
-        // -log2 U must be accurate relative to itself, also for U next to 1
-        // where it is tiny (and where the winning, largest Gumbel draws come
-        // from): the accurate log2f there, the fast approximation outside.
-        const float key = fmaf(v[j], kLog2e, -lg2_approx(-log2f(u)));
-        if (key > st.bk) {  // -inf (masked) never wins
+        const float key = fmaf(v[j], kLog2e, -lg2_approx(neg_log2_uniform(x[e])));
+        if (key > st.bk) {  // -inf (masked) never wins; ties keep the smaller index
           st.bk = key;
           st.bz = v[j];
           st.bi = cbase + j;
@@ -200,17 +217,25 @@ struct EpiSample {
   }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, int, int n_tile,
-                                              uint32_t taddr, int, uint8_t*) {
+                                              uint32_t taddr, int row, uint8_t* stage) {
     const int col0 = n_tile * kBN;
+    const int lane = row & 31;
+    const int sw = lane & 7;
+    uint4* words = reinterpret_cast<uint4*>(stage + lane * 128);  // this row only
 #pragma unroll 1
-    for (int c = 0; c < kBN; c += 64) {
+    for (int c = 0; c < kBN; c += 32) {
       if (col0 + c >= p.V) break;  // warp-uniform
-      uint32_t r0[32], r1[32];
+      uint32_t r0[32];
       tmem_ld32(taddr + c, r0);
-      tmem_ld32(taddr + c + 32, r1);
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        uint32_t x[4];
+        philox4x32_10(static_cast<uint32_t>((col0 + c) >> 2) + q, st.r_lo, st.r_hi, 0u, p.k0,
+                      p.k1, x);
+        words[q ^ sw] = make_uint4(x[0], x[1], x[2], x[3]);
+      }
       tmem_ld_wait();
-      chunk(p, st, r0, col0 + c);
-      if (col0 + c + 32 < p.V) chunk(p, st, r1, col0 + c + 32);
+      chunk(p, st, r0, col0 + c, words, sw);
     }
   }
 
