@@ -118,7 +118,7 @@ def d3(logpi, logmu):
     return float(np.mean(w - 1.0 - np.log(w)))
 
 
-def is_loss(logpi, logmu, cu_seqlens, adv):
+def is_loss(logpi, logmu, cu_seqlens, adv, mask=None):
     """The REINFORCE Zero loss and its per-token gradient coefficient.
 
     w_t = pi/mu = exp(log pi_t - log mu_t), never clipped [vLLM-zh s.4 item 2].
@@ -126,6 +126,11 @@ def is_loss(logpi, logmu, cu_seqlens, adv):
     D3 = mean_t (w_t - 1 - log w_t)                      [vLLM-zh s.3]
     c_t = A_i w_t / (B T_i) = -dL/dlog pi_t  (the derivative of w through the
     numerator only: dw/dlog pi = w)                      [RZ-page s.02]
+
+    mask (optional, [T], nonzero = valid action token): "T_i counts valid
+    action tokens" [RZ-page s.02]; a masked-out token (e.g. a tool output
+    inside an agentic response) is in no sum: T_i counts the valid tokens of
+    response i, D3 averages over all valid tokens, and c_t = 0.
 
     Returns dict(loss, d3, w [T], c [T]) in fp64.
     """
@@ -135,27 +140,29 @@ def is_loss(logpi, logmu, cu_seqlens, adv):
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     B = A.shape[0]
     T = lp.shape[0]
+    valid = np.ones(T, dtype=bool) if mask is None else (np.asarray(mask) != 0)
     w = np.exp(lp - lm)
     c = np.zeros(T, dtype=np.float64)
     total = 0.0
     for i in range(B):
         s, e = int(cu[i]), int(cu[i + 1])
-        Ti = e - s
+        v = valid[s:e]
+        Ti = int(v.sum())
         if Ti == 0:
             continue
-        total += A[i] * w[s:e].sum() / Ti
-        c[s:e] = A[i] * w[s:e] / (B * Ti)
+        total += A[i] * w[s:e][v].sum() / Ti
+        c[s:e] = np.where(v, A[i] * w[s:e] / (B * Ti), 0.0)
     loss = -total / B if B > 0 else 0.0
-    return {"loss": loss, "d3": d3(lp, lm), "w": w, "c": c}
+    return {"loss": loss, "d3": d3(lp[valid], lm[valid]), "w": w, "c": c}
 
 
-def loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv):
+def loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, mask=None):
     """Learner step: log pi, loss, D3 and the gradients dH, dW.
 
     dL/dz_tv = c_t (softmax_v(z_t) - [v = a_t]) because
     dL/dlog pi_t = -c_t and dlog pi_t/dz_tv = [v = a_t] - p_tv; mu and A are
     constants [RZ-page s.02: differentiate through the numerator].
-    z = H W^T gives dH = dz W and dW = dz^T H.
+    z = H W^T gives dH = dz W and dW = dz^T H.  `mask` as in is_loss.
     Returns dict(loss, d3, logpi, lse, c, dH, dW) in fp64.
     """
     Hd = _f64(H)
@@ -163,7 +170,7 @@ def loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv):
     tokens = np.asarray(tokens, dtype=np.int64)
     T = tokens.shape[0]
     logpi, lse = token_logprob(Hd, Wd, tokens)
-    r = is_loss(logpi, logmu, cu_seqlens, adv)
+    r = is_loss(logpi, logmu, cu_seqlens, adv, mask)
     c = r["c"]
     dH = np.zeros_like(Hd)
     dW = np.zeros_like(Wd)
@@ -179,7 +186,7 @@ def loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv):
             "c": c, "dH": dH, "dW": dW}
 
 
-def logits_loss_fwd_bwd(logits, tokens, logmu, cu_seqlens, adv, rows=None):
+def logits_loss_fwd_bwd(logits, tokens, logmu, cu_seqlens, adv, rows=None, mask=None):
     """The same loss and dlogits, starting from given logits z [T, V].
 
     Returns dict(loss, d3, logpi, lse, c) and, for the requested rows (all
@@ -195,7 +202,7 @@ def logits_loss_fwd_bwd(logits, tokens, logmu, cu_seqlens, adv, rows=None):
         l = logsumexp_rows(z)
         lse[s:e] = l
         logpi[s:e] = z[np.arange(e - s), tokens[s:e]] - l
-    r = is_loss(logpi, logmu, cu_seqlens, adv)
+    r = is_loss(logpi, logmu, cu_seqlens, adv, mask)
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
     dz = np.empty((rows.shape[0], np.asarray(logits[:1]).shape[1]), np.float64)
     for s in range(0, rows.shape[0], _ROW_BLOCK):

@@ -433,3 +433,35 @@ def test_peak_to_median():
     assert oracle.peak_to_median([1.0, 2.0, 3.0, 100.0]) == pytest.approx(40.0)
     assert oracle.peak_to_median([2.0, 2.0, 2.0]) == 1.0
     assert oracle.peak_to_median([3.0, 1.0, 2.0]) == pytest.approx(1.5)
+
+
+# ---------------------------------------------------------------- action masks
+
+def test_mask_all_ones_is_no_mask():
+    H, W, tok, lm, cu, A = _tiny_problem(30, T_lo=1, T_hi=7, B=5, d=4, V=9)
+    r0 = oracle.loss_fwd_bwd(H, W, tok, lm, cu, A)
+    r1 = oracle.loss_fwd_bwd(H, W, tok, lm, cu, A, mask=np.ones(len(tok), dtype=np.uint8))
+    for k in ("loss", "d3"):
+        assert r1[k] == r0[k]
+    np.testing.assert_array_equal(r1["dW"], r0["dW"])
+
+
+def test_masked_tokens_equal_removed_tokens():
+    """Masking a token out must give exactly the loss, D3 and dW of the batch
+    with that token removed, and a zero dH row for it."""
+    H, W, tok, lm, cu, A = _tiny_problem(31, T_lo=2, T_hi=8, B=6, d=5, V=11)
+    rng = _rng(32)
+    T = len(tok)
+    mask = (rng.random(T) < 0.7).astype(np.uint8)
+    mask[cu[2]:cu[3]] = 0                        # one response fully masked
+    rm = oracle.loss_fwd_bwd(H, W, tok, lm, cu, A, mask=mask)
+    keep = mask != 0
+    lengths = [int(keep[cu[i]:cu[i + 1]].sum()) for i in range(len(A))]
+    cu_k = np.concatenate([[0], np.cumsum(lengths)])
+    rk = oracle.loss_fwd_bwd(H[keep], W, tok[keep], lm[keep], cu_k, A)
+    assert rm["loss"] == pytest.approx(rk["loss"], abs=1e-14)
+    assert rm["d3"] == pytest.approx(rk["d3"], abs=1e-14)
+    np.testing.assert_allclose(rm["dW"], rk["dW"], atol=1e-14)
+    np.testing.assert_allclose(rm["dH"][keep], rk["dH"], atol=1e-14)
+    assert np.all(rm["dH"][~keep] == 0.0)
+    assert np.all(rm["c"][~keep] == 0.0)
