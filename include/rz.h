@@ -149,11 +149,16 @@ RZ_API int rz_group_advantage(const float* rewards, int32_t B, int32_t G,
  *   d3   = (1/T) sum_t (w_t - 1 - log w_t)           [vLLM-zh s.3]
  *   coef_out[t] = A_i w_t / (B T_i) = -dloss/dlogpi_t (nullable)
  * cu_seqlens [B+1] int64 (response i owns tokens cu[i] .. cu[i+1]-1),
- * adv [B] fp32.  Deterministic (fixed-order reductions).  T = 0 gives
- * loss = d3 = 0.  Workspace: rz_workspace_size(RZ_OP_IS_LOSS, T, 0, 0, B).
+ * adv [B] fp32.  action_mask [T] uint8 (nullable = all tokens are action
+ * tokens): "T_i counts valid action tokens" [RZ-page s.02] -- a token with
+ * mask 0 (e.g. a tool output inside an agentic response) enters no sum:
+ * T_i counts the valid tokens of response i, D3 averages over valid tokens,
+ * coef is 0 for it.  Deterministic (fixed-order reductions).  No valid
+ * token gives loss = d3 = 0.  Workspace: rz_workspace_size(RZ_OP_IS_LOSS, T,
+ * 0, 0, B).
  */
 RZ_API int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens,
-               const float* adv, int32_t B, int64_t T,
+               const float* adv, const uint8_t* action_mask, int32_t B, int64_t T,
                float* loss_out, float* d3_out, float* coef_out,
                void* ws, size_t ws_bytes, int32_t* err_flag, rz_stream_t stream);
 
@@ -193,7 +198,9 @@ RZ_API int rz_peak_to_median(const float* series, int64_t n, double* ratio_out);
  * Learner side: the fused logprob + REINFORCE Zero loss, forward and backward
  * [RZ-page s.02 objective and "differentiate through the numerator"].
  *   H [T,d] bf16, W [V,d] bf16, tokens [T] int32, logmu [T] fp32 (recorded by
- *   the rollout), cu_seqlens [B+1] int64, adv [B] fp32.
+ *   the rollout), cu_seqlens [B+1] int64, adv [B] fp32, action_mask [T] uint8
+ *   (nullable; as in rz_is_loss: masked tokens get log pi but no loss and no
+ *   gradient -- their dH rows are 0).
  * Outputs: loss_out, d3_out (fp32 scalars), logprob_out [T] fp32 (nullable),
  *   dH [T,d] bf16 = dz W, dW [V,d] fp32 = dz^T H (overwritten, not
  *   accumulated), with dz_tv = A_i w_t/(B T_i) (softmax_v(z_t) - [v = a_t]).
@@ -205,6 +212,7 @@ RZ_API int rz_peak_to_median(const float* series, int64_t n, double* ratio_out);
  */
 RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
                     const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                    const uint8_t* action_mask,
                     int32_t B, int64_t T, int32_t d, int32_t V,
                     float* loss_out, float* d3_out, float* logprob_out,
                     rz_bf16* dH, float* dW,
@@ -216,12 +224,14 @@ RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* to
  * log-softmax, gather, ratio and dlogits done in place.
  *   logits_inout [T, V] bf16: read as logits, overwritten with
  *   dz_tv = A_i w_t/(B T_i) (softmax_v - onehot) in bf16.  V % 8 == 0.
- *   logprob_out [T] fp32 (required), loss_out, d3_out as in rz_is_loss.
+ *   logprob_out [T] fp32 (required), loss_out, d3_out, action_mask as in
+ *   rz_is_loss (masked rows are overwritten with zeros).
  * Workspace: rz_workspace_size(RZ_OP_LOGITS_LOSS, T, 0, V, B).
  */
 RZ_API int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens,
                            const float* logmu, const int64_t* cu_seqlens,
-                           const float* adv, int32_t B, int64_t T, int32_t V,
+                           const float* adv, const uint8_t* action_mask,
+                           int32_t B, int64_t T, int32_t V,
                            float* loss_out, float* d3_out, float* logprob_out,
                            void* ws, size_t ws_bytes, int32_t* err_flag,
                            rz_stream_t stream);

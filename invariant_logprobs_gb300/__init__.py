@@ -46,11 +46,11 @@ _SIGNATURES = {
     "rz_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rz_token_logprob": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
     "rz_group_advantage": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
-    "rz_is_loss": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_is_loss": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_d3": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
-    "rz_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
+    "rz_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
                                        _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
-    "rz_logits_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32,
+    "rz_logits_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32,
                                               _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_lmhead_logits": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
     "rz_token_logprob_noalloc": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _P]),
@@ -167,7 +167,7 @@ def rz_group_advantage(rewards, G, adv_out=None, stream=None):
 
 
 def rz_is_loss(logpi, logmu, cu_seqlens, adv, loss_out=None, d3_out=None, coef_out=None,
-               ws=None, err_flag=None, stream=None):
+               ws=None, err_flag=None, stream=None, action_mask=None):
     torch = _torch()
     lib = load()
     _need(cu_seqlens, torch.int64, "cu_seqlens")
@@ -180,7 +180,10 @@ def rz_is_loss(logpi, logmu, cu_seqlens, adv, loss_out=None, d3_out=None, coef_o
         d3_out = torch.empty(1, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(RZ_OP_IS_LOSS, T, 0, 0, B, dev)
-    st = lib.rz_is_loss(_ptr(logpi), _ptr(logmu), _ptr(cu_seqlens), _ptr(adv), B, T,
+    if action_mask is not None:
+        _need(action_mask, torch.uint8, "action_mask")
+    st = lib.rz_is_loss(_ptr(logpi), _ptr(logmu), _ptr(cu_seqlens), _ptr(adv),
+                        _ptr(action_mask), B, T,
                         _ptr(loss_out), _ptr(d3_out), _ptr(coef_out), _ptr(ws), ws.numel(),
                         _ptr(err_flag), _stream(stream))
     _check("rz_is_loss", st)
@@ -201,7 +204,7 @@ def rz_d3(logpi, logmu, d3_out=None, stream=None):
 
 def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=None, dW=None,
                     loss_out=None, d3_out=None, ws=None, err_flag=None, stream=None,
-                    want_logprob=True):
+                    want_logprob=True, action_mask=None):
     """Learner-side fused logprob + loss forward/backward (see include/rz.h).
     Returns dict(loss, d3, logprob, dH, dW) of device tensors."""
     torch = _torch()
@@ -228,8 +231,10 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
         d3_out = torch.empty(1, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
+    if action_mask is not None:
+        _need(action_mask, torch.uint8, "action_mask")
     st = lib.rz_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(cu_seqlens),
-                             _ptr(adv), B, T, d, V, _ptr(loss_out), _ptr(d3_out),
+                             _ptr(adv), _ptr(action_mask), B, T, d, V, _ptr(loss_out), _ptr(d3_out),
                              _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
                              _ptr(err_flag), _stream(stream))
     _check("rz_loss_fwd_bwd", st)
@@ -237,7 +242,8 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
 
 
 def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob_out=None,
-                           loss_out=None, d3_out=None, ws=None, err_flag=None, stream=None):
+                           loss_out=None, d3_out=None, ws=None, err_flag=None, stream=None,
+                           action_mask=None):
     """Given-logits variant; overwrites logits_inout with dz (see include/rz.h)."""
     torch = _torch()
     lib = load()
@@ -257,8 +263,11 @@ def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob
         d3_out = torch.empty(1, dtype=torch.float32, device=dev)
     if ws is None:
         ws = alloc_workspace(RZ_OP_LOGITS_LOSS, T, 0, V, B, dev)
+    if action_mask is not None:
+        _need(action_mask, torch.uint8, "action_mask")
     st = lib.rz_logits_loss_fwd_bwd(_ptr(logits_inout), _ptr(tokens), _ptr(logmu),
-                                    _ptr(cu_seqlens), _ptr(adv), B, T, V, _ptr(loss_out),
+                                    _ptr(cu_seqlens), _ptr(adv), _ptr(action_mask), B, T, V,
+                                    _ptr(loss_out),
                                     _ptr(d3_out), _ptr(logprob_out), _ptr(ws), ws.numel(),
                                     _ptr(err_flag), _stream(stream))
     _check("rz_logits_loss_fwd_bwd", st)

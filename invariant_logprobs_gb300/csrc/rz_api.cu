@@ -178,7 +178,7 @@ size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
   switch (op) {
     case RZ_OP_TOKEN_LOGPROB: return fwd_layout(T, V > 0 ? V : 1).total;
     case RZ_OP_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
-    case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B);
+    case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B) + resp_scale_ws_bytes(B);
     case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
     case RZ_OP_SAMPLE: return sample_layout(T, V > 0 ? V : 1).total;
     default: return 0;
@@ -233,9 +233,9 @@ int rz_group_advantage(const float* rewards, int32_t B, int32_t G, float* adv_ou
 }
 
 int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens,
-               const float* adv, int32_t B, int64_t T, float* loss_out, float* d3_out,
-               float* coef_out, void* ws, size_t ws_bytes, int32_t* err_flag,
-               rz_stream_t stream) {
+               const float* adv, const uint8_t* action_mask, int32_t B, int64_t T,
+               float* loss_out, float* d3_out, float* coef_out, void* ws, size_t ws_bytes,
+               int32_t* err_flag, rz_stream_t stream) {
   if (B < 0 || T < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
   if (!loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
   if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
@@ -243,8 +243,8 @@ int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens
   const size_t need = rz_workspace_size(RZ_OP_IS_LOSS, T, 0, 0, B);
   if (need > 0 && (!ws || ws_bytes < need || !a256(ws))) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
-  return cuda_status(launch_is_loss(logpi, logmu, cu_seqlens, adv, B, T, loss_out, d3_out,
-                                    coef_out, ws, err_flag,
+  return cuda_status(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out,
+                                    d3_out, coef_out, ws, err_flag,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -274,10 +274,10 @@ int rz_peak_to_median(const float* series, int64_t n, double* ratio_out) {
 }
 
 int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, const float* logmu,
-                    const int64_t* cu_seqlens, const float* adv, int32_t B, int64_t T, int32_t d,
-                    int32_t V, float* loss_out, float* d3_out, float* logprob_out, rz_bf16* dH,
-                    float* dW, void* ws, size_t ws_bytes, int32_t* err_flag,
-                    rz_stream_t stream) {
+                    const int64_t* cu_seqlens, const float* adv, const uint8_t* action_mask,
+                    int32_t B, int64_t T, int32_t d, int32_t V, float* loss_out, float* d3_out,
+                    float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
+                    int32_t* err_flag, rz_stream_t stream) {
   if (!sizes_ok(T, d, V) || B < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
   if (!W || !dW || !loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
   if (T > 0 && (!H || !tokens || !logmu || !dH)) return RZ_ERR_INVALID_ARG;
@@ -292,8 +292,8 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
 
   if (T == 0) {
     RZ_TRY(cudaMemsetAsync(dW, 0, size_t(V) * size_t(d) * sizeof(float), st));
-    RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, B, 0, loss_out, d3_out, nullptr,
-                          w8 + L.resp, err_flag, st));
+    RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, nullptr, B, 0, loss_out, d3_out,
+                          nullptr, w8 + L.resp, err_flag, st));
     return RZ_OK;
   }
 
@@ -305,8 +305,8 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
   if (s != RZ_OK) return s;
 
   // 2. loss, D3 and the per-token coefficient c_t = A_i w_t / (B T_i).
-  RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, B, T, loss_out, d3_out, coef, w8 + L.resp,
-                        err_flag, st));
+  RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out, coef,
+                        w8 + L.resp, err_flag, st));
 
   // 3. backward, chunk by chunk in row order.
   uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
@@ -332,9 +332,10 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
 }
 
 int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const float* logmu,
-                           const int64_t* cu_seqlens, const float* adv, int32_t B, int64_t T,
-                           int32_t V, float* loss_out, float* d3_out, float* logprob_out,
-                           void* ws, size_t ws_bytes, int32_t* err_flag, rz_stream_t stream) {
+                           const int64_t* cu_seqlens, const float* adv,
+                           const uint8_t* action_mask, int32_t B, int64_t T, int32_t V,
+                           float* loss_out, float* d3_out, float* logprob_out, void* ws,
+                           size_t ws_bytes, int32_t* err_flag, rz_stream_t stream) {
   if (T < 0 || T >= (int64_t(1) << 31) || V < 1 || V > (1 << 24) || B < 0 || (B == 0 && T > 0))
     return RZ_ERR_INVALID_ARG;
   if (!loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
@@ -345,10 +346,13 @@ int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const f
   if (need > 0 && (!ws || ws_bytes < need || !a256(ws))) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, adv, B, logprob_out,
-                            err_flag, st));
-  RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, B, T, loss_out, d3_out, nullptr, ws,
-                        err_flag, st));
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  float* scale = reinterpret_cast<float*>(w8 + is_loss_ws_bytes(B));
+  RZ_TRY(launch_resp_scale(cu_seqlens, adv, action_mask, B, T, scale, st));
+  RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, scale, action_mask, B,
+                            logprob_out, err_flag, st));
+  RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
+                        nullptr, ws, err_flag, st));
   return RZ_OK;
 }
 

@@ -62,8 +62,11 @@ cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64
 size_t is_loss_ws_bytes(int32_t B);
 cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cudaStream_t st);
 cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
-                           const float* adv, int B, int64_t T, float* loss, float* d3,
-                           float* coef, void* ws, int* err, cudaStream_t st);
+                           const float* adv, const uint8_t* mask, int B, int64_t T, float* loss,
+                           float* d3, float* coef, void* ws, int* err, cudaStream_t st);
+size_t resp_scale_ws_bytes(int32_t B);
+cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
+                              int64_t T, float* scale, cudaStream_t st);
 cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
                       cudaStream_t st);
 cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, float* out,
@@ -71,7 +74,8 @@ cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, f
 
 // ---- given-logits kernel (rz_logits.cu)
 cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
-                               const float* logmu, const int64_t* cu, const float* adv, int B,
-                               float* logprob, int* err, cudaStream_t st);
+                               const float* logmu, const int64_t* cu, const float* scale,
+                               const uint8_t* mask, int B, float* logprob, int* err,
+                               cudaStream_t st);
 
 }  // namespace rz

@@ -70,8 +70,9 @@ __device__ __forceinline__ uint4 dz8(const uint4& q, float nl, float c, int rel)
 __global__ void __launch_bounds__(kRowThreads)
     logits_row_kernel(uint16_t* __restrict__ logits, long long T, int V,
                       const int32_t* __restrict__ tokens, const float* __restrict__ logmu,
-                      const int64_t* __restrict__ cu, const float* __restrict__ adv, int B,
-                      float* __restrict__ logprob, int* err) {
+                      const int64_t* __restrict__ cu, const float* __restrict__ scale,
+                      const uint8_t* __restrict__ mask, int B, float* __restrict__ logprob,
+                      int* err) {
   extern __shared__ uint4 stash[];
   __shared__ float red_m[kRowThreads / 32], red_s[kRowThreads / 32];
   __shared__ float bc[3];
@@ -133,9 +134,9 @@ __global__ void __launch_bounds__(kRowThreads)
         if (cu[mid] <= row) lo = mid;
         else hi = mid;
       }
-      const long long Ti = cu[lo + 1] - cu[lo];
-      const float inv_bt = Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
-      c = adv[lo] * is_weight(lp, logmu[row]) * inv_bt;
+      // c_t = A_i w_t / (B T_i); 0 for a masked (non-action) token
+      const bool act = !mask || mask[row] != 0;
+      c = act ? scale[lo] * is_weight(lp, logmu[row]) : 0.f;
     }
     logprob[row] = lp;
     bc[0] = -l2;
@@ -171,15 +172,16 @@ __global__ void __launch_bounds__(kRowThreads)
 }  // namespace
 
 cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
-                               const float* logmu, const int64_t* cu, const float* adv, int B,
-                               float* logprob, int* err, cudaStream_t st) {
+                               const float* logmu, const int64_t* cu, const float* scale,
+                               const uint8_t* mask, int B, float* logprob, int* err,
+                               cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(logits_row_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kRowSmem));
   if (e != cudaSuccess) return e;
   logits_row_kernel<<<static_cast<unsigned>(T), kRowThreads, kRowSmem, st>>>(
-      logits, T, V, tokens, logmu, cu, adv, B, logprob, err);
+      logits, T, V, tokens, logmu, cu, scale, mask, B, logprob, err);
   return cudaGetLastError();
 }
 

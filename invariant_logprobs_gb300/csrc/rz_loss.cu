@@ -7,6 +7,10 @@
 //   D3   = (1/T) sum_t (w_t - 1 - log w_t)                   (vLLM post s.3)
 //   c_t  = A_i w_t / (B T_i) = -dL/dlog pi_t
 //
+// An optional action mask removes tokens from every sum ("T_i counts valid
+// action tokens", project page s.02): T_i is the number of valid tokens of
+// response i, D3 averages over valid tokens, and c_t = 0 for masked tokens.
+//
 // Numerics: w = 1 + expm1(log pi - log mu), so the loss is evaluated as
 //   L = -(1/B) [ sum_i A_i  +  sum_i A_i (1/T_i) sum_t expm1(d_t) ]
 // over responses with T_i > 0; the first sum is exact for centred rewards
@@ -32,14 +36,26 @@ struct RespPart {
   double lag;   // A_i (1/T_i) sum_t expm1(d_t)
   double base;  // A_i if T_i > 0 else 0
   double d3;    // sum_t (w_t - 1 - log w_t)
+  double cnt;   // T_i (valid tokens of the response)
 };
+
+// Valid tokens of response [s, e): all of them, or those with mask != 0.
+__device__ __forceinline__ long long valid_count(const uint8_t* mask, long long s, long long e,
+                                                 int* red) {
+  if (!mask) return e - s;
+  int c = 0;
+  for (long long t = s + threadIdx.x; t < e; t += kRespThreads) c += mask[t] != 0;
+  return block_sum<int, kRespThreads>(c, red);  // valid in thread 0
+}
 
 __global__ void __launch_bounds__(kRespThreads)
     is_loss_resp_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu,
-                        const int64_t* __restrict__ cu, const float* __restrict__ adv, int B,
-                        long long T, float* __restrict__ coef, RespPart* __restrict__ part,
-                        int* err) {
+                        const int64_t* __restrict__ cu, const float* __restrict__ adv,
+                        const uint8_t* __restrict__ mask, int B, long long T,
+                        float* __restrict__ coef, RespPart* __restrict__ part, int* err) {
   __shared__ float red[kRespThreads / 32];
+  __shared__ int redi[kRespThreads / 32];
+  __shared__ long long nvalid;
   const int i = blockIdx.x;
   long long s = cu[i];
   long long e = cu[i + 1];
@@ -49,16 +65,22 @@ __global__ void __launch_bounds__(kRespThreads)
     if (s < 0 || s > T) s = 0;
     if (e < s || e > T) e = s;
   }
-  const long long Ti = e - s;
+  const long long v = valid_count(mask, s, e, redi);
+  if (threadIdx.x == 0) nvalid = v;
+  __syncthreads();
+  const long long Ti = nvalid;
   const float A = adv[i];
   const float inv_bt = Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
   float em1 = 0.f, d3s = 0.f;
   for (long long t = s + threadIdx.x; t < e; t += kRespThreads) {
+    const bool ok = !mask || mask[t] != 0;
     const float dl = logpi[t] - logmu[t];
     const float w = expf(dl);
-    if (coef) coef[t] = A * w * inv_bt;
-    em1 += expm1f(dl);
-    d3s += d3_term(dl);
+    if (coef) coef[t] = ok ? A * w * inv_bt : 0.f;
+    if (ok) {
+      em1 += expm1f(dl);
+      d3s += d3_term(dl);
+    }
   }
   const float em1_tot = block_sum<float, kRespThreads>(em1, red);
   const float d3_tot = block_sum<float, kRespThreads>(d3s, red);
@@ -68,26 +90,44 @@ __global__ void __launch_bounds__(kRespThreads)
                    : 0.0;
     r.base = Ti > 0 ? static_cast<double>(A) : 0.0;
     r.d3 = static_cast<double>(d3_tot);
+    r.cnt = static_cast<double>(Ti);
     part[i] = r;
   }
 }
 
+// Per-response coefficient A_i / (B T_i) (0 for an empty response), for the
+// given-logits kernel which forms c_t = scale_i w_t itself.
+__global__ void resp_scale_kernel(const int64_t* __restrict__ cu, const float* __restrict__ adv,
+                                  const uint8_t* __restrict__ mask, int B, long long T,
+                                  float* __restrict__ scale) {
+  __shared__ int redi[kRespThreads / 32];
+  const int i = blockIdx.x;
+  long long s = cu[i];
+  long long e = cu[i + 1];
+  if (s < 0 || s > T) s = 0;
+  if (e < s || e > T) e = s;
+  const long long Ti = valid_count(mask, s, e, redi);
+  if (threadIdx.x == 0)
+    scale[i] = Ti > 0 ? adv[i] * static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
+}
+
 __global__ void __launch_bounds__(kFinalThreads)
-    is_loss_final_kernel(const RespPart* __restrict__ part, int B, long long T, float* loss,
-                         float* d3) {
+    is_loss_final_kernel(const RespPart* __restrict__ part, int B, float* loss, float* d3) {
   __shared__ double red[kFinalThreads / 32];
-  double lag = 0.0, base = 0.0, dd = 0.0;
+  double lag = 0.0, base = 0.0, dd = 0.0, cnt = 0.0;
   for (int i = threadIdx.x; i < B; i += kFinalThreads) {
     lag += part[i].lag;
     base += part[i].base;
     dd += part[i].d3;
+    cnt += part[i].cnt;
   }
   const double lag_t = block_sum<double, kFinalThreads>(lag, red);
   const double base_t = block_sum<double, kFinalThreads>(base, red);
   const double d3_t = block_sum<double, kFinalThreads>(dd, red);
+  const double cnt_t = block_sum<double, kFinalThreads>(cnt, red);
   if (threadIdx.x == 0) {
     if (loss) *loss = B > 0 ? static_cast<float>(-(base_t + lag_t) / B) : 0.f;
-    if (d3) *d3 = T > 0 ? static_cast<float>(d3_t / static_cast<double>(T)) : 0.f;
+    if (d3) *d3 = cnt_t > 0 ? static_cast<float>(d3_t / cnt_t) : 0.f;
   }
 }
 
@@ -158,6 +198,11 @@ size_t is_loss_ws_bytes(int32_t B) {
   return (b * sizeof(RespPart) + 255) / 256 * 256;
 }
 
+size_t resp_scale_ws_bytes(int32_t B) {
+  const size_t b = B > 0 ? static_cast<size_t>(B) : 0;
+  return (b * sizeof(float) + 255) / 256 * 256;
+}
+
 cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
   const int threads = 256;
@@ -166,16 +211,23 @@ cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cud
 }
 
 cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
-                           const float* adv, int B, int64_t T, float* loss, float* d3,
-                           float* coef, void* ws, int* err, cudaStream_t st) {
+                           const float* adv, const uint8_t* mask, int B, int64_t T, float* loss,
+                           float* d3, float* coef, void* ws, int* err, cudaStream_t st) {
   RespPart* part = static_cast<RespPart*>(ws);
   if (B > 0) {
-    is_loss_resp_kernel<<<B, kRespThreads, 0, st>>>(logpi, logmu, cu, adv, B, T, coef, part,
-                                                    err);
+    is_loss_resp_kernel<<<B, kRespThreads, 0, st>>>(logpi, logmu, cu, adv, mask, B, T, coef,
+                                                    part, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, T, loss, d3);
+  is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, loss, d3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
+                              int64_t T, float* scale, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  resp_scale_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, B, T, scale);
   return cudaGetLastError();
 }
 

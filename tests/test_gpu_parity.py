@@ -192,3 +192,68 @@ def test_is_stats_vs_oracle(rz, T, spread):
     # layouts are allowed to differ by rounding; both must match the oracle)
     d3b = rz.rz_d3(logpi.to(DEV), logmu.to(DEV)).item()
     assert scalar_close(d3b, got["d3"])
+
+
+def _mask_for(cu, T, seed, frac=0.7):
+    rng = np.random.default_rng(seed)
+    m = (rng.random(T) < frac).astype(np.uint8)
+    if len(cu) > 3:
+        m[int(cu[1]):int(cu[2])] = 0   # one response without any action token
+    return m
+
+
+def test_learner_masked_vs_oracle(rz):
+    wl = synth.Workload("masked", 3, 4, 1, 180, 512, 5000, "bernoulli", 0.5, "uniform",
+                        4, 2e-3, 4343)
+    b = _tiny_inputs(wl)
+    cu = f64(b["cu"])
+    mask = _mask_for(cu, b["T"], 1)
+    out = rz.rz_loss_fwd_bwd(b["H"].to(DEV), b["W"].to(DEV), b["tokens"].to(DEV),
+                             b["logmu"].to(DEV), b["cu"].to(DEV), b["adv"].to(DEV),
+                             action_mask=torch.tensor(mask).to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.loss_fwd_bwd(f64(b["H"]), f64(b["W"]), f64(b["tokens"]), f64(b["logmu"]),
+                              cu, f64(b["adv"]), mask=mask)
+    _check_learner(out, ref)
+    assert bool(torch.all(out["dH"][torch.tensor(mask == 0).to(DEV)] == 0))
+
+
+@pytest.mark.parametrize("T,B", [(1_114_112, 128), (997, 9)])
+def test_is_loss_masked_vs_oracle(rz, T, B):
+    g = torch.Generator().manual_seed(T * 3 + B)
+    cuts = torch.sort(torch.randint(0, T + 1, (B - 1,), generator=g)).values
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64), cuts, torch.full((1,), T, dtype=torch.int64)])
+    logpi = -torch.rand(T, generator=g) * 12
+    logmu = logpi + torch.randn(T, generator=g) * 0.1
+    adv = torch.randn(B, generator=g)
+    mask = _mask_for(f64(cu), T, 2)
+    loss, d3, coef = rz.rz_is_loss(logpi.to(DEV), logmu.to(DEV), cu.to(DEV), adv.to(DEV),
+                                   coef_out=torch.empty(T, device=DEV),
+                                   action_mask=torch.tensor(mask).to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.is_loss(f64(logpi), f64(logmu), f64(cu), f64(adv), mask=mask)
+    assert scalar_close(loss.item(), ref["loss"]), (loss.item(), ref["loss"])
+    assert scalar_close(d3.item(), ref["d3"]), (d3.item(), ref["d3"])
+    np.testing.assert_allclose(f64(coef), ref["c"], rtol=1e-5, atol=1e-12)
+
+
+def test_logits_variant_masked_vs_oracle(rz):
+    T, V, B = 700, 2048, 7
+    g = torch.Generator().manual_seed(77)
+    logits = (torch.randn(T, V, generator=g) * 3.0).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    cu = torch.linspace(0, T, B + 1).round().to(torch.int64)
+    adv = torch.randn(B, generator=g)
+    logmu = torch.randn(T, generator=g) * 0.05 - 8.0
+    mask = _mask_for(f64(cu), T, 3)
+    ref = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), f64(logmu), f64(cu), f64(adv),
+                                     mask=mask)
+    buf = logits.to(DEV)
+    out = rz.rz_logits_loss_fwd_bwd(buf, tok.to(DEV), logmu.to(DEV), cu.to(DEV), adv.to(DEV),
+                                    action_mask=torch.tensor(mask).to(DEV))
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(out["logprob"]) - ref["logpi"])) <= TOL_LOGPI
+    assert scalar_close(out["loss"].item(), ref["loss"]), (out["loss"].item(), ref["loss"])
+    assert scalar_close(out["d3"].item(), ref["d3"]), (out["d3"].item(), ref["d3"])
+    assert rel_l2(f64(buf), ref["dz"]) <= TOL_GRAD_REL_L2
+    assert bool(torch.all(buf[torch.tensor(mask == 0).to(DEV)] == 0))
