@@ -272,6 +272,18 @@ RZ_API int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const in
                                     float* logprob_out, float* lse_out,
                                     int32_t* err_flag, rz_stream_t stream);
 
+/*
+ * Failure-detection self-test (no counterpart on the pages): launches one
+ * warp that waits, with the library's bounded pipeline wait, on a barrier
+ * nothing ever completes.  After limit_us microseconds (1 .. 2,000,000) the
+ * wait gives up, RZ_DEVERR_TIMEOUT is OR-ed into *err_flag (device int32,
+ * required) and *done_out (device int32, nullable) is set to 2 (1 would mean
+ * the barrier completed).  The GPU is neither faulted nor hung, and the
+ * context stays usable.
+ */
+RZ_API int rz_selftest_wait_timeout(int32_t* err_flag, int32_t* done_out, uint32_t limit_us,
+                                    rz_stream_t stream);
+
 /* Size in bytes of the built-in scratch used by rz_token_logprob_noalloc. */
 RZ_API size_t rz_noalloc_scratch_bytes(void);
 

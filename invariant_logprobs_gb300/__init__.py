@@ -56,6 +56,7 @@ _SIGNATURES = {
     "rz_token_logprob_noalloc": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P, _P, _P, _P]),
     "rz_noalloc_scratch_bytes": (_SZ, []),
     "rz_is_stats": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+    "rz_selftest_wait_timeout": (ctypes.c_int, [_P, _P, ctypes.c_uint32, _P]),
     "rz_sample_logprob": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, ctypes.c_uint64,
                                          _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_peak_to_median": (ctypes.c_int, [_P, _I64, _P]),
@@ -366,3 +367,11 @@ def rz_sample_logprob(H, W, seed, row_ids=None, tokens_out=None, logprob_out=Non
                                ws.numel(), _ptr(err_flag), _stream(stream))
     _check("rz_sample_logprob", st)
     return tokens_out, logprob_out
+
+
+def rz_selftest_wait_timeout(err_flag, done_out=None, limit_us=50000, stream=None):
+    """Run the bounded-wait self-test (see include/rz.h)."""
+    torch = _torch()
+    _need(err_flag, torch.int32, "err_flag")
+    _check("rz_selftest_wait_timeout", load().rz_selftest_wait_timeout(
+        _ptr(err_flag), _ptr(done_out), int(limit_us), _stream(stream)))

@@ -157,3 +157,19 @@ def test_host_argument_errors(rz):
     with pytest.raises(rz.RzError) as e:
         rz.rz_token_logprob(H, W, tok, ws=small[:1])
     assert e.value.status == rz.RZ_ERR_WORKSPACE
+
+
+def test_bounded_wait_gives_up_and_reports(rz):
+    """A pipeline wait on a barrier nothing completes returns after its limit
+    with RZ_DEVERR_TIMEOUT set; the context remains usable."""
+    import time
+    err = rz.new_err_flag(DEV)
+    done = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.perf_counter()
+    rz.rz_selftest_wait_timeout(err, done, limit_us=50000)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert err.item() & rz.RZ_DEVERR_TIMEOUT
+    assert done.item() == 2
+    assert 0.04 <= dt < 5.0, dt
+    assert torch.arange(10, device=DEV).sum().item() == 45
