@@ -255,10 +255,10 @@ RZ_API int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32
  * Same arguments and results as rz_token_logprob (bitwise the same output:
  * it runs the same kernels with the same launch shape), minus ws/ws_bytes.
  * Scratch is a fixed array inside the library of rz_noalloc_scratch_bytes()
- * bytes (8 MiB) on every GPU that loads the library, held until the process
- * exits.  It needs T * (8 * S + 4) bytes plus padding, S = min(8, ceil(V/256))
- * vocab splits -- about 123,000 rows at V = 151936; larger T returns
- * RZ_ERR_TOO_LARGE and enqueues nothing.
+ * bytes (32 MiB) on every GPU that loads the library, held until the
+ * process exits.  It needs T * (8 * S + 4) bytes plus padding, S = the
+ * number of vocab splits (at most 64; 60 at V = 151936) -- about 69,000 rows
+ * at V = 151936; larger T returns RZ_ERR_TOO_LARGE and enqueues nothing.
  *   - It never calls cudaMalloc/cudaFree or any allocating library routine.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.

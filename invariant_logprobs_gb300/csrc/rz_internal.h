@@ -12,11 +12,14 @@
 namespace rz {
 
 // Vocabulary split of the logprob pass: a function of V only (never of the
-// number of rows), so the per-row reduction order is batch-invariant.
+// number of rows), so the per-row reduction order is batch-invariant.  Up to
+// 64 splits (~9 tiles each at V = 151936) let a decode-sized batch of one
+// 128-row block still occupy 64 SMs.
+constexpr int kMaxVocabSplits = 64;
 inline int vocab_tiles(int V) { return (V + kBN - 1) / kBN; }
 inline int vocab_tiles_per_split(int V) {
   const int nt = vocab_tiles(V);
-  const int s = nt < 8 ? nt : 8;
+  const int s = nt < kMaxVocabSplits ? nt : kMaxVocabSplits;
   return (nt + s - 1) / s;
 }
 inline int vocab_splits(int V) {

@@ -29,7 +29,7 @@
 namespace rz {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
