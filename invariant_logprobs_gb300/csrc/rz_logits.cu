@@ -25,6 +25,33 @@ constexpr int kRowThreads = 512;
 constexpr int kStashVec = 6144;  // 96 KB of the row kept in shared memory
 constexpr size_t kRowSmem = kStashVec * sizeof(uint4);
 
+// L2 eviction priorities: the part of a row that pass 2 will read again from
+// L2 is loaded evict-last; everything read for the last time, and the dz
+// written back, is evict-first, so ~300 rows in flight keep their second
+// halves resident in the 129 MB L2.
+__device__ __forceinline__ uint64_t l2_policy_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_l2hint(const uint4* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_l2hint(uint4* ptr, const uint4& v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
@@ -82,6 +109,9 @@ __global__ void __launch_bounds__(kRowThreads)
   const int nvec = V >> 3;
   const int nstash = nvec < kStashVec ? nvec : kStashVec;
 
+  const uint64_t keep = l2_policy_last();
+  const uint64_t drop = l2_policy_first();
+
   // ---- pass 1: online (max, sum exp) in base 2
   float m2 = -INFINITY, s = 0.f;
   int i = threadIdx.x;
@@ -89,7 +119,10 @@ __global__ void __launch_bounds__(kRowThreads)
   for (; i + 3 * kRowThreads < nvec; i += 4 * kRowThreads) {
     uint4 q[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) q[u] = rowp[i + u * kRowThreads];
+    for (int u = 0; u < 4; ++u) {
+      const int ii = i + u * kRowThreads;
+      q[u] = ld_l2hint(rowp + ii, ii < nstash ? drop : keep);
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (i + u * kRowThreads < nstash) stash[i + u * kRowThreads] = q[u];
@@ -97,7 +130,7 @@ __global__ void __launch_bounds__(kRowThreads)
     }
   }
   for (; i < nvec; i += kRowThreads) {
-    const uint4 q0 = rowp[i];
+    const uint4 q0 = ld_l2hint(rowp + i, i < nstash ? drop : keep);
     if (i < nstash) stash[i] = q0;
     fold8(q0, m2, s);
   }
@@ -148,25 +181,27 @@ __global__ void __launch_bounds__(kRowThreads)
   const float c = bc[1];
   const int a = bci;
 
-  // ---- pass 2: dz = c (softmax - onehot), in place
-  int j = threadIdx.x;
-  for (; j + 3 * kRowThreads < nvec; j += 4 * kRowThreads) {
+  // ---- pass 2: dz = c (softmax - onehot), in place.  The part re-read from
+  // L2 goes first and backwards (most recently loaded lines first); the
+  // stashed head comes from shared memory.
+  const int R = nvec - nstash;
+  int k = threadIdx.x;
+  for (; k + 3 * kRowThreads < R; k += 4 * kRowThreads) {
     uint4 q[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int jj = j + u * kRowThreads;
-      q[u] = jj < nstash ? stash[jj] : rowp[jj];
-    }
+    for (int u = 0; u < 4; ++u) q[u] = ld_l2hint(rowp + (nvec - 1 - (k + u * kRowThreads)), drop);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int jj = j + u * kRowThreads;
-      rowp[jj] = dz8(q[u], nl, c, a - 8 * jj);
+      const int jj = nvec - 1 - (k + u * kRowThreads);
+      st_l2hint(rowp + jj, dz8(q[u], nl, c, a - 8 * jj), drop);
     }
   }
-  for (; j < nvec; j += kRowThreads) {
-    const uint4 q = j < nstash ? stash[j] : rowp[j];
-    rowp[j] = dz8(q, nl, c, a - 8 * j);
+  for (; k < R; k += kRowThreads) {
+    const int jj = nvec - 1 - k;
+    st_l2hint(rowp + jj, dz8(ld_l2hint(rowp + jj, drop), nl, c, a - 8 * jj), drop);
   }
+  for (int j = threadIdx.x; j < nstash; j += kRowThreads)
+    st_l2hint(rowp + j, dz8(stash[j], nl, c, a - 8 * j), drop);
 }
 
 }  // namespace
