@@ -105,15 +105,15 @@ SampleLayout sample_layout(int64_t T, int32_t V) {
 
 struct LearnLayout {
   FwdLayout fwd;
-  size_t logpi, lse2, coef, resp, dz, total;
+  size_t logpi, lse_ws, coef, resp, dz, total;
 };
 LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
   LearnLayout L{};
   const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
   L.fwd = fwd_layout(T, V);
   L.logpi = L.fwd.total;
-  L.lse2 = L.logpi + al256(t * 4);
-  L.coef = L.lse2 + al256(t * 4);
+  L.lse_ws = L.logpi + al256(t * 4);
+  L.coef = L.lse_ws + al256(t * 4);
   L.resp = L.coef + al256(t * 4);
   L.dz = L.resp + is_loss_ws_bytes(B);
   int64_t rows = chunk_rows(V);
@@ -139,7 +139,7 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RZ_OK : RZ_ERR
 
 // log pi for all T rows: identical launch sequence for rollout and learner.
 int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int64_t T, int32_t d,
-                 int32_t V, float* logprob, float* lse, float* lse2, uint8_t* ws, int* err,
+                 int32_t V, float* logprob, float* lse, float* lse_ws, uint8_t* ws, int* err,
                  cudaStream_t st) {
   if (T == 0) return RZ_OK;
   CUtensorMap tmH, tmW;
@@ -149,7 +149,7 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
   float2* part = reinterpret_cast<float2*>(ws + L.part);
   float* zg = reinterpret_cast<float*>(ws + L.zg);
   RZ_TRY(launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err, st));
-  RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse2, err, st));
+  RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse_ws, err, st));
   return RZ_OK;
 }
 
@@ -299,9 +299,9 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
 
   // 1. log pi for every row: the rollout's own launch sequence.
   float* logpi = logprob_out ? logprob_out : reinterpret_cast<float*>(w8 + L.logpi);
-  float* lse2 = reinterpret_cast<float*>(w8 + L.lse2);
+  float* lse_ws = reinterpret_cast<float*>(w8 + L.lse_ws);
   float* coef = reinterpret_cast<float*>(w8 + L.coef);
-  int s = logprob_pass(H, W, tokens, T, d, V, logpi, nullptr, lse2, w8, err_flag, st);
+  int s = logprob_pass(H, W, tokens, T, d, V, logpi, nullptr, lse_ws, w8, err_flag, st);
   if (s != RZ_OK) return s;
 
   // 2. loss, D3 and the per-token coefficient c_t = A_i w_t / (B T_i).
@@ -324,7 +324,7 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
       return RZ_ERR_UNSUPPORTED;
     if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
       return RZ_ERR_UNSUPPORTED;
-    RZ_TRY(launch_dlogits(tmH, tmW, r0, rows, d, V, tokens, lse2, coef, dz, ldz, err_flag, st));
+    RZ_TRY(launch_dlogits(tmH, tmW, r0, rows, d, V, tokens, lse_ws, coef, dz, ldz, err_flag, st));
     RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
     RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
   }

@@ -44,13 +44,13 @@ cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, i
                                int V, const int32_t* tokens, float2* part, float* zgather,
                                int* err, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const float2* part,
-                             const float* zgather, float* logprob, float* lse, float* lse2,
+                             const float* zgather, float* logprob, float* lse, float* lse_ws,
                              int* err, cudaStream_t st);
 cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
                           int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st);
 cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
-                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse2,
+                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse,
                            const float* coef, uint16_t* dz, int64_t ldz, int* err,
                            cudaStream_t st);
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,

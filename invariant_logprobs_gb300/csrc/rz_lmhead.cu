@@ -28,8 +28,8 @@
 namespace rz {
 
 // ============================================================== epilogues
-// Online log-sum-exp in base 2: state (m2, s) with m2 = max z*log2(e) so far
-// and s = sum 2^(z*log2(e) - m2); the row's logsumexp is (m2 + log2 s) ln 2.
+// Online log-sum-exp: state (m, s) with m = max z so far and
+// s = sum 2^((z - m) log2 e); the row's logsumexp is m + ln s.
 struct EpiLsePartial {
   struct Params {
     const int32_t* tokens;
@@ -40,7 +40,7 @@ struct EpiLsePartial {
     int S;
   };
   struct State {
-    float m2, s, za;
+    float m, s, za;
     int a;
     bool found;
   };
@@ -48,7 +48,7 @@ struct EpiLsePartial {
   static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk, int,
                                                     int row) {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
-    st.m2 = -INFINITY;
+    st.m = -INFINITY;
     st.s = 0.f;
     st.za = 0.f;
     st.found = false;
@@ -65,7 +65,7 @@ struct EpiLsePartial {
       for (int j = 0; j < 32; ++j)
         if (cbase + j >= p.V) v[j] = -INFINITY;
     }
-    lse_fold32(st.m2, st.s, v);
+    lse_fold32(st.m, st.s, v);
     const unsigned rel = static_cast<unsigned>(st.a - cbase);
     if (rel < 32u) {
 #pragma unroll
@@ -94,7 +94,7 @@ struct EpiLsePartial {
                                                   int row) {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
     if (g >= p.T) return;
-    p.part[g * p.S + grp] = make_float2(st.m2, st.s);
+    p.part[g * p.S + grp] = make_float2(st.m, st.s);
     if (st.found) p.zgather[g] = st.za;
   }
 };
@@ -141,7 +141,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
 struct EpiSample {
   struct Params {
     const int64_t* row_ids;  // nullable: row index
-    float4* part;            // [T, S]: m2, s, best key, z at best
+    float4* part;            // [T, S]: m, s, best key, z at best
     int* part_idx;           // [T, S]: best vocabulary index
     long long T;
     int V;
@@ -149,7 +149,7 @@ struct EpiSample {
     uint32_t k0, k1;
   };
   struct State {
-    float m2, s, bk, bz;
+    float m, s, bk, bz;
     int bi;
     uint32_t r_lo, r_hi;
   };
@@ -157,7 +157,7 @@ struct EpiSample {
   static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk, int,
                                                     int row) {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
-    st.m2 = -INFINITY;
+    st.m = -INFINITY;
     st.s = 0.f;
     st.bk = -INFINITY;
     st.bz = 0.f;
@@ -198,7 +198,7 @@ struct EpiSample {
       for (int j = 0; j < 32; ++j)
         if (cbase + j >= p.V) v[j] = -INFINITY;
     }
-    lse_fold32(st.m2, st.s, v);
+    lse_fold32(st.m, st.s, v);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const uint4 x4 = words[q ^ sw];
@@ -243,16 +243,16 @@ struct EpiSample {
                                                   int row) {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
     if (g >= p.T) return;
-    p.part[g * p.S + grp] = make_float4(st.m2, st.s, st.bk, st.bz);
+    p.part[g * p.S + grp] = make_float4(st.m, st.s, st.bk, st.bz);
     p.part_idx[g * p.S + grp] = st.bi;
   }
 };
 
-// dz_tv = c_t (2^(z log2e - lse2_t) - [v = a_t]) in bf16, one chunk of rows.
+// dz_tv = c_t (2^((z - lse_t) log2 e) - [v = a_t]) in bf16, one chunk of rows.
 struct EpiDlogits {
   struct Params {
     const int32_t* tokens;
-    const float* lse2;
+    const float* lse;
     const float* coef;
     uint16_t* dz;
     long long ldz;
@@ -261,7 +261,7 @@ struct EpiDlogits {
     int V;
   };
   struct State {
-    float nl, c;
+    float lse, c;
     int a;
     bool valid;
   };
@@ -273,11 +273,11 @@ struct EpiDlogits {
     if (st.valid) {
       const long long g = p.row0 + r;
       st.a = __ldg(p.tokens + g);
-      st.nl = -__ldg(p.lse2 + g);
+      st.lse = __ldg(p.lse + g);
       st.c = __ldg(p.coef + g);
     } else {
       st.a = -1;
-      st.nl = 0.f;
+      st.lse = 0.f;
       st.c = 0.f;
     }
   }
@@ -288,7 +288,7 @@ struct EpiDlogits {
     float g[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      g[j] = st.c * ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, st.nl));
+      g[j] = st.c * ex2_approx(__fmul_rn(__fsub_rn(__uint_as_float(r[j]), st.lse), kLog2e));
     const unsigned rel = static_cast<unsigned>(st.a - cbase);
     if (rel < 32u) {
 #pragma unroll
@@ -436,24 +436,24 @@ struct EpiStore {
 __global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __restrict__ tokens,
                                  const float2* __restrict__ part,
                                  const float* __restrict__ zgather, float* __restrict__ logprob,
-                                 float* __restrict__ lse, float* __restrict__ lse2_out, int* err) {
+                                 float* __restrict__ lse, float* __restrict__ lse_ws, int* err) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
-  float l2 = lse2_of_splits(part + t * S, S);
-  float l = __fmul_rn(l2, kLn2);
+  float sum;
+  const float M = lse_merge_parts(part + t * S, S, &sum);
+  float l = lse_from(M, sum);
   const int a = tokens[t];
   float lp;
   if (a < 0 || a >= V) {
     lp = __int_as_float(0x7fc00000);
     l = lp;
-    l2 = lp;
     if (err) atomicOr(err, 1);
   } else {
-    lp = logprob_from(zgather[t], l2);
+    lp = logprob_from(zgather[t], M, sum);
   }
   logprob[t] = lp;
   if (lse) lse[t] = l;
-  if (lse2_out) lse2_out[t] = l2;
+  if (lse_ws) lse_ws[t] = l;
 }
 
 // One thread per row: log-sum-exp exactly as lse_merge_kernel, and the
@@ -465,7 +465,8 @@ __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const float4* pp = part + t * S;
-  const float l2 = lse2_of_splits(pp, S);
+  float sum;
+  const float M = lse_merge_parts(pp, S, &sum);
   float bk = -INFINITY, bz = 0.f;
   int bi = 0;
   for (int g = 0; g < S; ++g) {
@@ -476,8 +477,8 @@ __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict
     }
   }
   tokens[t] = bi;
-  logprob[t] = logprob_from(bz, l2);
-  if (lse) lse[t] = __fmul_rn(l2, kLn2);
+  logprob[t] = logprob_from(bz, M, sum);
+  if (lse) lse[t] = lse_from(M, sum);
 }
 
 // ============================================================== launchers
@@ -530,13 +531,13 @@ cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, i
 }
 
 cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const float2* part,
-                             const float* zgather, float* logprob, float* lse, float* lse2,
+                             const float* zgather, float* logprob, float* lse, float* lse_ws,
                              int* err, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (T + threads - 1) / threads;
   lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      T, V, vocab_splits(V), tokens, part, zgather, logprob, lse, lse2, err);
+      T, V, vocab_splits(V), tokens, part, zgather, logprob, lse, lse_ws, err);
   return cudaGetLastError();
 }
 
@@ -560,7 +561,7 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
 }
 
 cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
-                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse2,
+                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse,
                            const float* coef, uint16_t* dz, int64_t ldz, int* err,
                            cudaStream_t st) {
   const int S = vocab_splits(V);
@@ -568,7 +569,7 @@ cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64
   s.tiles_per_group = vocab_tiles_per_split(V);
   s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
-  EpiDlogits::Params p{tokens, lse2, coef, dz, ldz, row0, rows, V};
+  EpiDlogits::Params p{tokens, lse, coef, dz, ldz, row0, rows, V};
   return run_gemm<EpiDlogits, false, false>(tmH, tmW, s, p, st);
 }
 

@@ -15,9 +15,10 @@
 namespace rz {
 
 // Fold 32 logits (natural units; -inf marks a column past V) into the running
-// base-2 state (m2 = max z*log2(e), s = sum 2^(z*log2(e) - m2)).  The caller
-// guarantees at least one finite logit.
-__device__ __forceinline__ void lse_fold32(float& m2, float& s, const float (&v)[32]) {
+// state (m = max z so far, s = sum 2^((z - m) log2 e)).  z - m is exact for
+// the maximum itself, whose term is exactly 1.  The caller guarantees at
+// least one finite logit.
+__device__ __forceinline__ void lse_fold32(float& m, float& s, const float (&v)[32]) {
   float mx[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
   for (int j = 4; j < 32; j += 4) {
@@ -26,32 +27,39 @@ __device__ __forceinline__ void lse_fold32(float& m2, float& s, const float (&v)
     mx[2] = fmaxf(mx[2], v[j + 2]);
     mx[3] = fmaxf(mx[3], v[j + 3]);
   }
-  const float cm2 = __fmul_rn(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), kLog2e);
-  if (cm2 > m2) {
-    s = __fmul_rn(s, ex2_approx(__fsub_rn(m2, cm2)));
-    m2 = cm2;
+  const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  if (cm > m) {
+    s = __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, cm), kLog2e)));
+    m = cm;
   }
-  const float nm = -m2;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j & 3] = __fadd_rn(acc[j & 3], ex2_approx(fmaf(v[j], kLog2e, nm)));
+  for (int j = 0; j < 32; ++j)
+    acc[j & 3] = __fadd_rn(acc[j & 3], ex2_approx(__fmul_rn(__fsub_rn(v[j], m), kLog2e)));
   s = __fadd_rn(s, __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])));
 }
 
-// Merge the S split states of a row in split order -> log2-sum-exp.
-// P is any struct with .x = m2 and .y = s (float2, float4).
+// Merge the partial states of a row in a fixed order.  P is any struct with
+// .x = m and .y = s (float2, float4).  Returns M = max m and sets *sum to the
+// row's sum 2^((z - M) log2 e) over the whole vocabulary.
 template <class P>
-__device__ __forceinline__ float lse2_of_splits(const P* pp, int S) {
+__device__ __forceinline__ float lse_merge_parts(const P* pp, int S, float* sum) {
   float M = -INFINITY;
   for (int g = 0; g < S; ++g) M = fmaxf(M, pp[g].x);
-  float sum = 0.f;
-  for (int g = 0; g < S; ++g) sum = fmaf(pp[g].y, exp2f(__fsub_rn(pp[g].x, M)), sum);
-  return __fadd_rn(M, log2f(sum));
+  float acc = 0.f;
+  for (int g = 0; g < S; ++g)
+    acc = fmaf(pp[g].y, exp2f(__fmul_rn(__fsub_rn(pp[g].x, M), kLog2e)), acc);
+  *sum = acc;
+  return M;
 }
 
-// log pi = z_a - lse, lse = lse2 * ln 2.
-__device__ __forceinline__ float logprob_from(float za, float lse2) {
-  return __fsub_rn(za, __fmul_rn(lse2, kLn2));
+// log pi = (z_a - M) - ln(sum): exactly 0 when a is the only token, and
+// logsumexp = M + ln(sum).
+__device__ __forceinline__ float logprob_from(float za, float M, float sum) {
+  return __fsub_rn(__fsub_rn(za, M), __fmul_rn(log2f(sum), kLn2));
+}
+__device__ __forceinline__ float lse_from(float M, float sum) {
+  return __fadd_rn(M, __fmul_rn(log2f(sum), kLn2));
 }
 
 }  // namespace rz

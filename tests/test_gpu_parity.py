@@ -257,3 +257,64 @@ def test_logits_variant_masked_vs_oracle(rz):
     assert scalar_close(out["d3"].item(), ref["d3"]), (out["d3"].item(), ref["d3"])
     assert rel_l2(f64(buf), ref["dz"]) <= TOL_GRAD_REL_L2
     assert bool(torch.all(buf[torch.tensor(mask == 0).to(DEV)] == 0))
+
+
+@pytest.mark.parametrize("T,d,V", [(5, 8, 37), (64, 4096, 1000)])
+def test_learner_extreme_d(rz, T, d, V):
+    wl = synth.Workload("extreme_d", 1, 2, T // 2, T // 2, d, V, "uniform", 0.0, "uniform",
+                        4, 1e-2, 55 + d)
+    b = _tiny_inputs(wl)
+    out = _run_learner(rz, b)
+    ref = oracle.loss_fwd_bwd(f64(b["H"]), f64(b["W"]), f64(b["tokens"]), f64(b["logmu"]),
+                              f64(b["cu"]), f64(b["adv"]))
+    _check_learner(out, ref)
+
+
+def test_single_token_vocabulary(rz):
+    # V = 1: softmax is 1, log pi = 0 exactly, dz = c (1 - 1) = 0
+    T, d = 40, 64
+    H = torch.randn(T, d).to(torch.bfloat16).to(DEV)
+    W = torch.randn(1, d).to(torch.bfloat16).to(DEV)
+    tok = torch.zeros(T, dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0, 15, 40], dtype=torch.int64, device=DEV)
+    adv = torch.tensor([1.0, -1.0], device=DEV)
+    logmu = torch.full((T,), -0.5, device=DEV)
+    out = rz.rz_loss_fwd_bwd(H, W, tok, logmu, cu, adv)
+    torch.cuda.synchronize()
+    assert bool(torch.all(out["logprob"] == 0.0))
+    assert bool(torch.all(out["dH"] == 0)) and bool(torch.all(out["dW"] == 0))
+    ref = oracle.is_loss(np.zeros(T), np.full(T, -0.5), f64(cu), f64(adv))
+    assert scalar_close(out["loss"].item(), ref["loss"])
+    assert scalar_close(out["d3"].item(), ref["d3"])
+
+
+@pytest.mark.parametrize("T", [38912, 38913])
+def test_learner_chunk_boundary(rz, T):
+    # exactly one backward chunk, and one row into a second chunk
+    g = torch.Generator().manual_seed(T)
+    d, V, B = 64, 256, 4
+    H = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g) * 0.1).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    cu = torch.tensor([0, 1000, 20000, T - 1, T], dtype=torch.int64)
+    adv = torch.tensor([0.3, -0.2, 0.5, -0.6])
+    lm = torch.tensor(oracle.token_logprob(f64(H), f64(W), f64(tok))[0], dtype=torch.float32)
+    lm = lm + torch.randn(T, generator=g) * 0.05
+    out = rz.rz_loss_fwd_bwd(H.to(DEV), W.to(DEV), tok.to(DEV), lm.to(DEV), cu.to(DEV), adv.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.loss_fwd_bwd(f64(H), f64(W), f64(tok), f64(lm), f64(cu), f64(adv))
+    _check_learner(out, ref)
+
+
+def test_equal_rewards_give_zero_advantage_loss_and_gradients(rz):
+    # a group whose rewards are all equal has A = 0: no loss, no gradient
+    wl = synth.Workload("flat", 1, 6, 20, 50, 128, 700, "uniform", 0.0, "uniform", 4, 1e-2, 9)
+    b = _tiny_inputs(wl)
+    r = torch.full((6,), 0.37)
+    adv = rz.rz_group_advantage(r.to(DEV), 6)
+    out = rz.rz_loss_fwd_bwd(b["H"].to(DEV), b["W"].to(DEV), b["tokens"].to(DEV),
+                             b["logmu"].to(DEV), b["cu"].to(DEV), adv)
+    torch.cuda.synchronize()
+    assert bool(torch.all(adv == 0))
+    assert out["loss"].item() == 0.0
+    assert bool(torch.all(out["dH"] == 0)) and bool(torch.all(out["dW"] == 0))
