@@ -121,6 +121,17 @@ def _need(t, dtype, name):
         raise TypeError("%s must be a contiguous CUDA tensor of %s" % (name, dtype))
 
 
+def _shape(t, shape, name):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _same_device(*ts):
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) > 1:
+        raise ValueError("all tensors must be on one CUDA device, got %s" % sorted(map(str, devs)))
+
+
 def alloc_workspace(op, T, d, V, B, device):
     torch = _torch()
     n = workspace_size(op, T, d, V, B)
@@ -144,8 +155,16 @@ def rz_token_logprob(H, W, tokens, logprob_out=None, lse_out=None, ws=None, err_
     _need(tokens, torch.int32, "tokens")
     T, d = H.shape
     V = W.shape[0]
+    _shape(W, (V, d), "W")
+    _shape(tokens, (T,), "tokens")
     if logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=H.device)
+    _need(logprob_out, torch.float32, "logprob_out")
+    _shape(logprob_out, (T,), "logprob_out")
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out")
+        _shape(lse_out, (T,), "lse_out")
+    _same_device(H, W, tokens, logprob_out, lse_out, ws, err_flag)
     if ws is None:
         ws = alloc_workspace(RZ_OP_TOKEN_LOGPROB, T, d, V, 0, H.device)
     st = lib.rz_token_logprob(_ptr(H), _ptr(W), _ptr(tokens), T, d, V, _ptr(logprob_out),
@@ -162,6 +181,9 @@ def rz_group_advantage(rewards, G, adv_out=None, stream=None):
     B = rewards.shape[0]
     if adv_out is None:
         adv_out = torch.empty_like(rewards)
+    _need(adv_out, torch.float32, "adv_out")
+    _shape(adv_out, (B,), "adv_out")
+    _same_device(rewards, adv_out)
     _check("rz_group_advantage",
            lib.rz_group_advantage(_ptr(rewards), B, int(G), _ptr(adv_out), _stream(stream)))
     return adv_out
@@ -172,8 +194,18 @@ def rz_is_loss(logpi, logmu, cu_seqlens, adv, loss_out=None, d3_out=None, coef_o
     torch = _torch()
     lib = load()
     _need(cu_seqlens, torch.int64, "cu_seqlens")
+    _need(logpi, torch.float32, "logpi")
+    _need(logmu, torch.float32, "logmu")
+    _need(adv, torch.float32, "adv")
     B = cu_seqlens.shape[0] - 1
     T = logpi.shape[0]
+    _shape(logmu, (T,), "logmu")
+    _shape(adv, (B,), "adv")
+    if coef_out is not None:
+        _need(coef_out, torch.float32, "coef_out")
+        _shape(coef_out, (T,), "coef_out")
+    _shape(action_mask, (T,), "action_mask")
+    _same_device(logpi, logmu, cu_seqlens, adv, coef_out, action_mask, ws, err_flag)
     dev = cu_seqlens.device
     if loss_out is None:
         loss_out = torch.empty(1, dtype=torch.float32, device=dev)
@@ -196,6 +228,8 @@ def rz_d3(logpi, logmu, d3_out=None, stream=None):
     lib = load()
     _need(logpi, torch.float32, "logpi")
     _need(logmu, torch.float32, "logmu")
+    _shape(logmu, tuple(logpi.shape), "logmu")
+    _same_device(logpi, logmu)
     if d3_out is None:
         d3_out = torch.empty(1, dtype=torch.float32, device=logpi.device)
     _check("rz_d3", lib.rz_d3(_ptr(logpi), _ptr(logmu), logpi.shape[0], _ptr(d3_out),
@@ -219,6 +253,19 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
     T, d = H.shape
     V = W.shape[0]
     B = cu_seqlens.shape[0] - 1
+    _shape(W, (V, d), "W")
+    _shape(tokens, (T,), "tokens")
+    _shape(logmu, (T,), "logmu")
+    _shape(adv, (B,), "adv")
+    _shape(action_mask, (T,), "action_mask")
+    for t, n, dt, sh in ((logprob_out, "logprob_out", torch.float32, (T,)),
+                         (dH, "dH", torch.bfloat16, (T, d)),
+                         (dW, "dW", torch.float32, (V, d))):
+        if t is not None:
+            _need(t, dt, n)
+            _shape(t, sh, n)
+    _same_device(H, W, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out, dH, dW, ws,
+                 err_flag)
     dev = H.device
     if want_logprob and logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -255,6 +302,13 @@ def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob
     _need(adv, torch.float32, "adv")
     T, V = logits_inout.shape
     B = cu_seqlens.shape[0] - 1
+    _shape(tokens, (T,), "tokens")
+    _shape(logmu, (T,), "logmu")
+    _shape(adv, (B,), "adv")
+    _shape(action_mask, (T,), "action_mask")
+    _shape(logprob_out, (T,), "logprob_out")
+    _same_device(logits_inout, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out, ws,
+                 err_flag)
     dev = logits_inout.device
     if logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -282,8 +336,12 @@ def rz_lmhead_logits(H, W, logits_out=None, err_flag=None, stream=None):
     _need(W, torch.bfloat16, "W")
     T, d = H.shape
     V = W.shape[0]
+    _shape(W, (V, d), "W")
     if logits_out is None:
         logits_out = torch.empty((T, V), dtype=torch.float32, device=H.device)
+    _need(logits_out, torch.float32, "logits_out")
+    _shape(logits_out, (T, V), "logits_out")
+    _same_device(H, W, logits_out, err_flag)
     st = lib.rz_lmhead_logits(_ptr(H), _ptr(W), T, d, V, _ptr(logits_out), _ptr(err_flag),
                               _stream(stream))
     _check("rz_lmhead_logits", st)
@@ -305,6 +363,11 @@ def rz_token_logprob_noalloc(H, W, tokens, logprob_out, lse_out=None, err_flag=N
     _need(logprob_out, torch.float32, "logprob_out")
     T, d = H.shape
     V = W.shape[0]
+    _shape(W, (V, d), "W")
+    _shape(tokens, (T,), "tokens")
+    _shape(logprob_out, (T,), "logprob_out")
+    _shape(lse_out, (T,), "lse_out")
+    _same_device(H, W, tokens, logprob_out, lse_out, err_flag)
     st = lib.rz_token_logprob_noalloc(_ptr(H), _ptr(W), _ptr(tokens), T, d, V,
                                       _ptr(logprob_out), _ptr(lse_out), _ptr(err_flag),
                                       _stream(stream))
@@ -326,6 +389,8 @@ def rz_is_stats(logpi, logmu, stats_out=None, stream=None):
     lib = load()
     _need(logpi, torch.float32, "logpi")
     _need(logmu, torch.float32, "logmu")
+    _shape(logmu, tuple(logpi.shape), "logmu")
+    _same_device(logpi, logmu, stats_out)
     if stats_out is None:
         stats_out = torch.empty(7, dtype=torch.float32, device=logpi.device)
     _check("rz_is_stats", lib.rz_is_stats(_ptr(logpi), _ptr(logmu), logpi.shape[0],
@@ -355,6 +420,11 @@ def rz_sample_logprob(H, W, seed, row_ids=None, tokens_out=None, logprob_out=Non
         _need(row_ids, torch.int64, "row_ids")
     T, d = H.shape
     V = W.shape[0]
+    _shape(W, (V, d), "W")
+    _shape(row_ids, (T,), "row_ids")
+    _shape(tokens_out, (T,), "tokens_out")
+    _shape(logprob_out, (T,), "logprob_out")
+    _same_device(H, W, row_ids, tokens_out, logprob_out, lse_out, ws, err_flag)
     if tokens_out is None:
         tokens_out = torch.empty(T, dtype=torch.int32, device=H.device)
     if logprob_out is None:

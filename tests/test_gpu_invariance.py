@@ -173,3 +173,21 @@ def test_bounded_wait_gives_up_and_reports(rz):
     assert done.item() == 2
     assert 0.04 <= dt < 5.0, dt
     assert torch.arange(10, device=DEV).sum().item() == 45
+
+
+def test_binding_rejects_mismatched_shapes_before_launch(rz):
+    H = torch.randn(10, 16, device=DEV).to(torch.bfloat16)
+    W = torch.randn(30, 16, device=DEV).to(torch.bfloat16)
+    tok = torch.zeros(9, dtype=torch.int32, device=DEV)      # one short
+    with pytest.raises(ValueError):
+        rz.rz_token_logprob(H, W, tok)
+    cu = torch.tensor([0, 4, 10], dtype=torch.int64, device=DEV)
+    lm = torch.zeros(10, device=DEV)
+    with pytest.raises(ValueError):
+        rz.rz_loss_fwd_bwd(H, W, torch.zeros(10, dtype=torch.int32, device=DEV), lm, cu,
+                           torch.zeros(3, device=DEV))             # adv has B+1 entries
+    with pytest.raises(ValueError):
+        rz.rz_is_loss(lm, lm[:9], cu, torch.zeros(2, device=DEV))
+    W_bad = torch.randn(30, 8, device=DEV).to(torch.bfloat16)  # d mismatch
+    with pytest.raises(ValueError):
+        rz.rz_token_logprob(H, W_bad, torch.zeros(10, dtype=torch.int32, device=DEV))
