@@ -254,6 +254,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     samp_ms = statistics.mean(rev[k].elapsed_time(rev[k + 1]) for k in range(kr))
     del ws_s, tok_s
+    # same-box reference: cuBLAS bf16 GEMM of one chunk's shape, interleaved
+    ours_tf, cub_tf = gemm_vs_cublas(b["H"], b["W_mu"], b["tokens"], rz, dev, stream)
     clocks = clk.stop()
 
     # end to end through the public API from pinned host buffers
@@ -282,6 +284,10 @@ def run_ours(args):
             "frac": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
             "peak_source": "%s bf16_tflops_sustained" % peak_src,
             "traffic": None},
+        "same_box_interleaved": {"logprob_gemm_tflops": ours_tf, "cublas_bf16_tflops": cub_tf,
+                                 "ratio": ours_tf / cub_tf,
+                                 "note": "alternating 1.5 s runs, 3 rounds, medians; cuBLAS "
+                                         "[38912,d]x[d,V] bf16 with its output written"},
         "rollout_tokens_per_s": T / (roll_ms / 1e3),
         "rollout_sample_tokens_per_s": T / (samp_ms / 1e3),
         "clocks": clocks,
@@ -300,6 +306,49 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
+
+
+def gemm_vs_cublas(H, W, tokens, rz, dev, stream, rows=155648, seconds=1.5, rounds=3):
+    """Same-box reference for the logprob GEMM: alternate ~1.5 s of our
+    rz_token_logprob on `rows` rows with ~1.5 s of torch.matmul (cuBLAS) bf16
+    on [38912, d] x [d, V] (its output is written, ours is not), three times,
+    so both run under the same power and thermal state.  Returns median
+    TFLOP/s of each."""
+    import torch
+    T = min(rows, H.shape[0])
+    Hs, ts = H[:T], tokens[:T]
+    d, V = H.shape[1], W.shape[0]
+    ws = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    Hc = H[:38912]
+    out = torch.empty((Hc.shape[0], V), dtype=torch.bfloat16, device=dev)
+
+    def ours():
+        rz.rz_token_logprob(Hs, W, ts, logprob_out=lp, ws=ws)
+        return 2.0 * d * V * T
+
+    def cub():
+        torch.matmul(Hc, W.t(), out=out)
+        return 2.0 * Hc.shape[0] * d * V
+
+    res = {"ours": [], "cublas": []}
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(rounds):
+        for name, f in (("ours", ours), ("cublas", cub)):
+            f()
+            torch.cuda.synchronize()
+            fl, t = 0.0, 0.0
+            e0.record(stream)
+            while t < seconds * 1e3:
+                for _ in range(4):
+                    fl += f()
+                e1.record(stream)
+                e1.synchronize()
+                t = e0.elapsed_time(e1)
+            res[name].append(fl / (t / 1e3) / 1e12)
+    del out, ws
+    return statistics.median(res["ours"]), statistics.median(res["cublas"])
 
 
 def launches_per_step(T, V):
