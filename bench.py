@@ -26,6 +26,34 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) of one full-size logprob-GEMM launch of the
+# 4B-shaped workload, from the 1-pass ncu capture summarised in
+# profiles/logprob_gemm_dram_traffic_fullsize.md.  Valid only while the GEMM
+# sources hash to the value recorded with it; otherwise reported as null.
+TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 935.0e9 + 1.97e9,
+                   "sources_sha256_16": "f0efadb1912df1db"}
+GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_math.cuh",
+                "rz_internal.h"]
+
+
+def gemm_sources_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "invariant_logprobs_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(workload):
+    if workload != TRAFFIC_CAPTURE["workload"]:
+        return None
+    try:
+        ok = gemm_sources_hash() == TRAFFIC_CAPTURE["sources_sha256_16"]
+    except OSError:
+        ok = False
+    return TRAFFIC_CAPTURE["bytes"] if ok else None
 METRIC = "action tokens/s, fused logprob+IS-loss fwd/bwd (1 GB300); % bf16 tensor roofline"
 
 
@@ -283,7 +311,8 @@ def run_ours(args):
             "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
             "frac": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
             "peak_source": "%s bf16_tflops_sustained" % peak_src,
-            "traffic": None},
+            "traffic": captured_traffic(wl.name),
+            "traffic_unit": "bytes per launch (ncu capture, see profiles/)"},
         "same_box_interleaved": {"logprob_gemm_tflops": ours_tf, "cublas_bf16_tflops": cub_tf,
                                  "ratio": ours_tf / cub_tf,
                                  "note": "alternating 1.5 s runs, 3 rounds, medians; cuBLAS "
