@@ -36,10 +36,11 @@ bool device_ok() {
 }
 
 int64_t chunk_rows(int32_t V) {
-  // dz chunk of rows x round_up(V, 8) bf16, at most 16 GiB.
-  const int64_t per_row = dz_ld(V) * 2;
+  // one chunk keeps rows x round_up(V, 8) logits in fp32 and dz in bf16,
+  // at most 40 GiB together.
+  const int64_t per_row = dz_ld(V) * 6;
   int64_t rows = kChunkRowsMax;
-  const int64_t cap = (int64_t(16) << 30) / (per_row > 0 ? per_row : 1);
+  const int64_t cap = (int64_t(40) << 30) / (per_row > 0 ? per_row : 1);
   if (rows > cap) rows = cap / kBM * kBM;
   if (rows < kBM) rows = kBM;
   return rows;
@@ -104,21 +105,26 @@ SampleLayout sample_layout(int64_t T, int32_t V) {
 }
 
 struct LearnLayout {
-  FwdLayout fwd;
-  size_t logpi, lse_ws, coef, resp, dz, total;
+  int64_t rows;  // rows per chunk
+  FwdLayout fwd;  // split states of one chunk
+  size_t logpi, lse_ws, coef, resp, fac, z, dz, total;
 };
 LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
   LearnLayout L{};
   const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
-  L.fwd = fwd_layout(T, V);
-  L.logpi = L.fwd.total;
-  L.lse_ws = L.logpi + al256(t * 4);
-  L.coef = L.lse_ws + al256(t * 4);
-  L.resp = L.coef + al256(t * 4);
-  L.dz = L.resp + is_loss_ws_bytes(B);
   int64_t rows = chunk_rows(V);
   if (T < rows) rows = (T + kBM - 1) / kBM * kBM;
-  L.total = L.dz + al256(static_cast<size_t>(rows) * static_cast<size_t>(dz_ld(V)) * 2);
+  L.rows = rows;
+  const size_t r = static_cast<size_t>(rows);
+  L.fwd = fwd_layout(rows, V);
+  L.logpi = L.fwd.total;
+  L.lse_ws = L.logpi + al256(t * 4);
+  L.coef = L.lse_ws + al256(r * 4);
+  L.resp = L.coef + al256(r * 4);
+  L.fac = L.resp + is_loss_ws_bytes(B);
+  L.z = L.fac + resp_factors_ws_bytes(B);
+  L.dz = L.z + al256(r * static_cast<size_t>(dz_ld(V)) * 4);
+  L.total = L.dz + al256(r * static_cast<size_t>(dz_ld(V)) * 2);
   return L;
 }
 
@@ -297,37 +303,47 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
     return RZ_OK;
   }
 
-  // 1. log pi for every row: the rollout's own launch sequence.
   float* logpi = logprob_out ? logprob_out : reinterpret_cast<float*>(w8 + L.logpi);
-  float* lse_ws = reinterpret_cast<float*>(w8 + L.lse_ws);
-  float* coef = reinterpret_cast<float*>(w8 + L.coef);
-  int s = logprob_pass(H, W, tokens, T, d, V, logpi, nullptr, lse_ws, w8, err_flag, st);
-  if (s != RZ_OK) return s;
-
-  // 2. loss, D3 and the per-token coefficient c_t = A_i w_t / (B T_i).
-  RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out, coef,
-                        w8 + L.resp, err_flag, st));
-
-  // 3. backward, chunk by chunk in row order.
+  float* lse_c = reinterpret_cast<float*>(w8 + L.lse_ws);
+  float* coef_c = reinterpret_cast<float*>(w8 + L.coef);
+  float2* fac = reinterpret_cast<float2*>(w8 + L.fac);
+  float2* part = reinterpret_cast<float2*>(w8 + L.fwd.part);
+  float* zg = reinterpret_cast<float*>(w8 + L.fwd.zg);
+  float* z = reinterpret_cast<float*>(w8 + L.z);
   uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
   const int64_t ldz = dz_ld(V);
-  const int64_t Tc = chunk_rows(V);
   CUtensorMap tmH, tmW, tmWmn, tmHmn;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmWmn, W, d, V, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmHmn, H, d, T, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
-  for (int64_t r0 = 0; r0 < T; r0 += Tc) {
-    const int64_t rows = (T - r0) < Tc ? (T - r0) : Tc;
+
+  // (A_i, 1/(B T_i)) per response: all the coefficient needs besides w_t.
+  RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+
+  // Chunk by chunk in row order: logits once (kept in fp32) with the
+  // rollout's log-sum-exp fold, merge + c_t, dz, then dH and dW.
+  for (int64_t r0 = 0; r0 < T; r0 += L.rows) {
+    const int64_t rows = (T - r0) < L.rows ? (T - r0) : L.rows;
     CUtensorMap tmDz, tmDzMn;
     if (!make_tmap_bf16(&tmDz, dz, V, rows, uint64_t(ldz) * 2, kBK, kBM))
       return RZ_ERR_UNSUPPORTED;
     if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
       return RZ_ERR_UNSUPPORTED;
-    RZ_TRY(launch_dlogits(tmH, tmW, r0, rows, d, V, tokens, lse_ws, coef, dz, ldz, err_flag, st));
+    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, z, ldz, err_flag,
+                           st));
+    RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
+                                 logmu + r0, cu_seqlens, fac,
+                                 action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
+                                 st));
+    RZ_TRY(launch_dz_rows(z, ldz, dz, rows, V, tokens + r0, lse_c, coef_c, st));
     RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
     RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
   }
+
+  // Loss and D3 over all rows (fixed-order reductions).
+  RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
+                        nullptr, w8 + L.resp, err_flag, st));
   return RZ_OK;
 }
 

@@ -28,7 +28,8 @@ inline int vocab_splits(int V) {
   return (nt + tps - 1) / tps;
 }
 
-// Rows per backward chunk: dz for one chunk lives in the workspace.
+// Rows per backward chunk: the chunk's fp32 logits and bf16 dz live in the
+// workspace (6 bytes per logit).
 constexpr int64_t kChunkRowsMax = 38912;  // 256 * 152
 int64_t chunk_rows(int32_t V);
 inline int64_t dz_ld(int32_t V) { return (static_cast<int64_t>(V) + 7) / 8 * 8; }
@@ -49,9 +50,16 @@ cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const floa
 cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
                           int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st);
-cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
-                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse,
-                           const float* coef, uint16_t* dz, int64_t ldz, int* err,
+cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
+                            int64_t rows, int d, int V, const int32_t* tokens, float2* part,
+                            float* zgather, float* z, int64_t ldz, int* err, cudaStream_t st);
+cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32_t* tokens,
+                                  const float2* part, const float* zgather, float* logprob,
+                                  float* lse_ws, const float* logmu, const int64_t* cu,
+                                  const float2* fac, const uint8_t* mask, int B, float* coef,
+                                  int* err, cudaStream_t st);
+cudaError_t launch_dz_rows(const float* z, int64_t ldz, uint16_t* dz, int64_t rows, int V,
+                           const int32_t* tokens, const float* lse, const float* coef,
                            cudaStream_t st);
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                               int V, float* out, int* err, cudaStream_t st);
@@ -70,6 +78,9 @@ cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t
 size_t resp_scale_ws_bytes(int32_t B);
 cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
                               int64_t T, float* scale, cudaStream_t st);
+size_t resp_factors_ws_bytes(int32_t B);
+cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
+                                int64_t T, float2* fac, cudaStream_t st);
 cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
                       cudaStream_t st);
 cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, float* out,

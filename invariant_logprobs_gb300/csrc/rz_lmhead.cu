@@ -5,8 +5,11 @@
 //                (max, sum of exp) over the tiles of its vocab split, in
 //                ascending vocab order, and picks out z[t, a_t].
 //   lse_merge    fixed-order merge of the splits -> logsumexp, log pi.
-//   dlogits      (learner pass 2) recomputes the same z tiles and writes
-//                dz = c_t (softmax - onehot) as bf16 for one token chunk.
+//   lse_keep     (learner, one token chunk) the lse_partial fold on the
+//                same tiles, bitwise, plus the fp32 logits written out.
+//   merge_coef   the fixed-order merge, then c_t = A_i w_t / (B T_i).
+//   dz_rows      HBM pass: dz = c_t (softmax - onehot) as bf16 from the kept
+//                logits (the chunk's logits are never recomputed).
 //   dH, dW       dz W and dz^T H on the same tensor-core pipeline.
 //   logits_f32   plain z = H W^T (same tiles) for callers that want logits.
 //
@@ -96,6 +99,80 @@ struct EpiLsePartial {
     if (g >= p.T) return;
     p.part[g * p.S + grp] = make_float2(st.m, st.s);
     if (st.found) p.zgather[g] = st.za;
+  }
+};
+
+// Learner pass 1 for one chunk of rows: exactly the EpiLsePartial fold (so
+// log pi is the rollout's, bit for bit) and, next to it, the fp32 logits of
+// the chunk, so that the backward pass reads them instead of recomputing.
+struct EpiLseKeep {
+  struct Params {
+    EpiLsePartial::Params lse;  // chunk-local rows: T = rows of the chunk
+    float* z;                   // [rows, ldz] fp32
+    long long ldz;              // multiple of 4
+  };
+  using State = EpiLsePartial::State;
+
+  static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk,
+                                                    int grp, int row) {
+    EpiLsePartial::task_begin(p.lse, st, m_blk, grp, row);
+  }
+  static __device__ __forceinline__ void task_end(const Params& p, State& st, int m_blk, int grp,
+                                                  int row) {
+    EpiLsePartial::task_end(p.lse, st, m_blk, grp, row);
+  }
+
+  // 32 columns of the warp's 32 rows through the warp's stage (row r at
+  // r*128, 16-byte piece j at j ^ (r & 7)), then 8 store instructions that
+  // each write four whole 128-byte row segments.
+  static __device__ __forceinline__ void keep32(const Params& p, const uint32_t (&r)[32],
+                                                long long rbase, int lane, int cbase,
+                                                uint8_t* stage) {
+    uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mine[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int rr = 4 * k + (lane >> 3);
+      const int j = lane & 7;
+      const uint4 v = reinterpret_cast<const uint4*>(stage + rr * 128)[j ^ (rr & 7)];
+      const long long gr = rbase + rr;
+      const int col = cbase + 4 * j;
+      if (gr < p.lse.T && col < p.lse.V) {
+        float* dst = p.z + gr * p.ldz + col;
+        if (col + 4 <= p.lse.V) {
+          st_global_v4(dst, v.x, v.y, v.z, v.w);
+        } else {
+          for (int e = 0; col + e < p.lse.V; ++e)
+            dst[e] = __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : v.z));
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  static __device__ __forceinline__ void tile(const Params& p, State& st, int m_blk, int n_tile,
+                                              uint32_t taddr, int row, uint8_t* stage) {
+    const int col0 = n_tile * kBN;
+    const int V = p.lse.V;
+    const int lane = row & 31;
+    const long long rbase = static_cast<long long>(m_blk) * kBM + (row & ~31);
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 64) {
+      if (col0 + c >= V) break;  // warp-uniform
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr + c, r0);
+      tmem_ld32(taddr + c + 32, r1);
+      tmem_ld_wait();
+      EpiLsePartial::chunk(p.lse, st, r0, col0 + c);
+      keep32(p, r0, rbase, lane, col0 + c, stage);
+      if (col0 + c + 32 < V) {
+        EpiLsePartial::chunk(p.lse, st, r1, col0 + c + 32);
+        keep32(p, r1, rbase, lane, col0 + c + 32, stage);
+      }
+    }
   }
 };
 
@@ -303,108 +380,6 @@ struct EpiSample {
   }
 };
 
-// dz_tv = c_t (2^((z - lse_t) log2 e) - [v = a_t]) in bf16, one chunk of rows.
-struct EpiDlogits {
-  struct Params {
-    const int32_t* tokens;
-    const float* lse;
-    const float* coef;
-    uint16_t* dz;
-    long long ldz;
-    long long row0;
-    long long rows;
-    int V;
-  };
-  struct State {
-    float lse, c;
-    int a;
-    bool valid;
-  };
-
-  static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk, int,
-                                                    int row) {
-    const long long r = static_cast<long long>(m_blk) * kBM + row;
-    st.valid = r < p.rows;
-    if (st.valid) {
-      const long long g = p.row0 + r;
-      st.a = __ldg(p.tokens + g);
-      st.lse = __ldg(p.lse + g);
-      st.c = __ldg(p.coef + g);
-    } else {
-      st.a = -1;
-      st.lse = 0.f;
-      st.c = 0.f;
-    }
-  }
-
-  // 32 columns of this thread's row -> 16 packed bf16 pairs.
-  static __device__ __forceinline__ void chunk(const State& st, const uint32_t (&r)[32],
-                                               int cbase, uint32_t* w) {
-    float g[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      g[j] = st.c * ex2_approx(__fmul_rn(__fsub_rn(__uint_as_float(r[j]), st.lse), kLog2e));
-    const unsigned rel = static_cast<unsigned>(st.a - cbase);
-    if (rel < 32u) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (rel == static_cast<unsigned>(j)) g[j] -= st.c;
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
-  }
-
-  // Each 64-column slab goes through the warp's shared-memory stage so that
-  // every global store instruction writes four whole 128-byte lines (4 rows
-  // x 64 columns) instead of 32 scattered 16-byte pieces.  Staging layout:
-  // row r at r*128, 16-byte piece j at position j ^ (r & 7) (conflict-free
-  // both when each thread writes its row and when 8 threads read a row).
-  static __device__ __forceinline__ void tile(const Params& p, State& st, int m_blk, int n_tile,
-                                              uint32_t taddr, int row, uint8_t* stage) {
-    const int col0 = n_tile * kBN;
-    const int lane = row & 31;
-    const long long rbase = static_cast<long long>(m_blk) * kBM + (row & ~31);
-    uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
-#pragma unroll 1
-    for (int c = 0; c < kBN; c += 64) {
-      if (col0 + c >= p.V) break;  // warp-uniform
-      uint32_t r0[32], r1[32];
-      tmem_ld32(taddr + c, r0);
-      tmem_ld32(taddr + c + 32, r1);
-      tmem_ld_wait();
-      uint32_t w[32];
-      chunk(st, r0, col0 + c, w);
-      chunk(st, r1, col0 + c + 32, w + 16);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mine[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int r = 4 * k + (lane >> 3);
-        const int j = lane & 7;
-        const uint4 v = reinterpret_cast<const uint4*>(stage + r * 128)[j ^ (r & 7)];
-        const long long gr = rbase + r;
-        const int col = col0 + c + 8 * j;
-        if (gr < p.rows && col < p.V) {
-          uint16_t* dst = p.dz + gr * p.ldz + col;
-          if (col + 8 <= p.V) {
-            st_global_v4(dst, v.x, v.y, v.z, v.w);
-          } else {
-            for (int e = 0; col + e < p.V; ++e) {
-              const uint32_t word = e < 2 ? v.x : (e < 4 ? v.y : (e < 6 ? v.z : v.w));
-              dst[e] = static_cast<uint16_t>((word >> (16 * (e & 1))) & 0xffffu);
-            }
-          }
-        }
-      }
-      __syncwarp();
-    }
-  }
-
-  static __device__ __forceinline__ void task_end(const Params&, State&, int, int, int) {}
-};
-
 // Plain stores of the accumulator: bf16 (dH) or fp32 (logits), optionally
 // fp32 accumulate (dW over token chunks, in chunk order).
 template <int kMode>  // 0: bf16 store, 1: fp32 store, 2: fp32 accumulate-or-store
@@ -485,30 +460,128 @@ struct EpiStore {
   }
 };
 
-// ============================================================== merge kernel
-// One thread per row: merge the S split states in split order, then
-// log pi = z[t, a_t] - logsumexp.
+// ============================================================== merge kernels
+// Merge one row's S split states in split order; log pi = z[t, a_t] - lse.
+// An out-of-range token gives NaN for both and raises RZ_DEVERR_TOKEN_RANGE.
+__device__ __forceinline__ float merge_row(const float2* pp, int S, int V, int a,
+                                           const float* zg, float* l_out, int* err) {
+  float sum;
+  const float M = lse_merge_parts(pp, S, &sum);
+  if (a < 0 || a >= V) {
+    if (err) atomicOr(err, 1);
+    *l_out = __int_as_float(0x7fc00000);
+    return *l_out;
+  }
+  *l_out = lse_from(M, sum);
+  return logprob_from(*zg, M, sum);
+}
+
+// One thread per row.
 __global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __restrict__ tokens,
                                  const float2* __restrict__ part,
                                  const float* __restrict__ zgather, float* __restrict__ logprob,
                                  float* __restrict__ lse, float* __restrict__ lse_ws, int* err) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
-  float sum;
-  const float M = lse_merge_parts(part + t * S, S, &sum);
-  float l = lse_from(M, sum);
-  const int a = tokens[t];
-  float lp;
-  if (a < 0 || a >= V) {
-    lp = __int_as_float(0x7fc00000);
-    l = lp;
-    if (err) atomicOr(err, 1);
-  } else {
-    lp = logprob_from(zgather[t], M, sum);
-  }
+  float l;
+  const float lp = merge_row(part + t * S, S, V, tokens[t], zgather + t, &l, err);
   logprob[t] = lp;
   if (lse) lse[t] = l;
   if (lse_ws) lse_ws[t] = l;
+}
+
+// Learner, one chunk of rows (row0 = the chunk's first global row; every
+// other pointer is chunk-local except cu and fac): the merge above, then the
+// per-token coefficient c_t = A_i w_t / (B T_i), w_t = exp(log pi - log mu),
+// 0 for a masked token.  fac[i] = (A_i, 1/(B T_i)).  Response of a row: the
+// last i with cu[i] <= row (empty responses own no row).
+__global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long row0,
+                                      const int32_t* __restrict__ tokens,
+                                      const float2* __restrict__ part,
+                                      const float* __restrict__ zgather,
+                                      float* __restrict__ logprob, float* __restrict__ lse_ws,
+                                      const float* __restrict__ logmu,
+                                      const int64_t* __restrict__ cu,
+                                      const float2* __restrict__ fac,
+                                      const uint8_t* __restrict__ mask, int B,
+                                      float* __restrict__ coef, int* err) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= rows) return;
+  float l;
+  const float lp = merge_row(part + t * S, S, V, tokens[t], zgather + t, &l, err);
+  logprob[t] = lp;
+  lse_ws[t] = l;
+  const long long g = row0 + t;
+  int lo = 0, hi = B;  // cu[lo] <= g < cu[hi] for a valid cu
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= g) lo = mid;
+    else hi = mid;
+  }
+  const bool act = !mask || mask[t] != 0;
+  const float2 f = fac[lo];
+  coef[t] = act ? f.x * is_weight(lp, logmu[t]) * f.y : 0.f;
+}
+
+// ============================================================== dz pass
+// dz_tv = c_t (2^((z_tv - lse_t) log2 e) - [v = a_t]) in bf16, from the
+// kept fp32 logits of one chunk; one CTA per row, 8 columns per step (two
+// 16-byte loads, one 16-byte store), four steps in flight per thread.  Both
+// buffers have row stride ldz (a multiple of 8); columns >= V are not touched.
+constexpr int kDzThreads = 256;
+
+__device__ __forceinline__ float dz_of(float z, float lse, float c) {
+  return __fmul_rn(c, ex2_approx(__fmul_rn(__fsub_rn(z, lse), kLog2e)));
+}
+
+__device__ __forceinline__ uint4 dz8(const float4& lo, const float4& hi, float lse, float c,
+                                     int rel) {
+  float g[8] = {dz_of(lo.x, lse, c), dz_of(lo.y, lse, c), dz_of(lo.z, lse, c),
+                dz_of(lo.w, lse, c), dz_of(hi.x, lse, c), dz_of(hi.y, lse, c),
+                dz_of(hi.z, lse, c), dz_of(hi.w, lse, c)};
+  if (static_cast<unsigned>(rel) < 8u) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (rel == j) g[j] = __fsub_rn(g[j], c);
+  }
+  return make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
+                    pack_bf16x2(g[6], g[7]));
+}
+
+__global__ void __launch_bounds__(kDzThreads)
+    dz_rows_kernel(const float* __restrict__ z, long long ldz, uint16_t* __restrict__ dz,
+                   int V, const int32_t* __restrict__ tokens, const float* __restrict__ lse,
+                   const float* __restrict__ coef) {
+  const long long row = blockIdx.x;
+  const float4* zr = reinterpret_cast<const float4*>(z + row * ldz);
+  uint4* dr = reinterpret_cast<uint4*>(dz + row * ldz);
+  const float l = lse[row];
+  const float c = coef[row];
+  const int a = tokens[row];
+  const int n8 = V >> 3;
+  int i = threadIdx.x;
+  for (; i + 3 * kDzThreads < n8; i += 4 * kDzThreads) {
+    float4 q[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      q[2 * u] = __ldcs(zr + 2 * (i + u * kDzThreads));
+      q[2 * u + 1] = __ldcs(zr + 2 * (i + u * kDzThreads) + 1);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = i + u * kDzThreads;
+      __stcs(dr + k, dz8(q[2 * u], q[2 * u + 1], l, c, a - 8 * k));
+    }
+  }
+  for (; i < n8; i += kDzThreads)
+    __stcs(dr + i, dz8(__ldcs(zr + 2 * i), __ldcs(zr + 2 * i + 1), l, c, a - 8 * i));
+  // ragged tail: V % 8 columns
+  const int v = 8 * n8 + static_cast<int>(threadIdx.x);
+  if (v < V) {
+    float g = dz_of(z[row * ldz + v], l, c);
+    if (v == a) g = __fsub_rn(g, c);
+    dz[row * ldz + v] = static_cast<uint16_t>(pack_bf16x2(g, 0.f) & 0xffffu);
+  }
 }
 
 // One thread per row: log-sum-exp exactly as lse_merge_kernel, and the
@@ -615,17 +688,39 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
   return cudaGetLastError();
 }
 
-cudaError_t launch_dlogits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
-                           int64_t rows, int d, int V, const int32_t* tokens, const float* lse,
-                           const float* coef, uint16_t* dz, int64_t ldz, int* err,
-                           cudaStream_t st) {
+cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
+                            int64_t rows, int d, int V, const int32_t* tokens, float2* part,
+                            float* zgather, float* z, int64_t ldz, int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
   GemmSched s = sched_of(rows, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
   s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
-  EpiDlogits::Params p{tokens, lse, coef, dz, ldz, row0, rows, V};
-  return run_gemm<EpiDlogits, false, false>(tmH, tmW, s, p, st);
+  EpiLseKeep::Params p{{tokens, part, zgather, static_cast<long long>(rows), V, S}, z, ldz};
+  return run_gemm<EpiLseKeep, false, false>(tmH, tmW, s, p, st);
+}
+
+cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32_t* tokens,
+                                  const float2* part, const float* zgather, float* logprob,
+                                  float* lse_ws, const float* logmu, const int64_t* cu,
+                                  const float2* fac, const uint8_t* mask, int B, float* coef,
+                                  int* err, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (rows + threads - 1) / threads;
+  lse_merge_coef_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      rows, V, vocab_splits(V), row0, tokens, part, zgather, logprob, lse_ws, logmu, cu, fac,
+      mask, B, coef, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dz_rows(const float* z, int64_t ldz, uint16_t* dz, int64_t rows, int V,
+                           const int32_t* tokens, const float* lse, const float* coef,
+                           cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  dz_rows_kernel<<<static_cast<unsigned>(rows), kDzThreads, 0, st>>>(z, ldz, dz, V, tokens, lse,
+                                                                     coef);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,

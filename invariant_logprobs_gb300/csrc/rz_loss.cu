@@ -111,6 +111,24 @@ __global__ void resp_scale_kernel(const int64_t* __restrict__ cu, const float* _
     scale[i] = Ti > 0 ? adv[i] * static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
 }
 
+// Per-response factors (A_i, 1/(B T_i)) (second 0 for an empty response), for
+// the learner's chunked backward, which forms c_t = A_i w_t (1/(B T_i)) with
+// the same rounding as is_loss_resp_kernel's coefficient.
+__global__ void resp_factors_kernel(const int64_t* __restrict__ cu, const float* __restrict__ adv,
+                                    const uint8_t* __restrict__ mask, int B, long long T,
+                                    float2* __restrict__ fac) {
+  __shared__ int redi[kRespThreads / 32];
+  const int i = blockIdx.x;
+  long long s = cu[i];
+  long long e = cu[i + 1];
+  if (s < 0 || s > T) s = 0;
+  if (e < s || e > T) e = s;
+  const long long Ti = valid_count(mask, s, e, redi);
+  if (threadIdx.x == 0)
+    fac[i] = make_float2(adv[i],
+                         Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f);
+}
+
 __global__ void __launch_bounds__(kFinalThreads)
     is_loss_final_kernel(const RespPart* __restrict__ part, int B, float* loss, float* d3) {
   __shared__ double red[kFinalThreads / 32];
@@ -228,6 +246,18 @@ cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t
                               int64_t T, float* scale, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
   resp_scale_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, B, T, scale);
+  return cudaGetLastError();
+}
+
+size_t resp_factors_ws_bytes(int32_t B) {
+  const size_t b = B > 0 ? static_cast<size_t>(B) : 0;
+  return (b * sizeof(float2) + 255) / 256 * 256;
+}
+
+cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
+                                int64_t T, float2* fac, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  resp_factors_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, B, T, fac);
   return cudaGetLastError();
 }
 
