@@ -381,9 +381,11 @@ def gemm_vs_cublas(H, W, tokens, rz, dev, stream, rows=155648, seconds=1.5, roun
 
 
 def launches_per_step(T, V):
-    chunk = 38912
+    chunk = 38912  # rows per backward chunk at V = 151936 (6 bytes per logit kept, <= 40 GiB)
     n_chunks = (T + chunk - 1) // chunk
-    return 1 + 2 + 2 + 3 * n_chunks   # advantage; lse GEMM + merge; loss (2); per chunk 3
+    # advantage; response factors; per chunk: logits+lse GEMM, merge+coef, dz pass, dH, dW;
+    # loss (2)
+    return 1 + 1 + 5 * n_chunks + 2
 
 
 def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err):

@@ -273,9 +273,10 @@ __device__ __forceinline__ float lg2_approx(float x) {
 // go to the smaller vocabulary index.
 struct EpiSample {
   struct Params {
-    const int64_t* row_ids;  // nullable: row index
+    const int64_t* row_ids;  // nullable: row index (row0 + local row)
     float4* part;            // [T, S]: m, s, best key, z at best
     int* part_idx;           // [T, S]: best vocabulary index
+    long long row0;          // first row of this launch (row ids only)
     long long T;
     int V;
     int S;
@@ -295,7 +296,7 @@ struct EpiSample {
     st.bk = -INFINITY;
     st.bz = 0.f;
     st.bi = -1;
-    const long long rid = g < p.T ? (p.row_ids ? __ldg(p.row_ids + g) : g) : 0;
+    const long long rid = g < p.T ? (p.row_ids ? __ldg(p.row_ids + g) : p.row0 + g) : 0;
     st.rng.init(static_cast<uint32_t>(static_cast<unsigned long long>(rid) & 0xffffffffull),
                 static_cast<uint32_t>(static_cast<unsigned long long>(rid) >> 32), p.k0, p.k1);
   }
@@ -693,15 +694,27 @@ GemmSched sched_of(long long m_rows, int n_cols, int n_groups, long long k_depth
 
 }  // namespace
 
+// The vocab-split GEMMs over many rows are launched in row blocks of
+// kChunkRowsMax (120 tasks per CTA at V = 151936): with fixed round-robin
+// task order, CTAs of one long launch drift apart by many vocab splits and
+// lose the L2 sharing of W (several times the DRAM traffic, and under the
+// power cap a lower clock).  A row's result does not depend on the block.
 cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                                int V, const int32_t* tokens, float2* part, float* zgather,
                                int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
-  GemmSched s = sched_of(T, V, S, d, err);
-  s.tiles_per_group = vocab_tiles_per_split(V);
-  s.m_group = vocab_raster_group();
-  EpiLsePartial::Params p{tokens, part, zgather, static_cast<long long>(T), V, S};
-  return run_gemm<EpiLsePartial, false, false>(tmH, tmW, s, p, st);
+  for (int64_t r0 = 0; r0 < T; r0 += kChunkRowsMax) {
+    const int64_t rows = (T - r0) < kChunkRowsMax ? (T - r0) : kChunkRowsMax;
+    GemmSched s = sched_of(rows, V, S, d, err);
+    s.tiles_per_group = vocab_tiles_per_split(V);
+    s.m_group = vocab_raster_group();
+    s.a_m_off = static_cast<int>(r0);
+    EpiLsePartial::Params p{tokens + r0, part + r0 * S, zgather + r0,
+                            static_cast<long long>(rows), V, S};
+    cudaError_t e = run_gemm<EpiLsePartial, false, false>(tmH, tmW, s, p, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const float2* part,
@@ -719,14 +732,24 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
                           int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
-  GemmSched s = sched_of(T, V, S, d, err);
-  s.tiles_per_group = vocab_tiles_per_split(V);
-  s.m_group = vocab_raster_group();
-  EpiSample::Params p{row_ids, part, part_idx, static_cast<long long>(T), V, S,
-                      static_cast<uint32_t>(seed & 0xffffffffull),
-                      static_cast<uint32_t>(seed >> 32)};
-  cudaError_t e = run_gemm<EpiSample, false, false>(tmH, tmW, s, p, st);
-  if (e != cudaSuccess) return e;
+  for (int64_t r0 = 0; r0 < T; r0 += kChunkRowsMax) {  // row blocks as in launch_lse_partial
+    const int64_t rows = (T - r0) < kChunkRowsMax ? (T - r0) : kChunkRowsMax;
+    GemmSched s = sched_of(rows, V, S, d, err);
+    s.tiles_per_group = vocab_tiles_per_split(V);
+    s.m_group = vocab_raster_group();
+    s.a_m_off = static_cast<int>(r0);
+    EpiSample::Params p{row_ids ? row_ids + r0 : nullptr,
+                        part + r0 * S,
+                        part_idx + r0 * S,
+                        static_cast<long long>(r0),
+                        static_cast<long long>(rows),
+                        V,
+                        S,
+                        static_cast<uint32_t>(seed & 0xffffffffull),
+                        static_cast<uint32_t>(seed >> 32)};
+    cudaError_t e = run_gemm<EpiSample, false, false>(tmH, tmW, s, p, st);
+    if (e != cudaSuccess) return e;
+  }
   const int threads = 256;
   const long long blocks = (T + threads - 1) / threads;
   sample_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(T, S, part, part_idx,
@@ -772,11 +795,17 @@ cudaError_t launch_dz_rows(const float* z, int64_t ldz, uint16_t* dz, int64_t ro
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                               int V, float* out, int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
-  GemmSched s = sched_of(T, V, S, d, err);
-  s.tiles_per_group = vocab_tiles_per_split(V);
-  s.m_group = vocab_raster_group();
-  EpiStore<1>::Params p{out, V, 0, T, V, 0};
-  return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
+  for (int64_t r0 = 0; r0 < T; r0 += kChunkRowsMax) {  // row blocks as in launch_lse_partial
+    const int64_t rows = (T - r0) < kChunkRowsMax ? (T - r0) : kChunkRowsMax;
+    GemmSched s = sched_of(rows, V, S, d, err);
+    s.tiles_per_group = vocab_tiles_per_split(V);
+    s.m_group = vocab_raster_group();
+    s.a_m_off = static_cast<int>(r0);
+    EpiStore<1>::Params p{out, V, r0, rows, V, 0};
+    cudaError_t e = run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
