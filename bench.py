@@ -27,12 +27,13 @@ if ROOT not in sys.path:
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one full-size logprob-GEMM launch of the
-# 4B-shaped workload, from the 1-pass ncu capture summarised in
+# DRAM bytes (read + write) of one logprob-GEMM launch of the 4B-shaped
+# workload (one 38,912-row block of the 1,083,112 rows; mean of the 27 full
+# blocks of one call), from the 1-pass ncu capture summarised in
 # profiles/logprob_gemm_dram_traffic_fullsize.md.  Valid only while the GEMM
 # sources hash to the value recorded with it; otherwise reported as null.
-TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 935.0e9 + 1.97e9,
-                   "sources_sha256_16": "f0efadb1912df1db"}
+TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 5.314e9 + 0.0514e9,
+                   "rows_per_launch": 38912, "sources_sha256_16": "a7bdac1a56732ca5"}
 GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_math.cuh",
                 "rz_internal.h"]
 
@@ -256,7 +257,7 @@ def run_ours(args):
     total_ms = ev[0].elapsed_time(ev[-1])
 
     # dominant kernel, timed live: the LM-head logprob GEMM (rollout entry point,
-    # one tcgen05 GEMM launch + a tiny merge) over the same rows
+    # one tcgen05 GEMM launch per 38,912 rows + a tiny merge) over the same rows
     lp2 = torch.empty(T, dtype=torch.float32, device=dev)
     ws_r = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, dev)
     rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], logprob_out=lp2, ws=ws_r)
@@ -312,7 +313,11 @@ def run_ours(args):
             "frac": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
             "peak_source": "%s bf16_tflops_sustained" % peak_src,
             "traffic": captured_traffic(wl.name),
-            "traffic_unit": "bytes per launch (ncu capture, see profiles/)"},
+            "traffic_unit": "DRAM bytes per launch of 38,912 rows (ncu capture, see profiles/)",
+            # H block + W + the block's split states and gathered logits
+            "algorithmic_bytes_per_launch": 38912 * d * 2 + V * d * 2 +
+            rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 38912, d, V, 0),
+            "launches_per_call": (T + 38911) // 38912},
         "same_box_interleaved": {"logprob_gemm_tflops": ours_tf, "cublas_bf16_tflops": cub_tf,
                                  "ratio": ours_tf / cub_tf,
                                  "note": "alternating 1.5 s runs, 3 rounds, medians; cuBLAS "
