@@ -124,10 +124,12 @@ struct EpiLseKeep {
 
   // 32 columns of the warp's 32 rows through the warp's stage (row r at
   // r*128, 16-byte piece j at j ^ (r & 7)), then 8 store instructions that
-  // each write four whole 128-byte row segments.
+  // each write four whole 128-byte row segments.  The logits are written
+  // evict-first: they are read back only after the whole chunk, and would
+  // otherwise push the H and W tiles the CTAs share out of L2.
   static __device__ __forceinline__ void keep32(const Params& p, const uint32_t (&r)[32],
                                                 long long rbase, int lane, int cbase,
-                                                uint8_t* stage) {
+                                                uint8_t* stage, uint64_t pol) {
     uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -143,7 +145,7 @@ struct EpiLseKeep {
       if (gr < p.lse.T && col < p.lse.V) {
         float* dst = p.z + gr * p.ldz + col;
         if (col + 4 <= p.lse.V) {
-          st_global_v4(dst, v.x, v.y, v.z, v.w);
+          st_l2hint(reinterpret_cast<uint4*>(dst), v, pol);
         } else {
           for (int e = 0; col + e < p.lse.V; ++e)
             dst[e] = __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : v.z));
@@ -159,6 +161,7 @@ struct EpiLseKeep {
     const int V = p.lse.V;
     const int lane = row & 31;
     const long long rbase = static_cast<long long>(m_blk) * kBM + (row & ~31);
+    const uint64_t pol = l2_policy_first();
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 64) {
       if (col0 + c >= V) break;  // warp-uniform
@@ -167,10 +170,10 @@ struct EpiLseKeep {
       tmem_ld32(taddr + c + 32, r1);
       tmem_ld_wait();
       EpiLsePartial::chunk(p.lse, st, r0, col0 + c);
-      keep32(p, r0, rbase, lane, col0 + c, stage);
+      keep32(p, r0, rbase, lane, col0 + c, stage, pol);
       if (col0 + c + 32 < V) {
         EpiLsePartial::chunk(p.lse, st, r1, col0 + c + 32);
-        keep32(p, r1, rbase, lane, col0 + c + 32, stage);
+        keep32(p, r1, rbase, lane, col0 + c + 32, stage, pol);
       }
     }
   }
