@@ -20,6 +20,8 @@ from .rz_oracle import (  # noqa: F401
     is_loss,
     d3,
     loss_fwd_bwd,
+    sc_loss,
+    sc_loss_fwd_bwd,
     logits_loss_fwd_bwd,
     segment_ids,
     is_stats,

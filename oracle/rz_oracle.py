@@ -12,7 +12,8 @@ Sources (web pages on REINFORCE Zero; cited by title and section):
     T_i = valid action tokens of response i, mu the recorded behaviour
     probability, gradient through the numerator pi only;
   - section "The full IS correction", items 01-04: w = p/q, E_q[w s] = 0,
-    g_IS = E_q[w A s] = Cov_p(A, s).
+    g_IS = E_q[w A s] = Cov_p(A, s); item 03 "Score centering":
+    g_SC = Cov_q(A, s) (the comparison estimator without IS).
 * [vLLM-zh]  "Zero Mismatch, Simple Async RL: REINFORCE Zero, DeepSeek-V4.1
   and Kimi K3.1" (Chinese rendering, todayforai.com):
   - section 3: the D3 diagnostic, the per-update mean over all tokens of
@@ -184,6 +185,77 @@ def loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, mask=None):
         dW += dz.T @ Hd[s:e]
     return {"loss": r["loss"], "d3": r["d3"], "logpi": logpi, "lse": lse,
             "c": c, "dH": dH, "dW": dW}
+
+
+def sc_loss(logpi, cu_seqlens, adv, mask=None):
+    """Score Centering (SC), the comparison estimator without importance
+    weights [RZ-page "The full IS correction", items 02-03]: the update
+    E_q[A s] taken on the sampler's tokens carries the drift E_q[A] E_q[s];
+    SC centres the sampler score and keeps g_SC = Cov_q(A, s).
+
+    Per-token form (a reading: the pages give only the expectation): each
+    sampled token's score s_t = grad log pi_t is centred by the batch
+    estimate of its mean, with the token weights of the IS loss,
+        g_SC = (1/B) sum_i (A_i/T_i) sum_t (s_t - sbar),
+        sbar = (1/B+) sum_{j: T_j > 0} (1/T_j) sum_t s_t,
+    B+ = number of responses with T_j > 0.  This equals
+    (1/B) sum_i ((A_i - Abar)/T_i) sum_t s_t with Abar the mean of A_i over
+    those B+ responses, so adding a constant to every advantage changes
+    nothing (the centred scores sum to zero).  Its surrogate loss
+    (gradient -g_SC) is
+        L_SC = -(1/B) sum_i ((A_i - Abar)/T_i) sum_{t in i} log pi_t,
+    c_t = -dL_SC/dlog pi_t = (A_i - Abar)/(B T_i).  T_i, B and the mask as in
+    is_loss; a response with T_i = 0 adds nothing.
+
+    Returns dict(loss, abar, c [T]) in fp64.
+    """
+    lp = _f64(logpi)
+    A = _f64(adv)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    B = A.shape[0]
+    T = lp.shape[0]
+    valid = np.ones(T, dtype=bool) if mask is None else (np.asarray(mask) != 0)
+    counts = np.array([int(valid[cu[i]:cu[i + 1]].sum()) for i in range(B)], dtype=np.int64)
+    nonempty = counts > 0
+    abar = A[nonempty].mean() if nonempty.any() else 0.0
+    c = np.zeros(T, dtype=np.float64)
+    total = 0.0
+    for i in range(B):
+        if counts[i] == 0:
+            continue
+        s, e = int(cu[i]), int(cu[i + 1])
+        v = valid[s:e]
+        total += (A[i] - abar) * lp[s:e][v].sum() / counts[i]
+        c[s:e] = np.where(v, (A[i] - abar) / (B * counts[i]), 0.0)
+    loss = -total / B if B > 0 else 0.0
+    return {"loss": loss, "abar": abar, "c": c}
+
+
+def sc_loss_fwd_bwd(H, W, tokens, cu_seqlens, adv, mask=None):
+    """Learner step of the Score Centering estimator (sc_loss): log pi, L_SC
+    and dH, dW with dz_tv = c_t (softmax_v(z_t) - [v = a_t]), as in
+    loss_fwd_bwd but with c_t from sc_loss (no log mu, no weight).
+    Returns dict(loss, abar, logpi, lse, c, dH, dW) in fp64.
+    """
+    Hd = _f64(H)
+    Wd = _f64(W)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    T = tokens.shape[0]
+    logpi, lse = token_logprob(Hd, Wd, tokens)
+    r = sc_loss(logpi, cu_seqlens, adv, mask)
+    c = r["c"]
+    dH = np.zeros_like(Hd)
+    dW = np.zeros_like(Wd)
+    for s in range(0, T, _ROW_BLOCK):
+        e = min(T, s + _ROW_BLOCK)
+        z = Hd[s:e] @ Wd.T
+        p = np.exp(z - lse[s:e, None])
+        p[np.arange(e - s), tokens[s:e]] -= 1.0
+        dz = c[s:e, None] * p
+        dH[s:e] = dz @ Wd
+        dW += dz.T @ Hd[s:e]
+    return {"loss": r["loss"], "abar": r["abar"], "logpi": logpi, "lse": lse, "c": c,
+            "dH": dH, "dW": dW}
 
 
 def logits_loss_fwd_bwd(logits, tokens, logmu, cu_seqlens, adv, rows=None, mask=None):

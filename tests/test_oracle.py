@@ -465,3 +465,106 @@ def test_masked_tokens_equal_removed_tokens():
     np.testing.assert_allclose(rm["dH"][keep], rk["dH"], atol=1e-14)
     assert np.all(rm["dH"][~keep] == 0.0)
     assert np.all(rm["c"][~keep] == 0.0)
+
+
+# ---------------------------------------------------------------- score centering
+
+def _scores(H, W, tok):
+    """Per-token score s_t = grad_(H, W) log pi_t by autograd: list of
+    (dH_t, dW_t) arrays."""
+    out = []
+    for t in range(len(tok)):
+        Ht = torch.tensor(H, requires_grad=True)
+        Wt = torch.tensor(W, requires_grad=True)
+        lp = torch.log_softmax(Ht @ Wt.T, 1)[t, int(tok[t])]
+        lp.backward()
+        out.append((Ht.grad.numpy().copy(), Wt.grad.numpy().copy()))
+    return out
+
+
+def test_sc_gradient_is_the_literal_centred_score_update():
+    """-(dH, dW) of L_SC equals (1/B) sum_i (A_i/T_i) sum_t (s_t - sbar),
+    sbar the mean per-token-averaged score over responses with tokens,
+    assembled from autograd scores (with a masked token and an empty
+    response in the batch)."""
+    H, W, tok, _, cu, A = _tiny_problem(40, T_lo=1, T_hi=5, B=5, d=4, V=7)
+    T = len(tok)
+    mask = np.ones(T, dtype=np.uint8)
+    mask[cu[1]:cu[2]] = 0          # response 1 has no valid token
+    mask[cu[3]] = 0                # one masked token in response 3
+    r = oracle.sc_loss_fwd_bwd(H, W, tok, cu, A, mask=mask)
+    sc = _scores(H, W, tok)
+    B = len(A)
+    resp_mean = []
+    for i in range(B):
+        ts = [t for t in range(cu[i], cu[i + 1]) if mask[t]]
+        if ts:
+            resp_mean.append((i, sum(sc[t][0] for t in ts) / len(ts),
+                              sum(sc[t][1] for t in ts) / len(ts)))
+    sbar_H = sum(m[1] for m in resp_mean) / len(resp_mean)
+    sbar_W = sum(m[2] for m in resp_mean) / len(resp_mean)
+    gH = sum(A[i] * (mH - sbar_H) for i, mH, _ in resp_mean) / B
+    gW = sum(A[i] * (mW - sbar_W) for i, _, mW in resp_mean) / B
+    np.testing.assert_allclose(-r["dH"], gH, atol=1e-13)
+    np.testing.assert_allclose(-r["dW"], gW, atol=1e-13)
+
+
+def test_sc_gradient_matches_central_differences():
+    H, W, tok, _, cu, A = _tiny_problem(41)
+    r = oracle.sc_loss_fwd_bwd(H, W, tok, cu, A)
+    eps = 1e-6
+    gW = np.zeros_like(W)
+    for idx in np.ndindex(W.shape):
+        Wp, Wm = W.copy(), W.copy()
+        Wp[idx] += eps
+        Wm[idx] -= eps
+        gW[idx] = (oracle.sc_loss_fwd_bwd(H, Wp, tok, cu, A)["loss"] -
+                   oracle.sc_loss_fwd_bwd(H, Wm, tok, cu, A)["loss"]) / (2 * eps)
+    assert np.linalg.norm(r["dW"] - gW) <= 1e-6 * np.linalg.norm(gW)
+
+
+def test_sc_invariant_to_advantage_shift_and_reduces_to_reinforce():
+    H, W, tok, _, cu, A = _tiny_problem(42, T_lo=0, T_hi=6, B=6, d=5, V=8)
+    r = oracle.sc_loss_fwd_bwd(H, W, tok, cu, A)
+    r2 = oracle.sc_loss_fwd_bwd(H, W, tok, cu, A + 3.25)
+    np.testing.assert_allclose(r2["dH"], r["dH"], atol=1e-13)
+    np.testing.assert_allclose(r2["dW"], r["dW"], atol=1e-13)
+    # advantages already centred over the responses with tokens: SC is the
+    # IS update at w = 1 (log mu := log pi), i.e. plain REINFORCE
+    counts = np.diff(cu)
+    Ac = A - A[counts > 0].mean()
+    rs = oracle.sc_loss_fwd_bwd(H, W, tok, cu, Ac)
+    lp, _ = oracle.token_logprob(H, W, tok)
+    ri = oracle.loss_fwd_bwd(H, W, tok, lp, cu, Ac)
+    assert abs(rs["abar"]) < 1e-15
+    np.testing.assert_allclose(rs["dH"], ri["dH"], atol=1e-13)
+    np.testing.assert_allclose(rs["dW"], ri["dW"], atol=1e-13)
+    np.testing.assert_allclose(rs["dW"], r["dW"], atol=1e-13)
+
+
+def test_sc_expectation_is_sampler_covariance_by_enumeration():
+    """Score centering keeps Cov_q(A, s) [item 03]: over every pair of
+    one-token responses drawn i.i.d. from q at the same state (B = 2), the
+    exact expectation of the SC update is (1 - 1/B) Cov_q(A, s), the usual
+    finite-batch factor of a batch-mean baseline; the uncentred update
+    E_q[A s] differs from it by the drift E_q[A] E_q[s] (item 02)."""
+    rng = _rng(43)
+    d, V = 3, 5
+    h = rng.standard_normal((1, d))
+    W = rng.standard_normal((V, d))
+    Wq = W + rng.standard_normal((V, d)) * 0.6
+    q = np.exp(np.array([oracle.token_logprob(h, Wq, np.array([a]))[0][0] for a in range(V)]))
+    Aof = rng.standard_normal(V) + 0.8     # E_q[A] != 0: there is a drift to remove
+    s = [_scores(h, W, np.array([a]))[0][1] for a in range(V)]   # dlog pi(a)/dW
+    cov = sum(q[a] * Aof[a] * s[a] for a in range(V)) - \
+        sum(q * Aof) * sum(q[a] * s[a] for a in range(V))
+    exp_g = np.zeros_like(W)
+    H2 = np.vstack([h, h])
+    for a1 in range(V):
+        for a2 in range(V):
+            r = oracle.sc_loss_fwd_bwd(H2, W, np.array([a1, a2]), np.array([0, 1, 2]),
+                                       np.array([Aof[a1], Aof[a2]]))
+            exp_g += q[a1] * q[a2] * (-r["dW"])
+    np.testing.assert_allclose(exp_g, 0.5 * cov, atol=1e-13)
+    drift = sum(q * Aof) * sum(q[a] * s[a] for a in range(V))
+    assert np.linalg.norm(drift) > 1e-2
