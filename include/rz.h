@@ -79,6 +79,7 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
 #define RZ_OP_LOGITS_LOSS     2
 #define RZ_OP_IS_LOSS         3
 #define RZ_OP_SAMPLE          4
+#define RZ_OP_SC_LOSS_FWD_BWD 5
 
 /*
  * Bytes of scratch the operation needs for these sizes (0 if none).  Pure
@@ -218,6 +219,33 @@ RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* to
                     rz_bf16* dH, float* dW,
                     void* ws, size_t ws_bytes, int32_t* err_flag,
                     rz_stream_t stream);
+
+/*
+ * Comparison estimator: Score Centering (SC), the learner step WITHOUT
+ * importance weights ["REINFORCE Zero" project page, "The full IS
+ * correction", items 02-03: the update on sampler tokens carries the drift
+ * E_q[A] E_q[s]; centring the sampler score keeps g_SC = Cov_q(A, s)].
+ * Per-token reading (the page gives only the expectation): each sampled
+ * token's score is centred by the batch mean of the per-response averaged
+ * scores, with the token weights of the IS loss, i.e.
+ *   L_SC = -(1/B) sum_i ((A_i - Abar)/T_i) sum_{t in i} log pi_t,
+ *   Abar = mean of A_i over the responses with at least one valid token,
+ *   dz_tv = (A_i - Abar)/(B T_i) (softmax_v(z_t) - [v = a_t]).
+ * A constant added to every advantage changes nothing; for advantages that
+ * already sum to zero it is the IS update at w = 1 (plain REINFORCE).
+ * Arguments, layouts, ownership, errors and determinism as rz_loss_fwd_bwd,
+ * without log mu and D3.  log pi (logprob_out, nullable) is bitwise the
+ * rollout's.  Workspace: rz_workspace_size(RZ_OP_SC_LOSS_FWD_BWD, T, d, V, B)
+ * (the same size as RZ_OP_LOSS_FWD_BWD).
+ */
+RZ_API int rz_sc_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                       const int64_t* cu_seqlens, const float* adv,
+                       const uint8_t* action_mask,
+                       int32_t B, int64_t T, int32_t d, int32_t V,
+                       float* loss_out, float* logprob_out,
+                       rz_bf16* dH, float* dW,
+                       void* ws, size_t ws_bytes, int32_t* err_flag,
+                       rz_stream_t stream);
 
 /*
  * Given-logits variant: the same loss on precomputed logits, with the

@@ -33,6 +33,7 @@ RZ_OP_LOSS_FWD_BWD = 1
 RZ_OP_LOGITS_LOSS = 2
 RZ_OP_IS_LOSS = 3
 RZ_OP_SAMPLE = 4
+RZ_OP_SC_LOSS_FWD_BWD = 5
 
 _lib = None
 
@@ -50,6 +51,8 @@ _SIGNATURES = {
     "rz_d3": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
     "rz_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
                                        _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_sc_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
+                                          _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_logits_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32,
                                               _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_lmhead_logits": (ctypes.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
@@ -287,6 +290,54 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
                              _ptr(err_flag), _stream(stream))
     _check("rz_loss_fwd_bwd", st)
     return {"loss": loss_out, "d3": d3_out, "logprob": logprob_out, "dH": dH, "dW": dW}
+
+
+def rz_sc_loss_fwd_bwd(H, W, tokens, cu_seqlens, adv, logprob_out=None, dH=None, dW=None,
+                       loss_out=None, ws=None, err_flag=None, stream=None, want_logprob=True,
+                       action_mask=None):
+    """Score Centering comparison estimator: the learner step without
+    importance weights, advantages centred over the batch (see include/rz.h).
+    Returns dict(loss, logprob, dH, dW) of device tensors."""
+    torch = _torch()
+    lib = load()
+    _need(H, torch.bfloat16, "H")
+    _need(W, torch.bfloat16, "W")
+    _need(tokens, torch.int32, "tokens")
+    _need(cu_seqlens, torch.int64, "cu_seqlens")
+    _need(adv, torch.float32, "adv")
+    T, d = H.shape
+    V = W.shape[0]
+    B = cu_seqlens.shape[0] - 1
+    _shape(W, (V, d), "W")
+    _shape(tokens, (T,), "tokens")
+    _shape(adv, (B,), "adv")
+    _shape(action_mask, (T,), "action_mask")
+    for t, n, dt, sh in ((logprob_out, "logprob_out", torch.float32, (T,)),
+                         (dH, "dH", torch.bfloat16, (T, d)),
+                         (dW, "dW", torch.float32, (V, d))):
+        if t is not None:
+            _need(t, dt, n)
+            _shape(t, sh, n)
+    _same_device(H, W, tokens, cu_seqlens, adv, action_mask, logprob_out, dH, dW, ws, err_flag)
+    dev = H.device
+    if want_logprob and logprob_out is None:
+        logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
+    if dH is None:
+        dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    if loss_out is None:
+        loss_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = alloc_workspace(RZ_OP_SC_LOSS_FWD_BWD, T, d, V, B, dev)
+    if action_mask is not None:
+        _need(action_mask, torch.uint8, "action_mask")
+    st = lib.rz_sc_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(cu_seqlens), _ptr(adv),
+                                _ptr(action_mask), B, T, d, V, _ptr(loss_out),
+                                _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                                _ptr(err_flag), _stream(stream))
+    _check("rz_sc_loss_fwd_bwd", st)
+    return {"loss": loss_out, "logprob": logprob_out, "dH": dH, "dW": dW}
 
 
 def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob_out=None,

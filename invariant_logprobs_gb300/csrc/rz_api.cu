@@ -159,6 +159,88 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
   return RZ_OK;
 }
 
+// The learner step shared by the IS loss and, with sc set, the Score
+// Centering loss (no weight, advantages centred, no log mu, no D3).
+int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                 const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                 const uint8_t* action_mask, int32_t B, int64_t T, int32_t d, int32_t V,
+                 float* loss_out, float* d3_out, float* logprob_out, rz_bf16* dH, float* dW,
+                 void* ws, size_t ws_bytes, int32_t* err_flag, cudaStream_t st) {
+  if (!sizes_ok(T, d, V) || B < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
+  if (!W || !dW || !loss_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
+  if (T > 0 && (!H || !tokens || !dH)) return RZ_ERR_INVALID_ARG;
+  if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
+  if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
+  if (!a16(W) || !a16(dW) || (T > 0 && (!a16(H) || !a16(dH)))) return RZ_ERR_UNSUPPORTED;
+  const LearnLayout L = learn_layout(T, V, B);
+  if (!ws || ws_bytes < L.total || !a256(ws)) return RZ_ERR_WORKSPACE;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  float2* fac = reinterpret_cast<float2*>(w8 + L.fac);
+
+  if (T == 0) {
+    RZ_TRY(cudaMemsetAsync(dW, 0, size_t(V) * size_t(d) * sizeof(float), st));
+    if (sc) {
+      RZ_TRY(launch_resp_factors(cu_seqlens, adv, nullptr, B, 0, fac, st));
+      RZ_TRY(launch_sc_loss(nullptr, cu_seqlens, nullptr, fac, B, 0, loss_out, w8 + L.resp,
+                            err_flag, st));
+    } else {
+      RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, nullptr, B, 0, loss_out, d3_out,
+                            nullptr, w8 + L.resp, err_flag, st));
+    }
+    return RZ_OK;
+  }
+
+  float* logpi = logprob_out ? logprob_out : reinterpret_cast<float*>(w8 + L.logpi);
+  float* lse_c = reinterpret_cast<float*>(w8 + L.lse_ws);
+  float* coef_c = reinterpret_cast<float*>(w8 + L.coef);
+  float2* part = reinterpret_cast<float2*>(w8 + L.fwd.part);
+  float* zg = reinterpret_cast<float*>(w8 + L.fwd.zg);
+  float* z = reinterpret_cast<float*>(w8 + L.z);
+  uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
+  const int64_t ldz = dz_ld(V);
+  CUtensorMap tmH, tmW, tmWmn, tmHmn;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmWmn, W, d, V, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmHmn, H, d, T, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
+
+  // (A_i, 1/(B T_i)) per response: all the coefficient needs besides w_t
+  // (Score Centering: A_i - Abar).
+  RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+  if (sc) RZ_TRY(launch_sc_centre(fac, B, st));
+
+  // Chunk by chunk in row order: logits once (kept in fp32) with the
+  // rollout's log-sum-exp fold, merge + c_t, dz, then dH and dW.
+  for (int64_t r0 = 0; r0 < T; r0 += L.rows) {
+    const int64_t rows = (T - r0) < L.rows ? (T - r0) : L.rows;
+    CUtensorMap tmDz, tmDzMn;
+    if (!make_tmap_bf16(&tmDz, dz, V, rows, uint64_t(ldz) * 2, kBK, kBM))
+      return RZ_ERR_UNSUPPORTED;
+    if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
+      return RZ_ERR_UNSUPPORTED;
+    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, z, ldz, err_flag,
+                           st));
+    RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
+                                 sc ? nullptr : logmu + r0, cu_seqlens, fac,
+                                 action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
+                                 st));
+    RZ_TRY(launch_dz_rows(z, ldz, dz, rows, V, tokens + r0, lse_c, coef_c, st));
+    RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
+    RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
+  }
+
+  // Loss (and D3) over all rows (fixed-order reductions).
+  if (sc) {
+    RZ_TRY(launch_sc_loss(logpi, cu_seqlens, action_mask, fac, B, T, loss_out, w8 + L.resp,
+                          err_flag, st));
+  } else {
+    RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
+                          nullptr, w8 + L.resp, err_flag, st));
+  }
+  return RZ_OK;
+}
+
 }  // namespace
 }  // namespace rz
 
@@ -183,7 +265,8 @@ size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
   if (T < 0) T = 0;
   switch (op) {
     case RZ_OP_TOKEN_LOGPROB: return fwd_layout(T, V > 0 ? V : 1).total;
-    case RZ_OP_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
+    case RZ_OP_LOSS_FWD_BWD:
+    case RZ_OP_SC_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
     case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B) + resp_scale_ws_bytes(B);
     case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
     case RZ_OP_SAMPLE: return sample_layout(T, V > 0 ? V : 1).total;
@@ -284,67 +367,20 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
                     int32_t B, int64_t T, int32_t d, int32_t V, float* loss_out, float* d3_out,
                     float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
                     int32_t* err_flag, rz_stream_t stream) {
-  if (!sizes_ok(T, d, V) || B < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
-  if (!W || !dW || !loss_out || !d3_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
-  if (T > 0 && (!H || !tokens || !logmu || !dH)) return RZ_ERR_INVALID_ARG;
-  if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
-  if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
-  if (!a16(W) || !a16(dW) || (T > 0 && (!a16(H) || !a16(dH)))) return RZ_ERR_UNSUPPORTED;
-  const LearnLayout L = learn_layout(T, V, B);
-  if (!ws || ws_bytes < L.total || !a256(ws)) return RZ_ERR_WORKSPACE;
-  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (!d3_out || (T > 0 && !logmu)) return RZ_ERR_INVALID_ARG;
+  return learner_step(false, H, W, tokens, logmu, cu_seqlens, adv, action_mask, B, T, d, V,
+                      loss_out, d3_out, logprob_out, dH, dW, ws, ws_bytes, err_flag,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
 
-  if (T == 0) {
-    RZ_TRY(cudaMemsetAsync(dW, 0, size_t(V) * size_t(d) * sizeof(float), st));
-    RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, nullptr, B, 0, loss_out, d3_out,
-                          nullptr, w8 + L.resp, err_flag, st));
-    return RZ_OK;
-  }
-
-  float* logpi = logprob_out ? logprob_out : reinterpret_cast<float*>(w8 + L.logpi);
-  float* lse_c = reinterpret_cast<float*>(w8 + L.lse_ws);
-  float* coef_c = reinterpret_cast<float*>(w8 + L.coef);
-  float2* fac = reinterpret_cast<float2*>(w8 + L.fac);
-  float2* part = reinterpret_cast<float2*>(w8 + L.fwd.part);
-  float* zg = reinterpret_cast<float*>(w8 + L.fwd.zg);
-  float* z = reinterpret_cast<float*>(w8 + L.z);
-  uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
-  const int64_t ldz = dz_ld(V);
-  CUtensorMap tmH, tmW, tmWmn, tmHmn;
-  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmWmn, W, d, V, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmHmn, H, d, T, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
-
-  // (A_i, 1/(B T_i)) per response: all the coefficient needs besides w_t.
-  RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
-
-  // Chunk by chunk in row order: logits once (kept in fp32) with the
-  // rollout's log-sum-exp fold, merge + c_t, dz, then dH and dW.
-  for (int64_t r0 = 0; r0 < T; r0 += L.rows) {
-    const int64_t rows = (T - r0) < L.rows ? (T - r0) : L.rows;
-    CUtensorMap tmDz, tmDzMn;
-    if (!make_tmap_bf16(&tmDz, dz, V, rows, uint64_t(ldz) * 2, kBK, kBM))
-      return RZ_ERR_UNSUPPORTED;
-    if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
-      return RZ_ERR_UNSUPPORTED;
-    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, z, ldz, err_flag,
-                           st));
-    RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
-                                 logmu + r0, cu_seqlens, fac,
-                                 action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
-                                 st));
-    RZ_TRY(launch_dz_rows(z, ldz, dz, rows, V, tokens + r0, lse_c, coef_c, st));
-    RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
-    RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
-  }
-
-  // Loss and D3 over all rows (fixed-order reductions).
-  RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
-                        nullptr, w8 + L.resp, err_flag, st));
-  return RZ_OK;
+int rz_sc_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                       const int64_t* cu_seqlens, const float* adv, const uint8_t* action_mask,
+                       int32_t B, int64_t T, int32_t d, int32_t V, float* loss_out,
+                       float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
+                       int32_t* err_flag, rz_stream_t stream) {
+  return learner_step(true, H, W, tokens, nullptr, cu_seqlens, adv, action_mask, B, T, d, V,
+                      loss_out, nullptr, logprob_out, dH, dW, ws, ws_bytes, err_flag,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const float* logmu,

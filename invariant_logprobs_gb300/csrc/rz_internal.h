@@ -81,6 +81,12 @@ cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t
 size_t resp_factors_ws_bytes(int32_t B);
 cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
                                 int64_t T, float2* fac, cudaStream_t st);
+// Score Centering: fac[i].x -= mean of A over responses with fac[i].y > 0;
+// the loss from log pi (ws: is_loss_ws_bytes(B)).
+cudaError_t launch_sc_centre(float2* fac, int B, cudaStream_t st);
+cudaError_t launch_sc_loss(const float* logpi, const int64_t* cu, const uint8_t* mask,
+                           const float2* fac, int B, int64_t T, float* loss, void* ws, int* err,
+                           cudaStream_t st);
 cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
                       cudaStream_t st);
 cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, float* out,

@@ -496,9 +496,11 @@ __global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __res
 
 // Learner, one chunk of rows (row0 = the chunk's first global row; every
 // other pointer is chunk-local except cu and fac): the merge above, then the
-// per-token coefficient c_t = A_i w_t / (B T_i), w_t = exp(log pi - log mu),
-// 0 for a masked token.  fac[i] = (A_i, 1/(B T_i)).  Response of a row: the
-// last i with cu[i] <= row (empty responses own no row).
+// per-token coefficient c_t = A_i w_t / (B T_i), w_t = exp(log pi - log mu)
+// (w_t = 1 when logmu is null: the Score Centering estimator, whose fac
+// holds the centred advantages), 0 for a masked token.
+// fac[i] = (A_i, 1/(B T_i)).  Response of a row: the last i with
+// cu[i] <= row (empty responses own no row).
 __global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long row0,
                                       const int32_t* __restrict__ tokens,
                                       const float2* __restrict__ part,
@@ -524,7 +526,8 @@ __global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long ro
   }
   const bool act = !mask || mask[t] != 0;
   const float2 f = fac[lo];
-  coef[t] = act ? f.x * is_weight(lp, logmu[t]) * f.y : 0.f;
+  const float w = logmu ? is_weight(lp, logmu[t]) : 1.f;
+  coef[t] = act ? f.x * w * f.y : 0.f;
 }
 
 // ============================================================== dz pass

@@ -129,6 +129,63 @@ __global__ void resp_factors_kernel(const int64_t* __restrict__ cu, const float*
                          Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f);
 }
 
+// Score Centering: Abar = mean of A_i over the responses with valid tokens
+// (fac[i].y > 0), then fac[i].x = A_i - Abar; fixed-order fp64 sum.
+__global__ void __launch_bounds__(kFinalThreads) sc_centre_kernel(float2* __restrict__ fac, int B) {
+  __shared__ double red[kFinalThreads / 32];
+  __shared__ double abar;
+  double sum = 0.0, cnt = 0.0;
+  for (int i = threadIdx.x; i < B; i += kFinalThreads) {
+    if (fac[i].y > 0.f) {
+      sum += static_cast<double>(fac[i].x);
+      cnt += 1.0;
+    }
+  }
+  const double tot = block_sum<double, kFinalThreads>(sum, red);
+  const double n = block_sum<double, kFinalThreads>(cnt, red);
+  if (threadIdx.x == 0) abar = n > 0.0 ? tot / n : 0.0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < B; i += kFinalThreads)
+    fac[i].x = static_cast<float>(static_cast<double>(fac[i].x) - abar);
+}
+
+// Score Centering loss, per response: (sum of log pi over valid tokens, T_i)
+// in fp64.  Same cu_seqlens checks as is_loss_resp_kernel.
+__global__ void __launch_bounds__(kRespThreads)
+    sc_loss_resp_kernel(const float* __restrict__ logpi, const int64_t* __restrict__ cu,
+                        const uint8_t* __restrict__ mask, int B, long long T,
+                        double2* __restrict__ part, int* err) {
+  __shared__ double red[kRespThreads / 32];
+  __shared__ int redi[kRespThreads / 32];
+  const int i = blockIdx.x;
+  long long s = cu[i];
+  long long e = cu[i + 1];
+  const bool bad = s < 0 || e < s || e > T || (i == 0 && s != 0) || (i == B - 1 && e != T);
+  if (bad) {
+    if (threadIdx.x == 0 && err) atomicOr(err, 2);
+    if (s < 0 || s > T) s = 0;
+    if (e < s || e > T) e = s;
+  }
+  const long long Ti = valid_count(mask, s, e, redi);
+  double acc = 0.0;
+  for (long long t = s + threadIdx.x; t < e; t += kRespThreads)
+    if (!mask || mask[t] != 0) acc += static_cast<double>(logpi[t]);
+  const double tot = block_sum<double, kRespThreads>(acc, red);
+  if (threadIdx.x == 0) part[i] = make_double2(tot, static_cast<double>(Ti));
+}
+
+// L_SC = -(1/B) sum_i (A_i - Abar) (1/T_i) sum_t log pi_t, fixed order.
+__global__ void __launch_bounds__(kFinalThreads)
+    sc_loss_final_kernel(const double2* __restrict__ part, const float2* __restrict__ fac, int B,
+                         float* loss) {
+  __shared__ double red[kFinalThreads / 32];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < B; i += kFinalThreads)
+    if (part[i].y > 0.0) acc += static_cast<double>(fac[i].x) * (part[i].x / part[i].y);
+  const double tot = block_sum<double, kFinalThreads>(acc, red);
+  if (threadIdx.x == 0) *loss = B > 0 ? static_cast<float>(-tot / B) : 0.f;
+}
+
 __global__ void __launch_bounds__(kFinalThreads)
     is_loss_final_kernel(const RespPart* __restrict__ part, int B, float* loss, float* d3) {
   __shared__ double red[kFinalThreads / 32];
@@ -258,6 +315,25 @@ cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8
                                 int64_t T, float2* fac, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
   resp_factors_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, B, T, fac);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sc_centre(float2* fac, int B, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  sc_centre_kernel<<<1, kFinalThreads, 0, st>>>(fac, B);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sc_loss(const float* logpi, const int64_t* cu, const uint8_t* mask,
+                           const float2* fac, int B, int64_t T, float* loss, void* ws, int* err,
+                           cudaStream_t st) {
+  double2* part = static_cast<double2*>(ws);
+  if (B > 0) {
+    sc_loss_resp_kernel<<<B, kRespThreads, 0, st>>>(logpi, cu, mask, B, T, part, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  sc_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, fac, B, loss);
   return cudaGetLastError();
 }
 
