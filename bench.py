@@ -568,9 +568,10 @@ def run_reference(args):
 
 
 def run_profile(args):
-    """Small fixed cases for ncu captures (not a benchmark): one rollout
-    logprob call, then `--steps` learner steps (or given-logits steps) on
-    `--rows` tokens of the workload's d and V."""
+    """Small fixed cases for ncu captures (not a benchmark), on `--rows`
+    tokens of the workload's d and V: one rollout logprob call then `--steps`
+    learner steps (learner), `--steps` given-logits steps (logits), fused
+    sampling calls (sample) or rollout logprob calls (rollout)."""
     import dataclasses
     import torch
     import invariant_logprobs_gb300 as rz
@@ -597,6 +598,12 @@ def run_profile(args):
         torch.cuda.synchronize()
         print("profile sample rows=%d ok" % b["T"])
         return 0
+    if args.profile == "rollout":
+        for _ in range(args.steps):
+            rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
+        torch.cuda.synchronize()
+        print("profile rollout rows=%d ok" % b["T"])
+        return 0
     logmu, _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
     adv = rz.rz_group_advantage(b["rewards"], b["G"])
     for _ in range(args.steps):
@@ -616,7 +623,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["learner", "logits", "sample"], default=None,
+    ap.add_argument("--profile", choices=["learner", "logits", "sample", "rollout"], default=None,
                     help="small fixed case for ncu captures (no timing output)")
     ap.add_argument("--rows", type=int, default=16384)
     args = ap.parse_args()
