@@ -36,9 +36,9 @@ bool device_ok() {
 }
 
 int64_t chunk_rows(int32_t V) {
-  // one chunk keeps rows x round_up(V, 8) logits in fp32 and dz in bf16,
-  // at most 40 GiB together.
-  const int64_t per_row = dz_ld(V) * 6;
+  // one chunk keeps rows x round_up(V, 8) fp16 terms (then bf16 dz) and a
+  // running max per 32 columns, at most 40 GiB together.
+  const int64_t per_row = dz_ld(V) * 2 + emax_ld(V) * 4;
   int64_t rows = kChunkRowsMax;
   const int64_t cap = (int64_t(40) << 30) / (per_row > 0 ? per_row : 1);
   if (rows > cap) rows = cap / kBM * kBM;
@@ -107,7 +107,7 @@ SampleLayout sample_layout(int64_t T, int32_t V) {
 struct LearnLayout {
   int64_t rows;  // rows per chunk
   FwdLayout fwd;  // split states of one chunk
-  size_t logpi, lse_ws, coef, resp, fac, z, dz, total;
+  size_t logpi, lse_ws, coef, resp, fac, emax, ez, total;
 };
 LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
   LearnLayout L{};
@@ -122,9 +122,9 @@ LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
   L.coef = L.lse_ws + al256(r * 4);
   L.resp = L.coef + al256(r * 4);
   L.fac = L.resp + is_loss_ws_bytes(B);
-  L.z = L.fac + resp_factors_ws_bytes(B);
-  L.dz = L.z + al256(r * static_cast<size_t>(dz_ld(V)) * 4);
-  L.total = L.dz + al256(r * static_cast<size_t>(dz_ld(V)) * 2);
+  L.emax = L.fac + resp_factors_ws_bytes(B);
+  L.ez = L.emax + al256(r * static_cast<size_t>(emax_ld(V)) * 4);
+  L.total = L.ez + al256(r * static_cast<size_t>(dz_ld(V)) * 2);
   return L;
 }
 
@@ -196,9 +196,10 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   float* coef_c = reinterpret_cast<float*>(w8 + L.coef);
   float2* part = reinterpret_cast<float2*>(w8 + L.fwd.part);
   float* zg = reinterpret_cast<float*>(w8 + L.fwd.zg);
-  float* z = reinterpret_cast<float*>(w8 + L.z);
-  uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
+  float* emax = reinterpret_cast<float*>(w8 + L.emax);
+  uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.ez);  // kept terms, then dz in place
   const int64_t ldz = dz_ld(V);
+  const int64_t ldm = emax_ld(V);
   CUtensorMap tmH, tmW, tmWmn, tmHmn;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
@@ -210,8 +211,8 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
   if (sc) RZ_TRY(launch_sc_centre(fac, B, st));
 
-  // Chunk by chunk in row order: logits once (kept in fp32) with the
-  // rollout's log-sum-exp fold, merge + c_t, dz, then dH and dW.
+  // Chunk by chunk in row order: logits once, folded exactly as the rollout
+  // folds them, keeping the fold's terms; merge + c_t; dz in place; dH, dW.
   for (int64_t r0 = 0; r0 < T; r0 += L.rows) {
     const int64_t rows = (T - r0) < L.rows ? (T - r0) : L.rows;
     CUtensorMap tmDz, tmDzMn;
@@ -219,13 +220,14 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
       return RZ_ERR_UNSUPPORTED;
     if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
       return RZ_ERR_UNSUPPORTED;
-    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, z, ldz, err_flag,
-                           st));
+    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, dz, ldz, emax, ldm,
+                           err_flag, st));
     RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
                                  sc ? nullptr : logmu + r0, cu_seqlens, fac,
                                  action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
                                  st));
-    RZ_TRY(launch_dz_rows(z, ldz, dz, rows, V, tokens + r0, lse_c, coef_c, st));
+    RZ_TRY(launch_dz_rows(dz, ldz, emax, ldm, rows, V, tokens + r0, lse_c, coef_c, logpi + r0,
+                          st));
     RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
     RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
   }

@@ -28,11 +28,12 @@ inline int vocab_splits(int V) {
   return (nt + tps - 1) / tps;
 }
 
-// Rows per backward chunk: the chunk's fp32 logits and bf16 dz live in the
-// workspace (6 bytes per logit).
+// Rows per backward chunk: the chunk's kept fp16 terms (overwritten in place
+// by bf16 dz) and one fp32 running max per 32 columns live in the workspace.
 constexpr int64_t kChunkRowsMax = 38912;  // 256 * 152
 int64_t chunk_rows(int32_t V);
 inline int64_t dz_ld(int32_t V) { return (static_cast<int64_t>(V) + 7) / 8 * 8; }
+inline int64_t emax_ld(int32_t V) { return (static_cast<int64_t>(V) + 127) / 128 * 4; }
 
 int num_sms();
 bool device_ok();  // current device is sm_103 (or newer family member we compiled for)
@@ -52,15 +53,16 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
                           int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st);
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
-                            float* zgather, float* z, int64_t ldz, int* err, cudaStream_t st);
+                            float* zgather, uint16_t* e16, int64_t lde, float* emax, int64_t ldm,
+                            int* err, cudaStream_t st);
 cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32_t* tokens,
                                   const float2* part, const float* zgather, float* logprob,
                                   float* lse_ws, const float* logmu, const int64_t* cu,
                                   const float2* fac, const uint8_t* mask, int B, float* coef,
                                   int* err, cudaStream_t st);
-cudaError_t launch_dz_rows(const float* z, int64_t ldz, uint16_t* dz, int64_t rows, int V,
-                           const int32_t* tokens, const float* lse, const float* coef,
-                           cudaStream_t st);
+cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t ldm,
+                           int64_t rows, int V, const int32_t* tokens, const float* lse,
+                           const float* coef, const float* logpi, cudaStream_t st);
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                               int V, float* out, int* err, cudaStream_t st);
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,

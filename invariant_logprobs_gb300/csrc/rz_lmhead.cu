@@ -1,15 +1,16 @@
 // rz_lmhead.cu -- the LM-head contractions and their fused epilogues.
 //
-//   lse_partial  (rollout + learner pass 1) z = H W^T per 128x256 tile in
-//                TMEM; the epilogue folds each row's logits into a running
-//                (max, sum of exp) over the tiles of its vocab split, in
-//                ascending vocab order, and picks out z[t, a_t].
+//   lse_partial  (rollout) z = H W^T per 128x256 tile in TMEM; the epilogue
+//                folds each row's logits into a running (max, sum of exp)
+//                over the tiles of its vocab split, in ascending vocab
+//                order, and picks out z[t, a_t].
 //   lse_merge    fixed-order merge of the splits -> logsumexp, log pi.
 //   lse_keep     (learner, one token chunk) the lse_partial fold on the
-//                same tiles, bitwise, plus the fp32 logits written out.
+//                same tiles, bitwise, keeping its terms 2^((z - m) log2 e)
+//                as fp16 and the running max m per 32 columns.
 //   merge_coef   the fixed-order merge, then c_t = A_i w_t / (B T_i).
-//   dz_rows      HBM pass: dz = c_t (softmax - onehot) as bf16 from the kept
-//                logits (the chunk's logits are never recomputed).
+//   dz_rows      HBM pass: dz = c_t (softmax - onehot) as bf16, in place
+//                over the kept terms (the logits are never recomputed).
 //   dH, dW       dz W and dz^T H on the same tensor-core pipeline.
 //   logits_f32   plain z = H W^T (same tiles) for callers that want logits.
 //
@@ -17,6 +18,7 @@
 // logprob, "REINFORCE Zero" project page s.02 and the vLLM post s.4 item 1);
 // dz from differentiating the loss through the numerator pi only (project
 // page s.02, "A minimal REINFORCE objective").
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -103,13 +105,18 @@ struct EpiLsePartial {
 };
 
 // Learner pass 1 for one chunk of rows: exactly the EpiLsePartial fold (so
-// log pi is the rollout's, bit for bit) and, next to it, the fp32 logits of
-// the chunk, so that the backward pass reads them instead of recomputing.
+// log pi is the rollout's, bit for bit), keeping what the backward pass needs
+// to form the softmax without recomputing the logits: the fold's own terms
+// e_tv = 2^((z_tv - m) log2 e) in (0, 1] as fp16, and m, the running maximum
+// they were taken against, once per 32 columns.  p_tv = e_tv 2^((m - lse_t)
+// log2 e) then needs only the row's final log-sum-exp.
 struct EpiLseKeep {
   struct Params {
     EpiLsePartial::Params lse;  // chunk-local rows: T = rows of the chunk
-    float* z;                   // [rows, ldz] fp32
-    long long ldz;              // multiple of 4
+    uint16_t* e16;              // [rows, lde] fp16 terms (later overwritten by dz)
+    float* emax;                // [rows, ldm] m per 32-column slice
+    long long lde;              // multiple of 8
+    long long ldm;              // >= ceil(V / 32), even
   };
   using State = EpiLsePartial::State;
 
@@ -122,46 +129,44 @@ struct EpiLseKeep {
     EpiLsePartial::task_end(p.lse, st, m_blk, grp, row);
   }
 
-  // 32 columns of the warp's 32 rows through the warp's stage (row r at
-  // r*128, 16-byte piece j at j ^ (r & 7)), then 8 store instructions that
-  // each write four whole 128-byte row segments.  The logits are written
-  // evict-first: they are read back only after the whole chunk, and would
-  // otherwise push the H and W tiles the CTAs share out of L2.
-  static __device__ __forceinline__ void keep32(const Params& p, const uint32_t (&r)[32],
-                                                long long rbase, int lane, int cbase,
-                                                uint8_t* stage, uint64_t pol) {
-    uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
+  // EpiLsePartial::chunk with the terms kept, packed to 16 fp16 pairs.
+  static __device__ __forceinline__ void chunk(const Params& p, State& st, const uint32_t (&r)[32],
+                                               int cbase, uint32_t* w) {
+    float v[32];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      mine[j ^ (lane & 7)] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-    __syncwarp();
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    if (cbase + 32 > p.lse.V) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int rr = 4 * k + (lane >> 3);
-      const int j = lane & 7;
-      const uint4 v = reinterpret_cast<const uint4*>(stage + rr * 128)[j ^ (rr & 7)];
-      const long long gr = rbase + rr;
-      const int col = cbase + 4 * j;
-      if (gr < p.lse.T && col < p.lse.V) {
-        float* dst = p.z + gr * p.ldz + col;
-        if (col + 4 <= p.lse.V) {
-          st_l2hint(reinterpret_cast<uint4*>(dst), v, pol);
-        } else {
-          for (int e = 0; col + e < p.lse.V; ++e)
-            dst[e] = __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : v.z));
-        }
-      }
+      for (int j = 0; j < 32; ++j)
+        if (cbase + j >= p.lse.V) v[j] = -INFINITY;
     }
-    __syncwarp();
+    float e[32];
+    lse_fold32_keep(st.m, st.s, v, e);
+    const unsigned rel = static_cast<unsigned>(st.a - cbase);
+    if (rel < 32u) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (rel == static_cast<unsigned>(j)) st.za = v[j];
+      st.found = true;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = pack_f16x2(e[2 * j], e[2 * j + 1]);
   }
 
+  // A 64-column slab of the warp's 32 rows goes through the warp's stage
+  // (row r at r*128, 16-byte piece j at j ^ (r & 7)) so each global store
+  // instruction writes four whole 128-byte row segments; evict-first, since
+  // the terms are read back only after the whole chunk and would otherwise
+  // push the H and W tiles the CTAs share out of L2.
   static __device__ __forceinline__ void tile(const Params& p, State& st, int m_blk, int n_tile,
                                               uint32_t taddr, int row, uint8_t* stage) {
     const int col0 = n_tile * kBN;
     const int V = p.lse.V;
     const int lane = row & 31;
+    const long long grow = static_cast<long long>(m_blk) * kBM + row;
     const long long rbase = static_cast<long long>(m_blk) * kBM + (row & ~31);
     const uint64_t pol = l2_policy_first();
+    uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 64) {
       if (col0 + c >= V) break;  // warp-uniform
@@ -169,12 +174,46 @@ struct EpiLseKeep {
       tmem_ld32(taddr + c, r0);
       tmem_ld32(taddr + c + 32, r1);
       tmem_ld_wait();
-      EpiLsePartial::chunk(p.lse, st, r0, col0 + c);
-      keep32(p, r0, rbase, lane, col0 + c, stage, pol);
+      uint32_t w[32];
+      chunk(p, st, r0, col0 + c, w);
+      const float m0 = st.m;
+      float m1 = m0;
       if (col0 + c + 32 < V) {
-        EpiLsePartial::chunk(p.lse, st, r1, col0 + c + 32);
-        keep32(p, r1, rbase, lane, col0 + c + 32, stage, pol);
+        chunk(p, st, r1, col0 + c + 32, w + 16);
+        m1 = st.m;
       }
+      if (grow < p.lse.T) {
+        float* em = p.emax + grow * p.ldm + ((col0 + c) >> 5);
+        if (col0 + c + 32 < V) {
+          *reinterpret_cast<float2*>(em) = make_float2(m0, m1);
+        } else {
+          em[0] = m0;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mine[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rr = 4 * k + (lane >> 3);
+        const int j = lane & 7;
+        const uint4 v = reinterpret_cast<const uint4*>(stage + rr * 128)[j ^ (rr & 7)];
+        const long long gr = rbase + rr;
+        const int col = col0 + c + 8 * j;
+        if (gr < p.lse.T && col < V) {
+          uint16_t* dst = p.e16 + gr * p.lde + col;
+          if (col + 8 <= V) {
+            st_l2hint(reinterpret_cast<uint4*>(dst), v, pol);
+          } else {
+            for (int q = 0; col + q < V; ++q) {
+              const uint32_t word = q < 2 ? v.x : (q < 4 ? v.y : (q < 6 ? v.z : v.w));
+              dst[q] = static_cast<uint16_t>((word >> (16 * (q & 1))) & 0xffffu);
+            }
+          }
+        }
+      }
+      __syncwarp();
     }
   }
 };
@@ -531,63 +570,78 @@ __global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long ro
 }
 
 // ============================================================== dz pass
-// dz_tv = c_t (2^((z_tv - lse_t) log2 e) - [v = a_t]) in bf16, from the
-// kept fp32 logits of one chunk; one CTA per row, 8 columns per step (two
-// 16-byte loads, one 16-byte store), four steps in flight per thread.  Both
-// buffers have row stride ldz (a multiple of 8); columns >= V are not touched.
+// dz_tv = c_t (p_tv - [v = a_t]) in bf16, written in place over the chunk's
+// kept fp16 terms: p_tv = e_tv 2^((m - lse_t) log2 e) with m the running
+// maximum of the term's 32-column slice; at v = a_t the exact
+// c_t expm1(log pi_t) (no cancellation of p - 1 as p -> 1).  One CTA per row,
+// 8 columns per 16-byte step (never straddling a slice), four steps in
+// flight per thread.  Columns >= V are not touched.
 constexpr int kDzThreads = 256;
 
-__device__ __forceinline__ float dz_of(float z, float lse, float c) {
-  return __fmul_rn(c, ex2_approx(__fmul_rn(__fsub_rn(z, lse), kLog2e)));
-}
-
-__device__ __forceinline__ uint4 dz8(const float4& lo, const float4& hi, float lse, float c,
-                                     int rel) {
-  float g[8] = {dz_of(lo.x, lse, c), dz_of(lo.y, lse, c), dz_of(lo.z, lse, c),
-                dz_of(lo.w, lse, c), dz_of(hi.x, lse, c), dz_of(hi.y, lse, c),
-                dz_of(hi.z, lse, c), dz_of(hi.w, lse, c)};
+__device__ __forceinline__ uint4 dz8(const uint4& q, float scale, float c_onehot, int rel) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float g[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+    const float2 f = __half22float2(h);
+    g[2 * j] = __fmul_rn(scale, f.x);
+    g[2 * j + 1] = __fmul_rn(scale, f.y);
+  }
   if (static_cast<unsigned>(rel) < 8u) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (rel == j) g[j] = __fsub_rn(g[j], c);
+      if (rel == j) g[j] = c_onehot;
   }
   return make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
                     pack_bf16x2(g[6], g[7]));
 }
 
 __global__ void __launch_bounds__(kDzThreads)
-    dz_rows_kernel(const float* __restrict__ z, long long ldz, uint16_t* __restrict__ dz,
-                   int V, const int32_t* __restrict__ tokens, const float* __restrict__ lse,
-                   const float* __restrict__ coef) {
+    dz_rows_kernel(uint16_t* __restrict__ ez, long long lde, const float* __restrict__ emax,
+                   long long ldm, int V, const int32_t* __restrict__ tokens,
+                   const float* __restrict__ lse, const float* __restrict__ coef,
+                   const float* __restrict__ logpi) {
   const long long row = blockIdx.x;
-  const float4* zr = reinterpret_cast<const float4*>(z + row * ldz);
-  uint4* dr = reinterpret_cast<uint4*>(dz + row * ldz);
+  uint4* er = reinterpret_cast<uint4*>(ez + row * lde);
+  const float* mr = emax + row * ldm;
   const float l = lse[row];
   const float c = coef[row];
   const int a = tokens[row];
+  const float c_onehot = __fmul_rn(c, expm1f(logpi[row]));
   const int n8 = V >> 3;
   int i = threadIdx.x;
   for (; i + 3 * kDzThreads < n8; i += 4 * kDzThreads) {
-    float4 q[8];
+    uint4 q[4];
+    float sc[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      q[2 * u] = __ldcs(zr + 2 * (i + u * kDzThreads));
-      q[2 * u + 1] = __ldcs(zr + 2 * (i + u * kDzThreads) + 1);
+      const int k = i + u * kDzThreads;
+      q[u] = __ldcs(er + k);
+      sc[u] = __fmul_rn(c, ex2_approx(__fmul_rn(__fsub_rn(__ldg(mr + (k >> 2)), l), kLog2e)));
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int k = i + u * kDzThreads;
-      __stcs(dr + k, dz8(q[2 * u], q[2 * u + 1], l, c, a - 8 * k));
+      __stcs(er + k, dz8(q[u], sc[u], c_onehot, a - 8 * k));
     }
   }
-  for (; i < n8; i += kDzThreads)
-    __stcs(dr + i, dz8(__ldcs(zr + 2 * i), __ldcs(zr + 2 * i + 1), l, c, a - 8 * i));
+  for (; i < n8; i += kDzThreads) {
+    const float sc = __fmul_rn(c, ex2_approx(__fmul_rn(__fsub_rn(__ldg(mr + (i >> 2)), l), kLog2e)));
+    __stcs(er + i, dz8(__ldcs(er + i), sc, c_onehot, a - 8 * i));
+  }
   // ragged tail: V % 8 columns
   const int v = 8 * n8 + static_cast<int>(threadIdx.x);
   if (v < V) {
-    float g = dz_of(z[row * ldz + v], l, c);
-    if (v == a) g = __fsub_rn(g, c);
-    dz[row * ldz + v] = static_cast<uint16_t>(pack_bf16x2(g, 0.f) & 0xffffu);
+    uint16_t* p = ez + row * lde + v;
+    float g;
+    if (v == a) {
+      g = c_onehot;
+    } else {
+      const float sc = __fmul_rn(c, ex2_approx(__fmul_rn(__fsub_rn(mr[v >> 5], l), kLog2e)));
+      g = __fmul_rn(sc, __half2float(__ushort_as_half(*p)));
+    }
+    *p = static_cast<uint16_t>(pack_bf16x2(g, 0.f) & 0xffffu);
   }
 }
 
@@ -765,13 +819,15 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
 
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
-                            float* zgather, float* z, int64_t ldz, int* err, cudaStream_t st) {
+                            float* zgather, uint16_t* e16, int64_t lde, float* emax, int64_t ldm,
+                            int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
   GemmSched s = sched_of(rows, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
   s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
-  EpiLseKeep::Params p{{tokens, part, zgather, static_cast<long long>(rows), V, S}, z, ldz};
+  EpiLseKeep::Params p{{tokens, part, zgather, static_cast<long long>(rows), V, S},
+                       e16, emax, lde, ldm};
   return run_gemm<EpiLseKeep, false, false>(tmH, tmW, s, p, st);
 }
 
@@ -789,12 +845,12 @@ cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32
   return cudaGetLastError();
 }
 
-cudaError_t launch_dz_rows(const float* z, int64_t ldz, uint16_t* dz, int64_t rows, int V,
-                           const int32_t* tokens, const float* lse, const float* coef,
-                           cudaStream_t st) {
+cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t ldm,
+                           int64_t rows, int V, const int32_t* tokens, const float* lse,
+                           const float* coef, const float* logpi, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  dz_rows_kernel<<<static_cast<unsigned>(rows), kDzThreads, 0, st>>>(z, ldz, dz, V, tokens, lse,
-                                                                     coef);
+  dz_rows_kernel<<<static_cast<unsigned>(rows), kDzThreads, 0, st>>>(ez, lde, emax, ldm, V,
+                                                                     tokens, lse, coef, logpi);
   return cudaGetLastError();
 }
 

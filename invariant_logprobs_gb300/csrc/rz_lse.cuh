@@ -17,8 +17,12 @@ namespace rz {
 // Fold 32 logits (natural units; -inf marks a column past V) into the running
 // state (m = max z so far, s = sum 2^((z - m) log2 e)).  z - m is exact for
 // the maximum itself, whose term is exactly 1.  The caller guarantees at
-// least one finite logit.
-__device__ __forceinline__ void lse_fold32(float& m, float& s, const float (&v)[32]) {
+// least one finite logit.  With kKeep the 32 terms 2^((z - m) log2 e), taken
+// against the updated m, are also returned in e (0 past V); the state is
+// computed by the very same operations either way.
+template <bool kKeep>
+__device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float (&v)[32],
+                                                float (&e)[32]) {
   float mx[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
   for (int j = 4; j < 32; j += 4) {
@@ -34,9 +38,22 @@ __device__ __forceinline__ void lse_fold32(float& m, float& s, const float (&v)[
   }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
-    acc[j & 3] = __fadd_rn(acc[j & 3], ex2_approx(__fmul_rn(__fsub_rn(v[j], m), kLog2e)));
+  for (int j = 0; j < 32; ++j) {
+    const float t = ex2_approx(__fmul_rn(__fsub_rn(v[j], m), kLog2e));
+    if (kKeep) e[j] = t;
+    acc[j & 3] = __fadd_rn(acc[j & 3], t);
+  }
   s = __fadd_rn(s, __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])));
+}
+
+__device__ __forceinline__ void lse_fold32(float& m, float& s, const float (&v)[32]) {
+  float unused[32];
+  lse_fold32_impl<false>(m, s, v, unused);
+}
+
+__device__ __forceinline__ void lse_fold32_keep(float& m, float& s, const float (&v)[32],
+                                                float (&e)[32]) {
+  lse_fold32_impl<true>(m, s, v, e);
 }
 
 // Merge the partial states of a row in a fixed order.  P is any struct with

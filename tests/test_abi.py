@@ -56,13 +56,15 @@ def test_workspace_sizes(lib):
     # independent of d, monotone in T
     assert s == rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 1000, 64, V, 0)
     assert rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 2000, 64, V, 0) > s
-    # learner: one chunk of at most 38912 rows x V logits kept in fp32 plus
-    # its dz in bf16 (6 bytes per logit), split states of one chunk, log pi
+    # learner: one chunk of at most 38912 rows x V kept fp16 terms (dz in
+    # place) plus a running max per 32 columns (2.125 bytes per logit), split
+    # states of one chunk, log pi
     big = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, 1_114_112, 2560, V, 128)
-    assert 38912 * V * 6 < big < 38912 * V * 6 + 38912 * (64 * 8 + 16) + 1_114_112 * 4 + 10**6
+    per_row = V * 2 + (V + 31) // 32 * 4
+    assert 38912 * per_row <= big < 38912 * per_row + 38912 * (64 * 8 + 16) + 1_114_112 * 4 + 10**6
     # a short batch only needs its own rows (rounded up to 128)
     small = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, 300, 256, 1024, 8)
-    assert 384 * 1024 * 6 < small < 384 * 1024 * 6 + (1 << 20)
+    assert 384 * (1024 * 2 + 32 * 4) < small < 384 * (1024 * 2 + 32 * 4) + (1 << 20)
     assert rz.workspace_size(rz.RZ_OP_IS_LOSS, 10, 0, 0, 256) >= 256 * 24
     assert rz.workspace_size(99, 10, 10, 10, 10) == 0
 
