@@ -150,7 +150,7 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
   if (T == 0) return RZ_OK;
   CUtensorMap tmH, tmW;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   const FwdLayout L = fwd_layout(T, V);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
   float* zg = reinterpret_cast<float*>(ws + L.zg);
@@ -202,7 +202,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   const int64_t ldm = emax_ld(V);
   CUtensorMap tmH, tmW, tmWmn, tmHmn;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmWmn, W, d, V, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmHmn, H, d, T, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
 
@@ -305,7 +305,7 @@ int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   CUtensorMap tmH, tmW;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   return cuda_status(launch_sample(tmH, tmW, T, d, V, row_ids, seed,
                                    reinterpret_cast<float4*>(w8 + L.part),
@@ -420,7 +420,7 @@ int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32_t d, i
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   CUtensorMap tmH, tmW;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   return cuda_status(launch_logits_f32(tmH, tmW, T, d, V, logits_out, err_flag,
                                        reinterpret_cast<cudaStream_t>(stream)));
 }

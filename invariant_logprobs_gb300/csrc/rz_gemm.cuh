@@ -45,24 +45,6 @@ constexpr uint32_t kEpiStageBytes = 32 * 128;  // per epilogue warp: 32 rows x 1
 constexpr uint32_t kSmemBytes =
     kSmemRing + 1024 /*align*/ + 256 /*barriers*/ + 4 * kEpiStageBytes;
 
-// CTA-pair pipeline (gemm_pair_kernel): M = 256 per tile over two SMs, each
-// CTA stages its own 128 rows of A and its own half (128 rows) of the
-// 256-wide B tile, so a stage is 32 KB per CTA and six of them fit.
-// Off: same tensor work per clock as the single-CTA pipeline, but about 13%
-// more energy per flop, so under the power cap it ran the full-size LM-head
-// GEMM at ~1.24 GHz instead of ~1.40 GHz (18-25% slower).
-constexpr bool kPairTiles = false;
-constexpr int kPairStages = 6;
-constexpr int kBNh = kBN / 2;
-constexpr uint32_t kTileBhBytes = kBNh * kBK * 2;                   // 16 KB
-constexpr uint32_t kPairStageBytes = kTileABytes + kTileBhBytes;    // 32 KB
-constexpr uint32_t kPairRing = kPairStages * kPairStageBytes;       // 192 KB
-constexpr uint32_t kPairSmemBytes =
-    kPairRing + 1024 /*align*/ + 256 /*barriers*/ + 4 * kEpiStageBytes;
-constexpr uint64_t kAbortSettleNs = 20000000ull;  // 20 ms for copies in flight
-// Rows (N) of the K-major B box one CTA loads.
-constexpr uint32_t kBBoxN = kPairTiles ? kBNh : kBN;
-
 struct GemmSched {
   int m_blocks;         // number of 128-row blocks
   int n_tiles;          // number of 256-wide tiles along N
@@ -111,39 +93,6 @@ struct Operands {
   static __device__ __forceinline__ uint64_t desc_b(uint32_t base, int k) {
     if constexpr (!kBMN) return sdesc_sw128(base + 32u * k, 16u, 1024u);
     else return sdesc_sw128(base + 2048u * k, 8192u, 1024u);
-  }
-};
-
-// The pair pipeline's per-CTA operand halves; copies signal the leader's
-// barrier (cluster address `bar`).
-template <bool kAMN, bool kBMN>
-struct PairOperands {
-  // A: this CTA's 128 rows, as in Operands.
-  static __device__ __forceinline__ void load_a(uint8_t* dst, const CUtensorMap* tm, uint32_t bar,
-                                                int m0, int k0) {
-    if constexpr (!kAMN) {
-      tma_load_2d_pair(dst, tm, bar, k0, m0);
-    } else {
-      tma_load_2d_pair(dst, tm, bar, m0, k0);
-      tma_load_2d_pair(dst + 8192, tm, bar, m0 + 64, k0);
-    }
-  }
-  // B: this CTA's 128 of the tile's 256 rows.  K-major: one 64(K) x 128(N)
-  // box.  MN-major: two 64(N) x 64(K) boxes.
-  static __device__ __forceinline__ void load_b(uint8_t* dst, const CUtensorMap* tm, uint32_t bar,
-                                                int n0, int k0) {
-    if constexpr (!kBMN) {
-      tma_load_2d_pair(dst, tm, bar, k0, n0);
-    } else {
-      tma_load_2d_pair(dst, tm, bar, n0, k0);
-      tma_load_2d_pair(dst + 8192, tm, bar, n0 + 64, k0);
-    }
-  }
-  static __device__ __forceinline__ uint64_t desc_a(uint32_t base, int k) {
-    return Operands<kAMN, kBMN>::desc_a(base, k);
-  }
-  static __device__ __forceinline__ uint64_t desc_b(uint32_t base, int k) {
-    return Operands<kAMN, kBMN>::desc_b(base, k);
   }
 };
 
@@ -372,220 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
-// ============================================================== CTA pairs
-// The same pipeline on a cluster of two CTAs (two SMs) that share each
-// 256x256 tile: rank 0 (the leader) issues tcgen05.mma.cta_group::2 with
-// M = 256, reading A rows 0..127 and B rows 0..127 from its own shared
-// memory and A rows 128..255, B rows 128..255 from the peer's (same
-// offsets); accumulator rows 0..127 land in the leader's TMEM, 128..255 in
-// the peer's.  Per CTA the roles are those of gemm_kernel:
-//   warp 0      producer: waits for its own ring slot ("empty", released by
-//               the leader's multicast commit), copies its A and B halves,
-//               both CTAs' copies completing on the LEADER's "full" barrier
-//               (the leader posts the 64 KB expected per stage).
-//   warp 1      both CTAs allocate TMEM together; the leader's lane 0
-//               issues the MMAs and multicasts its commits to both CTAs.
-//   warps 2..5  epilogue over this CTA's 128 rows; releases an accumulator
-//               by arriving on the leader's "tmem empty" barrier (8 warps).
-// Tasks are (256-row pair block, n-tile group); sched.m_blocks counts pair
-// blocks and this CTA's 128-row block is 2 * pair_block + rank.
-template <class Epi, bool kAMN, bool kBMN>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmSched sched,
-                     const typename Epi::Params ep) {
-  using Ops = PairOperands<kAMN, kBMN>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kPairStages * kTileABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPairRing);
-  uint64_t* empty = full + kPairStages;
-  uint64_t* tfull = empty + kPairStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* epi_stage = smem + kPairRing + 256;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int pair = static_cast<int>(blockIdx.x >> 1);
-  const int npairs = static_cast<int>(gridDim.x >> 1);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kPairStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);
-    }
-    mbar_init(drain, 1);
-    *abort = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int task = pair; ok && task < sched.num_tasks; task += npairs) {
-        int pm, grp, nb, ne;
-        task_coords(sched, task, pm, grp, nb, ne);
-        const int m0 = (2 * pm + static_cast<int>(rank)) * kBM + sched.a_m_off;
-        for (int n = nb; ok && n < ne; ++n) {
-          const int n0 = n * kBN + static_cast<int>(rank) * kBNh;
-          for (int kb = 0; kb < sched.k_blocks; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort, kWaitLimitNs)) {
-              raise_abort(abort, sched.err);
-              ok = false;
-              break;
-            }
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPairStageBytes);
-            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-            const int k0 = kb * kBK;
-            Ops::load_a(sA + stage * kTileABytes, &tmA, fb, m0, k0 + sched.a_k_off);
-            Ops::load_b(sB + stage * kTileBhBytes, &tmB, fb, n0, k0 + sched.b_k_off);
-            if (++stage == kPairStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-      }
-      // Tail: wait until the leader's MMAs have released every slot this CTA
-      // filled, so no multicast arrival reaches this CTA after it exits.
-      for (int i = 0; ok && i < kPairStages; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort, kWaitLimitNs)) {
-          raise_abort(abort, sched.err);
-          ok = false;
-          break;
-        }
-        if (++stage == kPairStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (leader && lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, kAMN, kBMN);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t it = 0;
-      bool ok = true;
-      for (int task = pair; ok && task < sched.num_tasks; task += npairs) {
-        int pm, grp, nb, ne;
-        task_coords(sched, task, pm, grp, nb, ne);
-        for (int n = nb; ok && n < ne; ++n, ++it) {
-          const uint32_t buf = it & 1u;
-          const uint32_t use = it >> 1;
-          if (!mbar_wait_cluster(&tempty[buf], (use & 1u) ^ 1u, abort, kWaitLimitNs)) {
-            raise_abort(abort, sched.err);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * kBN;
-          for (int kb = 0; kb < sched.k_blocks; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort, kWaitLimitNs)) {
-              raise_abort(abort, sched.err);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + stage * kTileABytes);
-            const uint32_t b_base = smem_u32(sB + stage * kTileBhBytes);
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              umma_bf16_pair(d_tmem, Ops::desc_a(a_base, k), Ops::desc_b(b_base, k), idesc,
-                             (kb > 0 || k > 0) ? 1u : 0u);
-            }
-            umma_commit_pair_mc(&empty[stage], 0x3);
-            if (++stage == kPairStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          if (ok) umma_commit_pair_mc(&tfull[buf], 0x3);
-        }
-      }
-      // Every MMA issued here has finished before either CTA releases TMEM.
-      umma_commit_pair(drain);
-      if (!mbar_wait(drain, 0, abort, kWaitLimitNs) && !*abort) raise_abort(abort, sched.err);
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
-    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
-    typename Epi::State st;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int task = pair; ok && task < sched.num_tasks; task += npairs) {
-      int pm, grp, nb, ne;
-      task_coords(sched, task, pm, grp, nb, ne);
-      const int m_blk = 2 * pm + static_cast<int>(rank);
-      Epi::task_begin(ep, st, m_blk, grp, row);
-      for (int n = nb; n < ne; ++n, ++it) {
-        const uint32_t buf = it & 1u;
-        const uint32_t use = it >> 1;
-        int got = 1;
-        if (lane == 0) got = mbar_wait<true>(&tfull[buf], use & 1u, abort, kWaitLimitNs) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          if (lane == 0) raise_abort(abort, sched.err);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        Epi::tile(ep, st, m_blk, n, lane_addr + buf * kBN, row,
-                  epi_stage + (warp - 2) * kEpiStageBytes);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
-      }
-      if (ok) Epi::task_end(ep, st, m_blk, grp, row);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (*abort && threadIdx.x == 0) {
-    // Copies issued by either CTA may still be landing: give them time
-    // (bounded) before the pair leaves.
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < kAbortSettleNs) {
-    }
-  }
-  cluster_sync();  // no MMA in flight, no cross-CTA arrival pending
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 

@@ -673,63 +673,18 @@ __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict
 // ============================================================== launchers
 namespace {
 
-// Largest number of two-CTA clusters of `kern` that are resident at once on
-// the current device (cached per device).
-template <class Kern>
-int max_pairs(Kern kern, cudaLaunchConfig_t cfg) {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cache[dev] > 0) return cache[dev];
-  cfg.gridDim = dim3(2);
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-    cudaGetLastError();
-    n = num_sms() / 2;
-  }
-  if (n < 1) n = 1;
-  cache[dev] = n;
-  return n;
-}
-
-// Launch a GEMM: the CTA-pair pipeline (clusters of two, one per pair of
-// SMs, persistent) on 256-row pair blocks, or the single-CTA one.
+// Launch a GEMM: one persistent CTA per SM (or per task, if fewer).
 template <class Epi, bool kAMN, bool kBMN>
-cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& b, GemmSched s,
+cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmSched& s,
                      const typename Epi::Params& p, cudaStream_t st) {
   if (s.num_tasks <= 0) return cudaSuccess;
-  if constexpr (kPairTiles) {
-    auto kern = gemm_pair_kernel<Epi, kAMN, kBMN>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
-    if (e != cudaSuccess) return e;
-    s.m_blocks = (s.m_blocks + 1) / 2;
-    s.num_tasks = s.m_blocks * s.n_groups;
-    s.m_group = s.m_group > 1 ? s.m_group / 2 : 1;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kPairSmemBytes;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const int pairs = max_pairs(kern, cfg);
-    const int np = s.num_tasks < pairs ? s.num_tasks : pairs;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * np));
-    return cudaLaunchKernelEx(&cfg, kern, a, b, s, p);
-  } else {
-    auto kern = gemm_kernel<Epi, kAMN, kBMN>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int grid = s.num_tasks < num_sms() ? s.num_tasks : num_sms();
-    kern<<<grid, kThreads, kSmemBytes, st>>>(a, b, s, p);
-    return cudaGetLastError();
-  }
+  auto kern = gemm_kernel<Epi, kAMN, kBMN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = s.num_tasks < num_sms() ? s.num_tasks : num_sms();
+  kern<<<grid, kThreads, kSmemBytes, st>>>(a, b, s, p);
+  return cudaGetLastError();
 }
 
 // m-blocks per raster group of the vocab-split GEMMs: half the SMs, so at

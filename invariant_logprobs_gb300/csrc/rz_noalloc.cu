@@ -84,7 +84,7 @@ int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const int32_t* 
 
   CUtensorMap tmH, tmW;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
-  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBBoxN)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   float2* part = reinterpret_cast<float2*>(scratch);
   float* zg = reinterpret_cast<float*>(scratch + part_bytes);
