@@ -386,7 +386,7 @@ def gemm_vs_cublas(H, W, tokens, rz, dev, stream, rows=155648, seconds=1.5, roun
 
 
 def launches_per_step(T, V):
-    chunk = 38912  # rows per backward chunk at V = 151936 (6 bytes per logit kept, <= 40 GiB)
+    chunk = 38912  # rows per backward chunk at V = 151936 (2.125 bytes per logit kept)
     n_chunks = (T + chunk - 1) // chunk
     # advantage; response factors; per chunk: logits+lse GEMM, merge+coef, dz pass, dH, dW;
     # loss (2)

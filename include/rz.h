@@ -206,9 +206,11 @@ RZ_API int rz_peak_to_median(const float* series, int64_t n, double* ratio_out);
  *   dH [T,d] bf16 = dz W, dW [V,d] fp32 = dz^T H (overwritten, not
  *   accumulated), with dz_tv = A_i w_t/(B T_i) (softmax_v(z_t) - [v = a_t]).
  * log pi is produced by exactly the rollout computation (bitwise equal to
- * rz_token_logprob on the same H, W, tokens).  The backward pass recomputes
- * logits tile by tile and never stores the [T, V] logits; dW is reduced over
- * token chunks in a fixed order, so results are run-to-run deterministic.
+ * rz_token_logprob on the same H, W, tokens).  Rows are processed in chunks
+ * of up to 38,912: the forward pass keeps, for the chunk only, its softmax
+ * terms exp(z - running max) in fp16 (the [T, V] logits are never stored or
+ * recomputed), from which dz is formed in place; dW is reduced over the
+ * chunks in a fixed order, so results are run-to-run deterministic.
  * Workspace: rz_workspace_size(RZ_OP_LOSS_FWD_BWD, T, d, V, B).
  */
 RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,

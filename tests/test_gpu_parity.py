@@ -318,3 +318,35 @@ def test_equal_rewards_give_zero_advantage_loss_and_gradients(rz):
     assert bool(torch.all(adv == 0))
     assert out["loss"].item() == 0.0
     assert bool(torch.all(out["dH"] == 0)) and bool(torch.all(out["dW"] == 0))
+
+
+@pytest.mark.parametrize("std", [6.0, 14.0])
+def test_learner_peaked_softmax_vs_oracle(rz, std):
+    """Peaked rows (logit standard deviation 6 and 14, tokens drawn from the
+    softmax itself): most terms of a row are many orders below the row's
+    maximum and the sampled token's probability is often close to 1, where
+    dz_a = c (p_a - 1) must keep its digits.  Whole-batch parity, and per
+    row for the rows with 1e-4 < 1 - p_a < 0.1."""
+    g = torch.Generator().manual_seed(int(std))
+    T, d, V = 700, 256, 4099
+    H = _rand_bf16((T, d), 1.0, g)
+    W = _rand_bf16((V, d), std / np.sqrt(d), g)
+    z = H.double() @ W.double().T
+    tok = torch.multinomial(torch.softmax(z, 1), 1, generator=g).squeeze(1).to(torch.int32)
+    cu = torch.tensor([0, 150, 151, 400, 700], dtype=torch.int64)
+    adv = torch.tensor([0.7, -1.3, 0.4, 0.2])
+    lp64, _ = oracle.token_logprob(f64(H), f64(W), f64(tok))
+    logmu = torch.tensor(lp64 + np.random.default_rng(int(std)).normal(0, 0.05, T),
+                         dtype=torch.float32)
+    out = rz.rz_loss_fwd_bwd(H.to(DEV), W.to(DEV), tok.to(DEV), logmu.to(DEV), cu.to(DEV),
+                             adv.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.loss_fwd_bwd(f64(H), f64(W), f64(tok), f64(logmu), f64(cu), f64(adv))
+    _check_learner(out, ref)
+    gap = -np.expm1(ref["logpi"])                        # 1 - p_a
+    rows = np.nonzero((gap > 1e-4) & (gap < 0.1))[0]
+    assert len(rows) >= 20, len(rows)
+    got = f64(out["dH"])[rows]
+    want = ref["dH"][rows]
+    per_row = np.linalg.norm(got - want, axis=1) / np.linalg.norm(want, axis=1)
+    assert per_row.max() <= 2e-2, per_row.max()
