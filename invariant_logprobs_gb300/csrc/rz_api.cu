@@ -220,7 +220,10 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
       return RZ_ERR_UNSUPPORTED;
     if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
       return RZ_ERR_UNSUPPORTED;
-    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, dz, ldz, emax, ldm,
+    CUtensorMap tmE16;
+    if (!make_tmap_bf16(&tmE16, dz, V, rows, uint64_t(ldz) * 2, 64, 32))
+      return RZ_ERR_UNSUPPORTED;
+    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, tmE16, emax, ldm,
                            err_flag, st));
     RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
                                  sc ? nullptr : logmu + r0, cu_seqlens, fac,

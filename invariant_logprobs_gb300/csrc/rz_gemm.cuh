@@ -42,8 +42,10 @@ constexpr int kErrTimeout = 4;                    // RZ_DEVERR_TIMEOUT
 
 constexpr uint32_t kSmemRing = kStages * (kTileABytes + kTileBBytes);
 constexpr uint32_t kEpiStageBytes = 32 * 128;  // per epilogue warp: 32 rows x 128 B
+// ring | barriers (first 256 B of a 1 KB block) | 4 epilogue stages, each
+// 1024-byte aligned (a TMA box with 128-byte swizzle)
 constexpr uint32_t kSmemBytes =
-    kSmemRing + 1024 /*align*/ + 256 /*barriers*/ + 4 * kEpiStageBytes;
+    kSmemRing + 1024 /*align*/ + 1024 /*barriers*/ + 4 * kEpiStageBytes;
 
 struct GemmSched {
   int m_blocks;         // number of 128-row blocks
@@ -128,11 +130,13 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, int* err) {
 //   static void task_end(const Params&, State&, int m_blk, int grp, int row);
 // `row` is the thread's row inside the 128-row block; `taddr` the TMEM
 // address of (this warp's 32 lanes, column 0) of the tile's accumulator;
-// `stage` a private 4 KB shared-memory buffer of the warp (128 B per row).
+// `stage` a private 4 KB shared-memory buffer of the warp (128 B per row,
+// 1024-byte aligned).  Params is a __grid_constant__ kernel parameter, so a
+// tensor map inside it can serve TMA stores.
 template <class Epi, bool kAMN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmSched sched, const typename Epi::Params ep) {
+                const GemmSched sched, const __grid_constant__ typename Epi::Params ep) {
   using Ops = Operands<kAMN, kBMN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* issued_ring = reinterpret_cast<int*>(tmem_slot + 2);  // [0] issued, [1] consumed
-  uint8_t* epi_stage = smem + kSmemRing + 256;
+  uint8_t* epi_stage = smem + kSmemRing + 1024;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -297,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) Epi::task_end(ep, st, m_blk, grp, row);
     }
+    // bulk stores an epilogue issued from its stage have completed
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();

@@ -51,9 +51,10 @@ cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const floa
 cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
                           int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st);
+// tmE16: the chunk's fp16 terms [rows, V] (row stride dz_ld(V)), box 64 x 32.
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
-                            float* zgather, uint16_t* e16, int64_t lde, float* emax, int64_t ldm,
+                            float* zgather, const CUtensorMap& tmE16, float* emax, int64_t ldm,
                             int* err, cudaStream_t st);
 cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32_t* tokens,
                                   const float2* part, const float* zgather, float* logprob,

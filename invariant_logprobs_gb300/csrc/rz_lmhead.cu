@@ -112,10 +112,9 @@ struct EpiLsePartial {
 // log2 e) then needs only the row's final log-sum-exp.
 struct EpiLseKeep {
   struct Params {
+    CUtensorMap tm_e16;         // the terms [rows, V] fp16, box 64 x 32, 128-byte swizzle
     EpiLsePartial::Params lse;  // chunk-local rows: T = rows of the chunk
-    uint16_t* e16;              // [rows, lde] fp16 terms (later overwritten by dz)
     float* emax;                // [rows, ldm] m per 32-column slice
-    long long lde;              // multiple of 8
     long long ldm;              // >= ceil(V / 32), even
   };
   using State = EpiLsePartial::State;
@@ -154,17 +153,18 @@ struct EpiLseKeep {
   }
 
   // A 64-column slab of the warp's 32 rows goes through the warp's stage
-  // (row r at r*128, 16-byte piece j at j ^ (r & 7)) so each global store
-  // instruction writes four whole 128-byte row segments; evict-first, since
-  // the terms are read back only after the whole chunk and would otherwise
-  // push the H and W tiles the CTAs share out of L2.
+  // (row r at r*128, 16-byte piece j at j ^ (r & 7): the 128-byte swizzle)
+  // and out with one TMA store (evict-first: the terms are read back only
+  // after the whole chunk and would otherwise push the H and W tiles the
+  // CTAs share out of L2).  Rows past the chunk and columns past V are
+  // clipped by the tensor map.
   static __device__ __forceinline__ void tile(const Params& p, State& st, int m_blk, int n_tile,
                                               uint32_t taddr, int row, uint8_t* stage) {
     const int col0 = n_tile * kBN;
     const int V = p.lse.V;
     const int lane = row & 31;
     const long long grow = static_cast<long long>(m_blk) * kBM + row;
-    const long long rbase = static_cast<long long>(m_blk) * kBM + (row & ~31);
+    const int rbase = m_blk * kBM + (row & ~31);
     const uint64_t pol = l2_policy_first();
     uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll 1
@@ -190,30 +190,17 @@ struct EpiLseKeep {
           em[0] = m0;
         }
       }
+      if (lane == 0) bulk_wait_read();  // the previous slab's store has read the stage
+      __syncwarp();
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         mine[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      fence_proxy_async_smem();
       __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int rr = 4 * k + (lane >> 3);
-        const int j = lane & 7;
-        const uint4 v = reinterpret_cast<const uint4*>(stage + rr * 128)[j ^ (rr & 7)];
-        const long long gr = rbase + rr;
-        const int col = col0 + c + 8 * j;
-        if (gr < p.lse.T && col < V) {
-          uint16_t* dst = p.e16 + gr * p.lde + col;
-          if (col + 8 <= V) {
-            st_l2hint(reinterpret_cast<uint4*>(dst), v, pol);
-          } else {
-            for (int q = 0; col + q < V; ++q) {
-              const uint32_t word = q < 2 ? v.x : (q < 4 ? v.y : (q < 6 ? v.z : v.w));
-              dst[q] = static_cast<uint16_t>((word >> (16 * (q & 1))) & 0xffffu);
-            }
-          }
-        }
+      if (lane == 0 && rbase < p.lse.T) {
+        tma_store_2d_hint(&p.tm_e16, stage, col0 + c, rbase, pol);
+        bulk_commit();
       }
-      __syncwarp();
     }
   }
 };
@@ -774,15 +761,15 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
 
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
-                            float* zgather, uint16_t* e16, int64_t lde, float* emax, int64_t ldm,
+                            float* zgather, const CUtensorMap& tmE16, float* emax, int64_t ldm,
                             int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
   GemmSched s = sched_of(rows, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
   s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
-  EpiLseKeep::Params p{{tokens, part, zgather, static_cast<long long>(rows), V, S},
-                       e16, emax, lde, ldm};
+  EpiLseKeep::Params p{tmE16, {tokens, part, zgather, static_cast<long long>(rows), V, S}, emax,
+                       ldm};
   return run_gemm<EpiLseKeep, false, false>(tmH, tmW, s, p, st);
 }
 

@@ -100,6 +100,33 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
       : "memory");
 }
 
+// 2-D tiled bulk tensor copy shared -> global from a 1024-byte aligned,
+// 128-byte swizzled stage (the box of `tm`), with an L2 cache policy.  The
+// copy reads shared memory asynchronously: the stage may be rewritten only
+// after bulk_wait_read(); the writes must have been made visible to the
+// async proxy first (fence_proxy_async_smem).  Coordinates are never
+// negative here; parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, const void* smem_src,
+                                                  int32_t c0, int32_t c1, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
