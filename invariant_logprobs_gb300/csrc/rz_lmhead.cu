@@ -390,7 +390,7 @@ struct EpiSample {
       if (col0 + c >= p.V) break;  // warp-uniform
       uint32_t r0[32];
       tmem_ld32(taddr + c, r0);
-#pragma unroll 1
+#pragma unroll 2  // two independent Philox blocks in flight: the chain is latency-bound
       for (int q = 0; q < 8; ++q) {
         uint32_t x[4];
         st.rng.words(static_cast<uint32_t>((col0 + c) >> 2) + q, x);
