@@ -32,8 +32,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # blocks of one call), from the 1-pass ncu capture summarised in
 # profiles/logprob_gemm_dram_traffic_fullsize.md.  Valid only while the GEMM
 # sources hash to the value recorded with it; otherwise reported as null.
-TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 5.2774e9 + 0.0511e9,
-                   "rows_per_launch": 38912, "sources_sha256_16": "70833ee576dc918a"}
+TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 4.2770e9 + 0.0481e9,
+                   "rows_per_launch": 38912, "sources_sha256_16": "4d8129ba19ae8e44"}
 GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_math.cuh",
                 "rz_internal.h"]
 

@@ -4,10 +4,11 @@
 //
 // Purely bandwidth-bound (no contraction): one CTA streams one row with
 // 16-byte loads, four in flight per thread.  Pass 1 computes (max, sum exp)
-// online and keeps the first 96 KB of the row in shared memory; pass 2
-// re-reads the rest (mostly from L2) and overwrites the row with dz.  Two
-// CTAs per SM keep ~300 rows (~90 MB) in flight, inside the 129 MB L2.  The loss and D3 over all rows are then
-// reduced by the same fixed-order kernels as the hidden-state path.
+// online and keeps the first 64 KB of the row in shared memory; pass 2
+// re-reads the rest (mostly from L2) and overwrites the row with dz.  Three
+// CTAs per SM keep ~456 rows in flight, their re-read parts inside the L2.
+// The loss and D3 over all rows are then reduced by the same fixed-order
+// kernels as the hidden-state path.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -22,7 +23,12 @@ namespace rz {
 namespace {
 
 constexpr int kRowThreads = 512;
-constexpr int kStashVec = 6144;  // 96 KB of the row kept in shared memory
+// 64 KB of each row kept in shared memory: three rows per SM in flight, and
+// the rest of their rows (re-read in pass 2, ~240 KB each at V = 151936,
+// ~109 MB over 456 rows) still fits the L2.  (96 KB and two rows per SM:
+// 30.6 ms per 262,144-row step; 64 KB and three: 27.5 ms; 72 KB no longer
+// fits three per SM.)
+constexpr int kStashVec = 4096;
 constexpr size_t kRowSmem = kStashVec * sizeof(uint4);
 
 // L2 eviction priorities: the part of a row that pass 2 will read again from
@@ -71,7 +77,7 @@ __device__ __forceinline__ uint4 dz8(const uint4& q, float nl, float c, int rel)
   return o;
 }
 
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 registers)
     logits_row_kernel(uint16_t* __restrict__ logits, long long T, int V,
                       const int32_t* __restrict__ tokens, const float* __restrict__ logmu,
                       const int64_t* __restrict__ cu, const float* __restrict__ scale,
