@@ -272,7 +272,7 @@ size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
     case RZ_OP_TOKEN_LOGPROB: return fwd_layout(T, V > 0 ? V : 1).total;
     case RZ_OP_LOSS_FWD_BWD:
     case RZ_OP_SC_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
-    case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B) + resp_scale_ws_bytes(B);
+    case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B) + resp_factors_ws_bytes(B);
     case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
     case RZ_OP_SAMPLE: return sample_layout(T, V > 0 ? V : 1).total;
     default: return 0;
@@ -404,9 +404,9 @@ int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const f
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  float* scale = reinterpret_cast<float*>(w8 + is_loss_ws_bytes(B));
-  RZ_TRY(launch_resp_scale(cu_seqlens, adv, action_mask, B, T, scale, st));
-  RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, scale, action_mask, B,
+  float2* fac = reinterpret_cast<float2*>(w8 + is_loss_ws_bytes(B));
+  RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+  RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, fac, action_mask, B,
                             logprob_out, err_flag, st));
   RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
                         nullptr, ws, err_flag, st));

@@ -78,9 +78,7 @@ cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cud
 cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
                            const float* adv, const uint8_t* mask, int B, int64_t T, float* loss,
                            float* d3, float* coef, void* ws, int* err, cudaStream_t st);
-size_t resp_scale_ws_bytes(int32_t B);
-cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
-                              int64_t T, float* scale, cudaStream_t st);
+// Per-response factors (A_i, 1/(B T_i)) of the coefficient c_t = A_i w_t/(B T_i).
 size_t resp_factors_ws_bytes(int32_t B);
 cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
                                 int64_t T, float2* fac, cudaStream_t st);
@@ -97,7 +95,7 @@ cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, f
 
 // ---- given-logits kernel (rz_logits.cu)
 cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
-                               const float* logmu, const int64_t* cu, const float* scale,
+                               const float* logmu, const int64_t* cu, const float2* fac,
                                const uint8_t* mask, int B, float* logprob, int* err,
                                cudaStream_t st);
 

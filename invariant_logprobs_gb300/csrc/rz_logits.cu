@@ -80,7 +80,7 @@ __device__ __forceinline__ uint4 dz8(const uint4& q, float nl, float c, int rel)
 __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 registers)
     logits_row_kernel(uint16_t* __restrict__ logits, long long T, int V,
                       const int32_t* __restrict__ tokens, const float* __restrict__ logmu,
-                      const int64_t* __restrict__ cu, const float* __restrict__ scale,
+                      const int64_t* __restrict__ cu, const float2* __restrict__ fac,
                       const uint8_t* __restrict__ mask, int B, float* __restrict__ logprob,
                       int* err) {
   extern __shared__ uint4 stash[];
@@ -152,7 +152,9 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
       }
       // c_t = A_i w_t / (B T_i); 0 for a masked (non-action) token
       const bool act = !mask || mask[row] != 0;
-      c = act ? scale[lo] * is_weight(lp, logmu[row]) : 0.f;
+      // same factors and rounding as the hidden-state learner:
+      // fac[i] = (A_i, 1/(B T_i)), c = A_i w_t (1/(B T_i))
+      c = act ? fac[lo].x * is_weight(lp, logmu[row]) * fac[lo].y : 0.f;
     }
     logprob[row] = lp;
     bc[0] = -l2;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
 }  // namespace
 
 cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
-                               const float* logmu, const int64_t* cu, const float* scale,
+                               const float* logmu, const int64_t* cu, const float2* fac,
                                const uint8_t* mask, int B, float* logprob, int* err,
                                cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
@@ -199,7 +201,7 @@ cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t
                                        static_cast<int>(kRowSmem));
   if (e != cudaSuccess) return e;
   logits_row_kernel<<<static_cast<unsigned>(T), kRowThreads, kRowSmem, st>>>(
-      logits, T, V, tokens, logmu, cu, scale, mask, B, logprob, err);
+      logits, T, V, tokens, logmu, cu, fac, mask, B, logprob, err);
   return cudaGetLastError();
 }
 

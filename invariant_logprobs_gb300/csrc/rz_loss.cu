@@ -95,25 +95,9 @@ __global__ void __launch_bounds__(kRespThreads)
   }
 }
 
-// Per-response coefficient A_i / (B T_i) (0 for an empty response), for the
-// given-logits kernel which forms c_t = scale_i w_t itself.
-__global__ void resp_scale_kernel(const int64_t* __restrict__ cu, const float* __restrict__ adv,
-                                  const uint8_t* __restrict__ mask, int B, long long T,
-                                  float* __restrict__ scale) {
-  __shared__ int redi[kRespThreads / 32];
-  const int i = blockIdx.x;
-  long long s = cu[i];
-  long long e = cu[i + 1];
-  if (s < 0 || s > T) s = 0;
-  if (e < s || e > T) e = s;
-  const long long Ti = valid_count(mask, s, e, redi);
-  if (threadIdx.x == 0)
-    scale[i] = Ti > 0 ? adv[i] * static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
-}
-
-// Per-response factors (A_i, 1/(B T_i)) (second 0 for an empty response), for
-// the learner's chunked backward, which forms c_t = A_i w_t (1/(B T_i)) with
-// the same rounding as is_loss_resp_kernel's coefficient.
+// Per-response factors (A_i, 1/(B T_i)) (second 0 for an empty response), from
+// which the learner and the given-logits kernel form c_t = A_i w_t (1/(B T_i))
+// with the same rounding as is_loss_resp_kernel's coefficient.
 __global__ void resp_factors_kernel(const int64_t* __restrict__ cu, const float* __restrict__ adv,
                                     const uint8_t* __restrict__ mask, int B, long long T,
                                     float2* __restrict__ fac) {
@@ -273,11 +257,6 @@ size_t is_loss_ws_bytes(int32_t B) {
   return (b * sizeof(RespPart) + 255) / 256 * 256;
 }
 
-size_t resp_scale_ws_bytes(int32_t B) {
-  const size_t b = B > 0 ? static_cast<size_t>(B) : 0;
-  return (b * sizeof(float) + 255) / 256 * 256;
-}
-
 cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
   const int threads = 256;
@@ -296,13 +275,6 @@ cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t
     if (e != cudaSuccess) return e;
   }
   is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, loss, d3);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_resp_scale(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
-                              int64_t T, float* scale, cudaStream_t st) {
-  if (B <= 0) return cudaSuccess;
-  resp_scale_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, B, T, scale);
   return cudaGetLastError();
 }
 
