@@ -28,33 +28,47 @@ if ROOT not in sys.path:
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) of one logprob-GEMM launch of the 4B-shaped
-# workload (one 38,912-row block of the 1,083,112 rows; mean of the 27 full
+# workload (one 38,912-row block of the 1,083,112 rows; median of the 27 full
 # blocks of one call), from the 1-pass ncu capture summarised in
 # profiles/logprob_gemm_dram_traffic_fullsize.md.  Valid only while the GEMM
 # sources hash to the value recorded with it; otherwise reported as null.
-TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 4.2770e9 + 0.0481e9,
-                   "rows_per_launch": 38912, "sources_sha256_16": "4d8129ba19ae8e44"}
+TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 4.3941e9 + 0.0495e9,
+                   "rows_per_launch": 38912, "sources_sha256_16": "2b3585dd752b3c93"}
 GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_math.cuh",
                 "rz_internal.h"]
 
+# DRAM bytes (read + write) of one launch of the given-logits kernel over the
+# 262,144-row MoE-shaped workload (1-pass ncu capture summarised in
+# profiles/logits_row_kernel_moe30b_8192rows.md), tied to its sources' hash.
+LOGITS_TRAFFIC_CAPTURE = {"workload": "moe30b_logits", "bytes": 106.960e9 + 79.575e9,
+                          "sources_sha256_16": "d67650bec883fd47"}
+LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 
-def gemm_sources_hash():
+
+def sources_hash(files):
     import hashlib
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "invariant_logprobs_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
+def gemm_sources_hash():
+    return sources_hash(GEMM_SOURCES)
+
+
 def captured_traffic(workload):
-    if workload != TRAFFIC_CAPTURE["workload"]:
+    cap, files = {TRAFFIC_CAPTURE["workload"]: (TRAFFIC_CAPTURE, GEMM_SOURCES),
+                  LOGITS_TRAFFIC_CAPTURE["workload"]: (LOGITS_TRAFFIC_CAPTURE, LOGITS_SOURCES)
+                  }.get(workload, (None, None))
+    if cap is None or cap["bytes"] is None:
         return None
     try:
-        ok = gemm_sources_hash() == TRAFFIC_CAPTURE["sources_sha256_16"]
+        ok = sources_hash(files) == cap["sources_sha256_16"]
     except OSError:
         ok = False
-    return TRAFFIC_CAPTURE["bytes"] if ok else None
+    return cap["bytes"] if ok else None
 METRIC = "action tokens/s, fused logprob+IS-loss fwd/bwd (1 GB300); % bf16 tensor roofline"
 
 
@@ -506,7 +520,11 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
         "roofline": {"kernel": "logits_row_kernel", "bound": "hbm",
                      "achieved": alg_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": alg_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                     "peak_source": "%s hbm_gbs" % peak_src, "traffic": None},
+                     "peak_source": "%s hbm_gbs" % peak_src,
+                     "traffic": captured_traffic(wl.name),
+                     "traffic_unit": "DRAM bytes per launch (262,144 rows; ncu capture, "
+                                     "see profiles/)",
+                     "algorithmic_bytes_per_launch": alg_bytes},
         "clocks": clocks,
         "gpu_launches": 3 * args.steps,
         "device_err_flag": int(err.item()),
