@@ -526,7 +526,7 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
                                      "see profiles/)",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # response factors, row kernel, loss (2)
         "device_err_flag": int(err.item()),
     }
     if rank == 0:
