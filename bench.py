@@ -634,7 +634,7 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="qwen4b_lag64",
                     choices=["qwen4b_lag64", "qwen1p5b_lag2", "moe30b_logits", "tiny"])
