@@ -100,8 +100,10 @@ RZ_API const char* rz_status_string(int status);
  *                         z = H W^T (fp32 accumulation, temperature 1)
  *   lse_out [T] fp32      logsumexp_v z_tv (nullable)
  * Rows whose token is out of range get NaN and set RZ_DEVERR_TOKEN_RANGE.
- * The learner side (rz_loss_fwd_bwd) runs this very computation with the same
- * kernels and launch shape, so both sides agree bit for bit at equal weights
+ * Rows are processed in blocks of 38,912 (one GEMM launch each).  The learner
+ * side (rz_loss_fwd_bwd) runs this very computation -- the same tiles, K
+ * order, vocab splits and log-sum-exp fold, only keeping more of it for its
+ * backward pass -- so both sides agree bit for bit at equal weights
  * [vLLM-zh s.5 "diff 0"].
  */
 RZ_API int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
