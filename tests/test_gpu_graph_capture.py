@@ -1,0 +1,78 @@
+"""The rollout and learner entry points inside a captured CUDA graph: they
+allocate nothing and never synchronise the host, so a graph captured once
+replays them exactly -- bit for bit the eager results, also after the
+inputs are rewritten in place between replays."""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(g, T, d, V):
+    H = torch.randn(T, d, generator=g, device=DEV).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, device=DEV, dtype=torch.int32)
+    return H, W, tok
+
+
+def test_rollout_and_learner_replay_bitwise(rz):
+    T, d, V, B = 1500, 256, 5003, 6
+    g = torch.Generator(device=DEV)
+    g.manual_seed(31)
+    H, W, tok = _inputs(g, T, d, V)
+    cu = torch.tensor([0, 100, 400, 401, 900, 1200, 1500], dtype=torch.int64, device=DEV)
+    adv = torch.randn(B, generator=g, device=DEV)
+    logmu = torch.empty(T, device=DEV)
+
+    # buffers the graph will own
+    ws_r = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, DEV)
+    ws_l = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, B, DEV)
+    lp = torch.empty(T, device=DEV)
+    dH = torch.empty(T, d, dtype=torch.bfloat16, device=DEV)
+    dW = torch.empty(V, d, device=DEV)
+    loss = torch.empty(1, device=DEV)
+    d3 = torch.empty(1, device=DEV)
+
+    def work():
+        rz.rz_token_logprob(H, W, tok, logprob_out=logmu, ws=ws_r)
+        logmu.add_(-0.01)  # a small recorded-vs-learner gap, inside the graph too
+        rz.rz_loss_fwd_bwd(H, W, tok, logmu, cu, adv, logprob_out=lp, dH=dH, dW=dW,
+                           loss_out=loss, d3_out=d3, ws=ws_l)
+
+    def snapshot():
+        torch.cuda.synchronize()
+        return [x.clone() for x in (logmu, lp, dH, dW, loss, d3)]
+
+    work()
+    eager = snapshot()
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        work()  # warm-up on the side stream, as graph capture expects
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        work()
+    for x in (logmu, lp, dH, dW, loss, d3):
+        x.zero_()
+    graph.replay()
+    replay = snapshot()
+    for a, b in zip(eager, replay):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+    # new inputs written in place, then replay vs eager on the same inputs
+    H.copy_(torch.randn(T, d, generator=g, device=DEV).to(torch.bfloat16))
+    tok.copy_(torch.randint(0, V, (T,), generator=g, device=DEV, dtype=torch.int32))
+    graph.replay()
+    replay2 = snapshot()
+    work()
+    eager2 = snapshot()
+    for a, b in zip(eager2, replay2):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert not np.array_equal(bits(replay2[1]), bits(replay[1]))  # the inputs did change
