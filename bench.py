@@ -185,6 +185,33 @@ def oracle_sample(b, n_tokens, seed=7):
             "adv": b["adv"][:k].cpu().double().numpy(), "T": T}
 
 
+def logits_oracle_sample(logits, tokens, logmu, cu, adv, n_tokens):
+    """The given-logits counterpart of oracle_sample: the first n_tokens rows
+    (whole responses where they fit, the last one cut short), bf16 logits
+    widened exactly to fp32 on the host."""
+    import numpy as np
+    import torch
+    cu = cu.cpu().numpy()
+    B = cu.shape[0] - 1
+    k = 1
+    while k < B and cu[k] < n_tokens:
+        k += 1
+    T = min(int(cu[k]), n_tokens)
+    return {"logits": logits[:T].to("cpu", torch.float32).numpy(),
+            "tokens": tokens[:T].cpu().numpy(), "logmu": logmu[:T].cpu().double().numpy(),
+            "cu": np.minimum(cu[:k + 1], T), "adv": adv[:k].cpu().double().numpy(), "T": T}
+
+
+def time_logits_oracle(sample, reps=1):
+    import oracle
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.logits_loss_fwd_bwd(sample["logits"], sample["tokens"], sample["logmu"],
+                                   sample["cu"], sample["adv"])
+    dt = (time.perf_counter() - t0) / reps
+    return sample["T"] / dt, dt
+
+
 def time_oracle(sample, reps=1):
     import oracle
     import numpy as np
@@ -529,6 +556,14 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
         "gpu_launches": 4 * args.steps,  # response factors, row kernel, loss (2)
         "device_err_flag": int(err.item()),
     }
+    if rank == 0 and not args.no_cpu_baseline:
+        s = logits_oracle_sample(b["logits"], b["tokens"], logmu, b["cu"], adv, args.cpu_tokens)
+        v, dt = time_logits_oracle(s)
+        out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_threads(),
+                               "kind": "oracle",
+                               "sample": "first %d rows of the same logits at V=%d (log pi, "
+                                         "loss, dz for every row); fp64 numpy, %.1f s"
+                                         % (s["T"], V, dt)}
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
@@ -546,9 +581,7 @@ def run_reference(args):
     from invariant_logprobs_gb300 import synth
     import oracle
     if args.config == "moe30b_logits":
-        print(json.dumps({"impl": "reference", "unavailable":
-                          "reference arm is defined for the hidden-state learner workloads"}))
-        return 0
+        return run_reference_logits(args, world)
     wl = synth.WORKLOADS[args.config]
     # draw the same distributions on the host (no GPU needed): a small batch
     # of whole responses at full d and V
@@ -579,6 +612,49 @@ def run_reference(args):
                             "kind": "oracle",
                             "sample": "%d tokens at full d=%d, V=%d per step" % (
                                 s["T"], wl.d, wl.V)},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def run_reference_logits(args, world):
+    """Reference arm of the given-logits workload: the oracle on one group of
+    responses drawn with the same distributions (N(0,3) logits at full V,
+    uniform tokens, log mu = log pi + N(0,0.05)), --cpu-tokens rows in all."""
+    import dataclasses
+    import numpy as np
+    import torch
+    from invariant_logprobs_gb300 import synth
+    import oracle
+    wl = synth.WORKLOADS["moe30b_logits"]
+    n = max(wl.group, args.cpu_tokens)
+    small = dataclasses.replace(wl, len_lo=n // wl.group, len_hi=n // wl.group)
+    b = synth.make_logits_batch(small, device="cpu", T=n // wl.group * wl.group)
+    T = b["T"]
+    logits = b["logits"].to(torch.float32).numpy()
+    tokens, cu = b["tokens"].numpy(), b["cu"].numpy()
+    adv = oracle.group_advantage(b["rewards"].double().numpy(), b["G"])
+    logpi = oracle.logits_loss_fwd_bwd(logits, tokens, np.zeros(T), cu, adv,
+                                       rows=np.zeros(0, np.int64))["logpi"]
+    logmu = synth.logmu_near(torch.tensor(logpi), synth.LOGMU_NOISE_STD, b["gen"])
+    s = {"logits": logits, "tokens": tokens, "logmu": logmu.double().numpy(), "cu": cu,
+         "adv": adv, "T": T}
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_logits_oracle(s)
+    times = [time_logits_oracle(s)[1] for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    v = T / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)",
+           "config": {"workload": wl.name, "V": wl.V, "tokens_per_step": T,
+                      "responses": b["B"], "parallelism": "cpu oracle, rank 0"},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_threads(),
+                            "kind": "oracle",
+                            "sample": "%d rows of %d responses at V=%d per step" % (
+                                T, b["B"], wl.V)},
            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
