@@ -124,3 +124,70 @@ def test_peak_to_median_host_function(lib):
         assert rz.rz_peak_to_median(list(x)) == pytest.approx(oracle.peak_to_median(x), rel=1e-12)
     out = ctypes.c_double(0)
     assert lib.rz_peak_to_median(None, 3, ctypes.byref(out)) == 1
+
+
+def _declared_arity():
+    """name -> number of parameters, parsed from the prototypes in rz.h."""
+    src = open(HEADER).read()
+    out = {}
+    for m in re.finditer(r"^RZ_API\s+[\w\s\*]+?\b(rz_\w+)\s*\(([^)]*)\)\s*;", src, flags=re.M):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    import invariant_logprobs_gb300 as rz
+    arity = _declared_arity()
+    assert set(arity) == set(_declared())
+    for name, n in arity.items():
+        assert name in rz._SIGNATURES, name
+        assert len(rz._SIGNATURES[name][1]) == n, name
+
+
+def test_more_host_side_argument_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails validation first
+    odd = P((1 << 20) + 8)  # 8-byte but not 16-byte aligned
+    null = None
+    big = 1 << 40
+    # Score Centering learner: B = 0 with tokens, missing dW, d % 8, misaligned
+    # dW, workspace too small
+    sc = lib.rz_sc_loss_fwd_bwd
+    assert sc(fake, fake, fake, fake, fake, null, 0, 5, 16, 100, fake, null, fake, fake,
+              fake, big, null, null) == 1
+    assert sc(fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, fake, null,
+              fake, big, null, null) == 1
+    assert sc(fake, fake, fake, fake, fake, null, 2, 5, 12, 100, fake, null, fake, fake,
+              fake, big, null, null) == 2
+    assert sc(fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, fake, odd,
+              fake, big, null, null) == 2
+    assert sc(fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, fake, fake,
+              fake, 64, null, null) == 3
+    # IS learner: D3 output and log mu are required
+    isl = lib.rz_loss_fwd_bwd
+    assert isl(fake, fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, null,
+               fake, fake, fake, big, null, null) == 1
+    assert isl(fake, fake, fake, null, fake, fake, null, 2, 5, 16, 100, fake, fake, null,
+               fake, fake, fake, big, null, null) == 1
+    # fused sampler: missing tokens_out, d % 8, missing workspace; T = 0 is a no-op
+    smp = lib.rz_sample_logprob
+    assert smp(fake, fake, null, 5, 16, 100, 1, null, fake, null, fake, big, null, null) == 1
+    assert smp(fake, fake, null, 5, 20, 100, 1, fake, fake, null, fake, big, null, null) == 2
+    assert smp(fake, fake, null, 5, 16, 100, 1, fake, fake, null, null, big, null, null) == 3
+    assert smp(null, null, null, 0, 16, 100, 1, null, null, null, null, 0, null, null) == 0
+    # logits: missing output, misaligned W
+    assert lib.rz_lmhead_logits(fake, fake, 5, 16, 100, null, null, null) == 1
+    assert lib.rz_lmhead_logits(fake, odd, 5, 16, 100, fake, null, null) == 2
+    # no-alloc entry point: past its built-in scratch, bad d
+    assert lib.rz_token_logprob_noalloc(fake, fake, fake, 10_000_000, 16, 151936, fake, null,
+                                        null, null) == 5
+    assert lib.rz_token_logprob_noalloc(fake, fake, fake, 5, 7, 100, fake, null, null,
+                                        null) == 1
+    # self-test: the wait limit must be 1 us .. 2 s and the flag present
+    assert lib.rz_selftest_wait_timeout(fake, null, 0, null) == 1
+    assert lib.rz_selftest_wait_timeout(fake, null, 2_000_001, null) == 1
+    assert lib.rz_selftest_wait_timeout(null, null, 1000, null) == 1
+    # diagnostics: negative T
+    assert lib.rz_is_stats(fake, fake, -1, fake, null) == 1
+    assert lib.rz_d3(null, null, 5, fake, null) == 1
