@@ -108,9 +108,17 @@ def _ptr(t):
 
 
 def _stream(stream):
+    """The stream handle to launch on: the given torch stream, which must
+    belong to the current device (the library launches there), else the
+    current device's current stream."""
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    dev = getattr(stream, "device", None)
+    if dev is not None and dev.index is not None and dev.index != torch.cuda.current_device():
+        raise ValueError("stream is on %s but the current device is cuda:%d"
+                         % (dev, torch.cuda.current_device()))
+    return ctypes.c_void_p(stream.cuda_stream)
 
 
 def _check(name, status):
@@ -124,15 +132,43 @@ def _need(t, dtype, name):
         raise TypeError("%s must be a contiguous CUDA tensor of %s" % (name, dtype))
 
 
+def _out(t, dtype, name, shape=None, min_numel=1):
+    """Check a caller-supplied output buffer (None is allowed: the wrapper
+    allocates it): dtype, contiguity and device as _need, then the exact
+    shape or at least min_numel elements, so that the library never writes
+    past its end."""
+    if t is None:
+        return
+    _need(t, dtype, name)
+    if shape is not None:
+        _shape(t, shape, name)
+    elif t.numel() < min_numel:
+        raise ValueError("%s needs at least %d elements, got %d" % (name, min_numel, t.numel()))
+
+
+def _ws_bytes(ws):
+    """Size in bytes of a caller workspace (a contiguous CUDA uint8 tensor)."""
+    _need(ws, _torch().uint8, "ws")
+    return ws.numel()
+
+
 def _shape(t, shape, name):
     if t is not None and tuple(t.shape) != tuple(shape):
         raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
 
 
 def _same_device(*ts):
+    """All tensors on one CUDA device, and that the current device: the
+    library launches on the current device's context."""
     devs = {t.device for t in ts if t is not None}
     if len(devs) > 1:
         raise ValueError("all tensors must be on one CUDA device, got %s" % sorted(map(str, devs)))
+    if devs:
+        dev = next(iter(devs))
+        cur = _torch().cuda.current_device()
+        if dev.type == "cuda" and dev.index is not None and dev.index != cur:
+            raise ValueError("tensors are on %s but the current device is cuda:%d; call under "
+                             "torch.cuda.device(%s)" % (dev, cur, dev))
 
 
 def alloc_workspace(op, T, d, V, B, device):
@@ -164,14 +200,13 @@ def rz_token_logprob(H, W, tokens, logprob_out=None, lse_out=None, ws=None, err_
         logprob_out = torch.empty(T, dtype=torch.float32, device=H.device)
     _need(logprob_out, torch.float32, "logprob_out")
     _shape(logprob_out, (T,), "logprob_out")
-    if lse_out is not None:
-        _need(lse_out, torch.float32, "lse_out")
-        _shape(lse_out, (T,), "lse_out")
+    _out(lse_out, torch.float32, "lse_out", (T,))
+    _out(err_flag, torch.int32, "err_flag")
     _same_device(H, W, tokens, logprob_out, lse_out, ws, err_flag)
     if ws is None:
         ws = alloc_workspace(RZ_OP_TOKEN_LOGPROB, T, d, V, 0, H.device)
     st = lib.rz_token_logprob(_ptr(H), _ptr(W), _ptr(tokens), T, d, V, _ptr(logprob_out),
-                              _ptr(lse_out), _ptr(ws), ws.numel(), _ptr(err_flag),
+                              _ptr(lse_out), _ptr(ws), _ws_bytes(ws), _ptr(err_flag),
                               _stream(stream))
     _check("rz_token_logprob", st)
     return logprob_out, lse_out
@@ -204,11 +239,13 @@ def rz_is_loss(logpi, logmu, cu_seqlens, adv, loss_out=None, d3_out=None, coef_o
     T = logpi.shape[0]
     _shape(logmu, (T,), "logmu")
     _shape(adv, (B,), "adv")
-    if coef_out is not None:
-        _need(coef_out, torch.float32, "coef_out")
-        _shape(coef_out, (T,), "coef_out")
+    _out(coef_out, torch.float32, "coef_out", (T,))
+    _out(loss_out, torch.float32, "loss_out")
+    _out(d3_out, torch.float32, "d3_out")
+    _out(err_flag, torch.int32, "err_flag")
     _shape(action_mask, (T,), "action_mask")
-    _same_device(logpi, logmu, cu_seqlens, adv, coef_out, action_mask, ws, err_flag)
+    _same_device(logpi, logmu, cu_seqlens, adv, coef_out, loss_out, d3_out, action_mask, ws,
+                 err_flag)
     dev = cu_seqlens.device
     if loss_out is None:
         loss_out = torch.empty(1, dtype=torch.float32, device=dev)
@@ -220,7 +257,7 @@ def rz_is_loss(logpi, logmu, cu_seqlens, adv, loss_out=None, d3_out=None, coef_o
         _need(action_mask, torch.uint8, "action_mask")
     st = lib.rz_is_loss(_ptr(logpi), _ptr(logmu), _ptr(cu_seqlens), _ptr(adv),
                         _ptr(action_mask), B, T,
-                        _ptr(loss_out), _ptr(d3_out), _ptr(coef_out), _ptr(ws), ws.numel(),
+                        _ptr(loss_out), _ptr(d3_out), _ptr(coef_out), _ptr(ws), _ws_bytes(ws),
                         _ptr(err_flag), _stream(stream))
     _check("rz_is_loss", st)
     return loss_out, d3_out, coef_out
@@ -232,7 +269,8 @@ def rz_d3(logpi, logmu, d3_out=None, stream=None):
     _need(logpi, torch.float32, "logpi")
     _need(logmu, torch.float32, "logmu")
     _shape(logmu, tuple(logpi.shape), "logmu")
-    _same_device(logpi, logmu)
+    _out(d3_out, torch.float32, "d3_out")
+    _same_device(logpi, logmu, d3_out)
     if d3_out is None:
         d3_out = torch.empty(1, dtype=torch.float32, device=logpi.device)
     _check("rz_d3", lib.rz_d3(_ptr(logpi), _ptr(logmu), logpi.shape[0], _ptr(d3_out),
@@ -261,14 +299,14 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
     _shape(logmu, (T,), "logmu")
     _shape(adv, (B,), "adv")
     _shape(action_mask, (T,), "action_mask")
-    for t, n, dt, sh in ((logprob_out, "logprob_out", torch.float32, (T,)),
-                         (dH, "dH", torch.bfloat16, (T, d)),
-                         (dW, "dW", torch.float32, (V, d))):
-        if t is not None:
-            _need(t, dt, n)
-            _shape(t, sh, n)
-    _same_device(H, W, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out, dH, dW, ws,
-                 err_flag)
+    _out(logprob_out, torch.float32, "logprob_out", (T,))
+    _out(dH, torch.bfloat16, "dH", (T, d))
+    _out(dW, torch.float32, "dW", (V, d))
+    _out(loss_out, torch.float32, "loss_out")
+    _out(d3_out, torch.float32, "d3_out")
+    _out(err_flag, torch.int32, "err_flag")
+    _same_device(H, W, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out, dH, dW,
+                 loss_out, d3_out, ws, err_flag)
     dev = H.device
     if want_logprob and logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -286,7 +324,7 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
         _need(action_mask, torch.uint8, "action_mask")
     st = lib.rz_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(cu_seqlens),
                              _ptr(adv), _ptr(action_mask), B, T, d, V, _ptr(loss_out), _ptr(d3_out),
-                             _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                             _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), _ws_bytes(ws),
                              _ptr(err_flag), _stream(stream))
     _check("rz_loss_fwd_bwd", st)
     return {"loss": loss_out, "d3": d3_out, "logprob": logprob_out, "dH": dH, "dW": dW}
@@ -312,13 +350,13 @@ def rz_sc_loss_fwd_bwd(H, W, tokens, cu_seqlens, adv, logprob_out=None, dH=None,
     _shape(tokens, (T,), "tokens")
     _shape(adv, (B,), "adv")
     _shape(action_mask, (T,), "action_mask")
-    for t, n, dt, sh in ((logprob_out, "logprob_out", torch.float32, (T,)),
-                         (dH, "dH", torch.bfloat16, (T, d)),
-                         (dW, "dW", torch.float32, (V, d))):
-        if t is not None:
-            _need(t, dt, n)
-            _shape(t, sh, n)
-    _same_device(H, W, tokens, cu_seqlens, adv, action_mask, logprob_out, dH, dW, ws, err_flag)
+    _out(logprob_out, torch.float32, "logprob_out", (T,))
+    _out(dH, torch.bfloat16, "dH", (T, d))
+    _out(dW, torch.float32, "dW", (V, d))
+    _out(loss_out, torch.float32, "loss_out")
+    _out(err_flag, torch.int32, "err_flag")
+    _same_device(H, W, tokens, cu_seqlens, adv, action_mask, logprob_out, dH, dW, loss_out, ws,
+                 err_flag)
     dev = H.device
     if want_logprob and logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -334,7 +372,7 @@ def rz_sc_loss_fwd_bwd(H, W, tokens, cu_seqlens, adv, logprob_out=None, dH=None,
         _need(action_mask, torch.uint8, "action_mask")
     st = lib.rz_sc_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(cu_seqlens), _ptr(adv),
                                 _ptr(action_mask), B, T, d, V, _ptr(loss_out),
-                                _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(),
+                                _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), _ws_bytes(ws),
                                 _ptr(err_flag), _stream(stream))
     _check("rz_sc_loss_fwd_bwd", st)
     return {"loss": loss_out, "logprob": logprob_out, "dH": dH, "dW": dW}
@@ -357,9 +395,12 @@ def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob
     _shape(logmu, (T,), "logmu")
     _shape(adv, (B,), "adv")
     _shape(action_mask, (T,), "action_mask")
-    _shape(logprob_out, (T,), "logprob_out")
-    _same_device(logits_inout, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out, ws,
-                 err_flag)
+    _out(logprob_out, torch.float32, "logprob_out", (T,))
+    _out(loss_out, torch.float32, "loss_out")
+    _out(d3_out, torch.float32, "d3_out")
+    _out(err_flag, torch.int32, "err_flag")
+    _same_device(logits_inout, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out,
+                 loss_out, d3_out, ws, err_flag)
     dev = logits_inout.device
     if logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -374,7 +415,7 @@ def rz_logits_loss_fwd_bwd(logits_inout, tokens, logmu, cu_seqlens, adv, logprob
     st = lib.rz_logits_loss_fwd_bwd(_ptr(logits_inout), _ptr(tokens), _ptr(logmu),
                                     _ptr(cu_seqlens), _ptr(adv), _ptr(action_mask), B, T, V,
                                     _ptr(loss_out),
-                                    _ptr(d3_out), _ptr(logprob_out), _ptr(ws), ws.numel(),
+                                    _ptr(d3_out), _ptr(logprob_out), _ptr(ws), _ws_bytes(ws),
                                     _ptr(err_flag), _stream(stream))
     _check("rz_logits_loss_fwd_bwd", st)
     return {"loss": loss_out, "d3": d3_out, "logprob": logprob_out}
@@ -392,6 +433,7 @@ def rz_lmhead_logits(H, W, logits_out=None, err_flag=None, stream=None):
         logits_out = torch.empty((T, V), dtype=torch.float32, device=H.device)
     _need(logits_out, torch.float32, "logits_out")
     _shape(logits_out, (T, V), "logits_out")
+    _out(err_flag, torch.int32, "err_flag")
     _same_device(H, W, logits_out, err_flag)
     st = lib.rz_lmhead_logits(_ptr(H), _ptr(W), T, d, V, _ptr(logits_out), _ptr(err_flag),
                               _stream(stream))
@@ -417,7 +459,8 @@ def rz_token_logprob_noalloc(H, W, tokens, logprob_out, lse_out=None, err_flag=N
     _shape(W, (V, d), "W")
     _shape(tokens, (T,), "tokens")
     _shape(logprob_out, (T,), "logprob_out")
-    _shape(lse_out, (T,), "lse_out")
+    _out(lse_out, torch.float32, "lse_out", (T,))
+    _out(err_flag, torch.int32, "err_flag")
     _same_device(H, W, tokens, logprob_out, lse_out, err_flag)
     st = lib.rz_token_logprob_noalloc(_ptr(H), _ptr(W), _ptr(tokens), T, d, V,
                                       _ptr(logprob_out), _ptr(lse_out), _ptr(err_flag),
@@ -441,6 +484,7 @@ def rz_is_stats(logpi, logmu, stats_out=None, stream=None):
     _need(logpi, torch.float32, "logpi")
     _need(logmu, torch.float32, "logmu")
     _shape(logmu, tuple(logpi.shape), "logmu")
+    _out(stats_out, torch.float32, "stats_out", min_numel=len(IS_STATS_FIELDS))
     _same_device(logpi, logmu, stats_out)
     if stats_out is None:
         stats_out = torch.empty(7, dtype=torch.float32, device=logpi.device)
@@ -473,8 +517,10 @@ def rz_sample_logprob(H, W, seed, row_ids=None, tokens_out=None, logprob_out=Non
     V = W.shape[0]
     _shape(W, (V, d), "W")
     _shape(row_ids, (T,), "row_ids")
-    _shape(tokens_out, (T,), "tokens_out")
-    _shape(logprob_out, (T,), "logprob_out")
+    _out(tokens_out, torch.int32, "tokens_out", (T,))
+    _out(logprob_out, torch.float32, "logprob_out", (T,))
+    _out(lse_out, torch.float32, "lse_out", (T,))
+    _out(err_flag, torch.int32, "err_flag")
     _same_device(H, W, row_ids, tokens_out, logprob_out, lse_out, ws, err_flag)
     if tokens_out is None:
         tokens_out = torch.empty(T, dtype=torch.int32, device=H.device)
@@ -485,7 +531,7 @@ def rz_sample_logprob(H, W, seed, row_ids=None, tokens_out=None, logprob_out=Non
     st = lib.rz_sample_logprob(_ptr(H), _ptr(W), _ptr(row_ids), T, d, V,
                                ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
                                _ptr(tokens_out), _ptr(logprob_out), _ptr(lse_out), _ptr(ws),
-                               ws.numel(), _ptr(err_flag), _stream(stream))
+                               _ws_bytes(ws), _ptr(err_flag), _stream(stream))
     _check("rz_sample_logprob", st)
     return tokens_out, logprob_out
 
@@ -494,5 +540,7 @@ def rz_selftest_wait_timeout(err_flag, done_out=None, limit_us=50000, stream=Non
     """Run the bounded-wait self-test (see include/rz.h)."""
     torch = _torch()
     _need(err_flag, torch.int32, "err_flag")
+    _out(done_out, torch.int32, "done_out")
+    _same_device(err_flag, done_out)
     _check("rz_selftest_wait_timeout", load().rz_selftest_wait_timeout(
         _ptr(err_flag), _ptr(done_out), int(limit_us), _stream(stream)))
