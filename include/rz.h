@@ -32,7 +32,9 @@
  *     copy engine).
  *   - Sizes: 0 <= T < 2^31, 1 <= V <= 2^24, 8 <= d <= 65536, B >= 0.
  *   - Return value: RZ_OK or an RZ_ERR_* code; nothing is enqueued when an
- *     argument check fails.  rz_status_string() gives the text.
+ *     argument check fails.  RZ_ERR_CUDA (a launch or driver call failed)
+ *     can come after some of the call's launches were enqueued: the
+ *     outputs are then undefined.  rz_status_string() gives the text.
  *   - err_flag (nullable, device int32): device-side problems are OR-ed
  *     into it (RZ_DEVERR_*).  The caller zeroes it before the call and reads
  *     it afterwards.  No kernel ever traps.
