@@ -54,6 +54,12 @@ def workspace(nbytes, cls=CUDA0):
     return dev(buf[off:off + max(nbytes, 256)], cls)
 
 
+# Host tensors posing as device tensors must never reach a real GPU: with
+# one present the library would launch on them.
+pytestmark = pytest.mark.skipif(torch.cuda.is_available(),
+                                reason="fake device tensors are kept off machines with a GPU")
+
+
 @pytest.fixture(scope="module")
 def lib():
     from invariant_logprobs_gb300 import build
