@@ -42,7 +42,8 @@ def test_learner_full_size_sampled(rz, name):
     b = synth.make_batch(wl, device=DEV)
     T, d, V, B = b["T"], b["d"], b["V"], b["B"]
     logmu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
-    adv = rz.rz_group_advantage(b["rewards"], b["G"])
+    A32 = oracle.group_advantage(f64(b["rewards"]), b["G"]).astype(np.float32)
+    adv = torch.tensor(A32, device=DEV)
     err = rz.new_err_flag(DEV)
     out = rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv, err_flag=err)
     loss2, d32, _ = rz.rz_is_loss(out["logprob"], logmu, b["cu"], adv)
@@ -71,7 +72,7 @@ def test_learner_full_size_sampled(rz, name):
     seg = np.searchsorted(cu, rows, side="right") - 1
     Ti = cu[seg + 1] - cu[seg]
     n = rows.shape[0]
-    A_rows = f64(adv)[seg] * n / (B * Ti)
+    A_rows = A32.astype(np.float64)[seg] * n / (B * Ti)
     sub = oracle.loss_fwd_bwd(Hs, Wd, tok, f64(logmu[r_t]), np.arange(n + 1), A_rows)
     assert np.max(np.abs(sub["logpi"] - lp_ref)) <= 1e-12
     assert rel_l2(f64(out["dH"][r_t]), sub["dH"]) <= TOL_GRAD_REL_L2
@@ -102,7 +103,8 @@ def test_logits_variant_full_size_sampled(rz):
         logpi[s0:e] = zz.gather(1, b["tokens"][s0:e].long()[:, None])[:, 0]
         del zz
     logmu = synth.logmu_near(logpi, synth.LOGMU_NOISE_STD, b["gen"])
-    adv = rz.rz_group_advantage(b["rewards"], b["G"])
+    A32 = oracle.group_advantage(f64(b["rewards"]), b["G"]).astype(np.float32)
+    adv = torch.tensor(A32, device=DEV)
     err = rz.new_err_flag(DEV)
     out = rz.rz_logits_loss_fwd_bwd(b["logits"], b["tokens"], logmu, b["cu"], adv, err_flag=err)
     loss2, d32, _ = rz.rz_is_loss(out["logprob"], logmu, b["cu"], adv)
@@ -114,7 +116,7 @@ def test_logits_variant_full_size_sampled(rz):
     seg = np.searchsorted(cu, rows, side="right") - 1
     Ti = cu[seg + 1] - cu[seg]
     n = rows.shape[0]
-    A_rows = f64(adv)[seg] * n / (B * Ti)
+    A_rows = A32.astype(np.float64)[seg] * n / (B * Ti)
     ref = oracle.logits_loss_fwd_bwd(z_rows, f64(b["tokens"][r_t]), f64(logmu[r_t]),
                                      np.arange(n + 1), A_rows)
     assert np.max(np.abs(f64(out["logprob"][r_t]) - ref["logpi"])) <= TOL_LOGPI

@@ -43,16 +43,17 @@ def test_random_shape_learner_vs_oracle(rz, seed):
     Hd, Wd, tok = f64(c["H"]), f64(c["W"]), f64(c["tok"])
     logmu = oracle.token_logprob(Hd, f64(c["W_mu"]), tok)[0].astype(np.float32)
     A = oracle.group_advantage(f64(c["rewards"]), c["G"])
+    A32 = A.astype(np.float32)  # the learner's input: the oracle's advantages at fp32
     adv_gpu = rz.rz_group_advantage(c["rewards"].to(DEV), c["G"])
     mask_t = None if c["mask"] is None else torch.tensor(c["mask"]).to(DEV)
     out = rz.rz_loss_fwd_bwd(c["H"].to(DEV), c["W"].to(DEV), c["tok"].to(DEV),
-                             torch.tensor(logmu).to(DEV), torch.tensor(c["cu"]).to(DEV), adv_gpu,
-                             action_mask=mask_t)
+                             torch.tensor(logmu).to(DEV), torch.tensor(c["cu"]).to(DEV),
+                             torch.tensor(A32).to(DEV), action_mask=mask_t)
     lp_roll, _ = rz.rz_token_logprob(c["H"].to(DEV), c["W"].to(DEV), c["tok"].to(DEV))
     torch.cuda.synchronize()
     np.testing.assert_allclose(f64(adv_gpu), A, atol=1e-6)
-    ref = oracle.loss_fwd_bwd(Hd, Wd, tok, logmu.astype(np.float64), c["cu"], f64(adv_gpu),
-                              mask=c["mask"])
+    ref = oracle.loss_fwd_bwd(Hd, Wd, tok, logmu.astype(np.float64), c["cu"],
+                              A32.astype(np.float64), mask=c["mask"])
     assert np.max(np.abs(f64(out["logprob"]) - ref["logpi"])) <= TOL_LOGPI
     assert torch.equal(out["logprob"], lp_roll)
     assert scalar_close(out["loss"].item(), ref["loss"]), (out["loss"].item(), ref["loss"])

@@ -31,7 +31,11 @@ def _check_against_oracle(H, W, row_ids, seed, tok, lmu):
         keys, _ = rz_sampler.key_of(Hd[t], Wd, rid[t], seed, got[t])
         assert keys[got[t]] >= keys.max() - NEAR_TIE, (t, keys[got[t]], keys.max())
     assert same.mean() >= 0.99, same.mean()
-    lp_gpu_tok, _ = oracle.token_logprob(Hd, Wd, got)
+    # the oracle's log-softmax of each row (from H and W only), read at the
+    # token the GPU drew: the recorded log mu must be that token's log pi
+    z = oracle.lmhead_logits(Hd, Wd)
+    lp_rows = z - oracle.logsumexp_rows(z)[:, None]
+    lp_gpu_tok = lp_rows[np.arange(got.shape[0]), got]
     assert np.max(np.abs(f64(lmu) - lp_gpu_tok)) <= TOL_LOGPI
 
 
