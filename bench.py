@@ -164,33 +164,39 @@ def max_over_ranks(x, world):
 
 
 # ----------------------------------------------------------------- CPU oracle leg
-def oracle_sample(b, n_tokens, seed=7):
+def oracle_sample(b, n_tokens):
     """A bounded sample of the workload for the CPU oracle: the first responses
     whose total length reaches n_tokens (whole responses, so the per-response
-    means are the workload's own)."""
+    means are the workload's own; the last one is cut short if needed).  Its
+    recorded log mu and advantages are the oracle's own, from the batch's
+    W_mu and rewards (computed here, outside the timed call)."""
     import numpy as np
     import torch
+    import oracle
     cu = b["cu"].cpu().numpy()
     B = cu.shape[0] - 1
     k = 1
     while k < B and cu[k] < n_tokens:
         k += 1
-    T = int(cu[k])
-    if T > n_tokens:  # cut the last response short to bound the work
-        T = n_tokens
+    T = min(int(cu[k]), n_tokens)
     cu_s = np.minimum(cu[:k + 1], T)
     f = lambda t: t.to("cpu", torch.float64).numpy()
-    return {"H": f(b["H"][:T]), "W": f(b["W"]), "tokens": b["tokens"][:T].cpu().numpy(),
-            "logmu": b["logmu"][:T].cpu().double().numpy(), "cu": cu_s,
-            "adv": b["adv"][:k].cpu().double().numpy(), "T": T}
+    H = f(b["H"][:T])
+    tokens = b["tokens"][:T].cpu().numpy().astype(np.int64)
+    logmu, _ = oracle.token_logprob(H, f(b["W_mu"]), tokens)
+    adv = oracle.group_advantage(f(b["rewards"]), b["G"])[:k]
+    return {"H": H, "W": f(b["W"]), "tokens": tokens, "logmu": logmu, "cu": cu_s, "adv": adv,
+            "T": T}
 
 
-def logits_oracle_sample(logits, tokens, logmu, cu, adv, n_tokens):
+def logits_oracle_sample(logits, tokens, logmu, cu, rewards, G, n_tokens):
     """The given-logits counterpart of oracle_sample: the first n_tokens rows
     (whole responses where they fit, the last one cut short), bf16 logits
-    widened exactly to fp32 on the host."""
+    widened exactly to fp32 on the host; advantages are the oracle's own."""
     import numpy as np
     import torch
+    import oracle
+    adv = oracle.group_advantage(rewards.to("cpu", torch.float64).numpy(), G)
     cu = cu.cpu().numpy()
     B = cu.shape[0] - 1
     k = 1
@@ -199,7 +205,7 @@ def logits_oracle_sample(logits, tokens, logmu, cu, adv, n_tokens):
     T = min(int(cu[k]), n_tokens)
     return {"logits": logits[:T].to("cpu", torch.float32).numpy(),
             "tokens": tokens[:T].cpu().numpy(), "logmu": logmu[:T].cpu().double().numpy(),
-            "cu": np.minimum(cu[:k + 1], T), "adv": adv[:k].cpu().double().numpy(), "T": T}
+            "cu": np.minimum(cu[:k + 1], T), "adv": adv[:k], "T": T}
 
 
 def time_logits_oracle(sample, reps=1):
@@ -557,7 +563,8 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
         "device_err_flag": int(err.item()),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        s = logits_oracle_sample(b["logits"], b["tokens"], logmu, b["cu"], adv, args.cpu_tokens)
+        s = logits_oracle_sample(b["logits"], b["tokens"], logmu, b["cu"], b["rewards"], b["G"],
+                                 args.cpu_tokens)
         v, dt = time_logits_oracle(s)
         out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cpu_threads(),
                                "kind": "oracle",
@@ -570,6 +577,14 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
 
 
 # ----------------------------------------------------------------- reference arm
+def reference_tokens(args):
+    """Tokens per reference-arm step: --cpu-tokens for up to 10 steps, fewer
+    for longer runs, so that the whole run stays within a few minutes."""
+    if args.steps <= 10:
+        return args.cpu_tokens
+    return max(64, args.cpu_tokens * 10 // args.steps)
+
+
 def run_reference(args):
     """The CPU oracle as it stands, on the host cores, on a bounded sample of
     the same workload; rank 0 only."""
@@ -577,23 +592,17 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import torch
     from invariant_logprobs_gb300 import synth
-    import oracle
     if args.config == "moe30b_logits":
         return run_reference_logits(args, world)
     wl = synth.WORKLOADS[args.config]
     # draw the same distributions on the host (no GPU needed): a small batch
     # of whole responses at full d and V
     import dataclasses
-    n = args.cpu_tokens
+    n = reference_tokens(args)
     small = dataclasses.replace(wl, n_prompts=1, group=2, len_lo=n // 2, len_hi=n // 2)
     b = synth.make_batch(small, device="cpu")
-    f = lambda t: t.to(torch.float64).numpy()
-    lm, _ = oracle.token_logprob(f(b["H"]), f(b["W_mu"]), b["tokens"].numpy())
-    b["logmu"] = torch.tensor(lm)
-    b["adv"] = torch.tensor(oracle.group_advantage(f(b["rewards"]), b["G"]))
-    s = oracle_sample(b, args.cpu_tokens)
+    s = oracle_sample(b, n)
     for _ in range(max(0, min(args.warmup, 1))):
         time_oracle(s)
     times = []
@@ -628,7 +637,7 @@ def run_reference_logits(args, world):
     from invariant_logprobs_gb300 import synth
     import oracle
     wl = synth.WORKLOADS["moe30b_logits"]
-    n = max(wl.group, args.cpu_tokens)
+    n = max(wl.group, reference_tokens(args))
     small = dataclasses.replace(wl, len_lo=n // wl.group, len_hi=n // wl.group)
     b = synth.make_logits_batch(small, device="cpu", T=n // wl.group * wl.group)
     T = b["T"]
@@ -715,7 +724,8 @@ def main():
     ap.add_argument("--config", default="qwen4b_lag64",
                     choices=["qwen4b_lag64", "qwen1p5b_lag2", "moe30b_logits", "tiny"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--cpu-tokens", type=int, default=1024,
+                    help="tokens of the CPU oracle's timed sample (about 10 s at the 4B shape)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["learner", "logits", "sample", "rollout"], default=None,
                     help="small fixed case for ncu captures (no timing output)")
