@@ -13,8 +13,9 @@ same way, so dW = sum_r dW_r and each rank's dH is final.  D3 is a token
 mean: D3 = sum_r D3_r T_r / T.
 
 Only the sums cross ranks (dW, and two scalars), which is the one exchange
-step of the path; this module holds the bookkeeping, the exchange itself is
-the caller's (e.g. a fixed-order all-reduce).
+step of the path.  Its order is fixed: fixed_order_sum gathers every rank's
+partial and adds them in rank order, so dW is bitwise the same on every rank
+and from run to run, whatever order the backend's own all-reduce would use.
 """
 
 import numpy as np
@@ -59,3 +60,20 @@ def combine_scalars(loss_locals, d3_locals, T_locals):
         loss += l
         d3 += d * t
     return loss, (d3 / T if T > 0 else 0.0)
+
+
+def fixed_order_sum(t, group=None):
+    """Sum of tensor t over the ranks of `group`, added in rank order
+    0, 1, ..., N-1 on every rank: an all-gather of the partials, then a
+    serial sum.  The result is bitwise identical on every rank and from run
+    to run (a backend all-reduce may add in any order).  Holds N copies of t
+    while it runs."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(t) for _ in range(world)]
+    dist.all_gather(parts, t.contiguous(), group=group)
+    out = parts[0].clone()
+    for part in parts[1:]:
+        out += part
+    return out

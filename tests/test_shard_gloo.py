@@ -63,8 +63,7 @@ def _worker(rank, world, port, out_dir):
         dH = res["dH"]
     else:
         loss, d3, dW, dH = 0.0, 0.0, np.zeros_like(W), np.zeros((0, W.shape[1]))
-    dW_t = torch.tensor(dW)
-    dist.all_reduce(dW_t)
+    dW_t = shard.fixed_order_sum(torch.tensor(dW))
     scal = [None] * world
     dist.all_gather_object(scal, (loss, d3, t1 - t0))
     g_loss, g_d3 = shard.combine_scalars([s[0] for s in scal], [s[1] for s in scal],
@@ -87,3 +86,36 @@ def test_two_rank_gloo_shard_equals_unsharded(tmp_path, world):
     np.testing.assert_allclose(np.load(tmp_path / "dW.npy"), ref["dW"], atol=1e-13)
     dH = np.concatenate([np.load(tmp_path / ("dH_%d.npy" % r)) for r in range(world)])
     np.testing.assert_allclose(dH, ref["dH"], atol=1e-13)
+
+
+def _partial(rank, n=4096):
+    """A rank's fp32 partial whose sum depends on the order of addition
+    (magnitudes from 1e-4 to 1e4)."""
+    g = torch.Generator().manual_seed(100 + rank)
+    return torch.randn(n, generator=g) * torch.pow(10.0, torch.randint(-4, 5, (n,), generator=g))
+
+
+def _sum_worker(rank, world, port, out_dir):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    out = shard.fixed_order_sum(_partial(rank))
+    np.save(os.path.join(out_dir, "sum_%d.npy" % rank), out.numpy())
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_fixed_order_sum_is_the_rank_order_sum_on_every_rank(tmp_path, world):
+    mp.spawn(_sum_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    want = _partial(0).clone()
+    for r in range(1, world):
+        want += _partial(r)
+    # a different order gives different bits, so the check can fail
+    rev = _partial(world - 1).clone()
+    for r in range(world - 2, -1, -1):
+        rev += _partial(r)
+    if world > 2:
+        assert not torch.equal(rev, want)
+    for r in range(world):
+        got = torch.from_numpy(np.load(tmp_path / ("sum_%d.npy" % r)))
+        assert torch.equal(got.view(torch.int32), want.view(torch.int32)), r
