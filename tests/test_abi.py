@@ -67,6 +67,15 @@ def test_workspace_sizes(lib):
     assert 384 * (1024 * 2 + 32 * 4) < small < 384 * (1024 * 2 + 32 * 4) + (1 << 20)
     assert rz.workspace_size(rz.RZ_OP_IS_LOSS, 10, 0, 0, 256) >= 256 * 24
     assert rz.workspace_size(99, 10, 10, 10, 10) == 0
+    # a vocabulary so large that 38,912 rows of kept terms would pass 40 GiB:
+    # the chunk shrinks to the largest multiple of 128 rows that fits
+    V = 1 << 20
+    per_row = V * 2 + (V // 128) * 4 * 4
+    rows = (40 << 30) // per_row // 128 * 128
+    assert rows == 19200
+    huge = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, 10**6, 64, V, 8)
+    assert rows * per_row <= huge < rows * per_row + rows * (64 * 8 + 16) + 10**6 * 4 + 10**6
+    assert huge <= (40 << 30) + (64 << 20)
 
 
 def _no_gpu():
