@@ -210,3 +210,26 @@ def test_more_host_side_argument_checks(lib):
     # diagnostics: negative T
     assert lib.rz_is_stats(fake, fake, -1, fake, null) == 1
     assert lib.rz_d3(null, null, 5, fake, null) == 1
+
+
+def test_vocab_splits_depend_on_v_only(lib):
+    """The logprob pass keeps T x S split states (8 bytes each) plus one
+    gathered logit per row; S groups consecutive 256-column vocab tiles,
+    at most 64 groups, and is a function of V alone (never of T), which is
+    what fixes each row's reduction order whatever batch it is in."""
+    import invariant_logprobs_gb300 as rz
+
+    def splits(V, T=32):
+        ws = rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, T, 64, V, 0)
+        return (ws - 256) // (T * 8)  # T * 4 bytes of gathered logits -> one 256-byte block
+
+    def rule(V):
+        tiles = -(-V // 256)
+        per = -(-tiles // min(tiles, 64))
+        return -(-tiles // per)
+
+    for V, want in [(1, 1), (256, 1), (257, 2), (16384, 64), (16385, 33), (151936, 60),
+                    (1 << 24, 64)]:
+        assert splits(V) == want == rule(V), V
+    for T in (32, 64, 320):
+        assert splits(151936, T) == 60
