@@ -8,7 +8,9 @@ mistake which a fixed example happens to hide still fails somewhere.
     D3 >= 0; a masked token equals the token removed;
   * <dW, W> = <dH, H> (both are sum_t sum_v dz_tv z_tv); each column of dW
     sums to 0 over the vocabulary (each dz row does); one coordinate of dW
-    and of dH against a central difference of the loss.
+    and of dH against a central difference of the loss;
+  * Score Centering: unchanged by a constant added to every advantage, and
+    one coordinate of dW against a central difference of L_SC.
 """
 
 import numpy as np
@@ -133,3 +135,28 @@ def test_gradient_identities_and_central_differences(p):
         Hm[t, k] -= h
         fd = (loss_at(Hp, W) - loss_at(Hm, W)) / (2 * h)
         assert fd == pytest.approx(dH[t, k], rel=1e-5, abs=1e-9)
+
+
+@SETTINGS
+@given(problems())
+def test_score_centering_gradient_and_shift_invariance(p):
+    H, W, tok, cu, A, mask = p["H"], p["W"], p["tok"], p["cu"], p["A"], p["mask"]
+    r = oracle.sc_loss_fwd_bwd(H, W, tok, cu, A, mask=mask)
+    # a constant added to every advantage changes neither loss nor gradient
+    r2 = oracle.sc_loss_fwd_bwd(H, W, tok, cu, A + 0.75, mask=mask)
+    assert r2["loss"] == pytest.approx(r["loss"], rel=1e-9, abs=1e-12)
+    assert np.allclose(r2["dW"], r["dW"], atol=1e-12)
+    assert np.allclose(r2["dH"], r["dH"], atol=1e-12)
+
+    def loss_at(W2):
+        lp = oracle.token_logprob(H, W2, tok)[0]
+        return oracle.sc_loss(lp, cu, A, mask)["loss"]
+
+    rng = p["rng"]
+    h = 1e-6
+    v, k = int(rng.integers(0, p["V"])), int(rng.integers(0, p["d"]))
+    Wp, Wm = W.copy(), W.copy()
+    Wp[v, k] += h
+    Wm[v, k] -= h
+    fd = (loss_at(Wp) - loss_at(Wm)) / (2 * h)
+    assert fd == pytest.approx(r["dW"][v, k], rel=1e-5, abs=1e-9)
