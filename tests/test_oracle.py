@@ -132,9 +132,11 @@ def test_logprob_shift_invariance_and_large_logits():
     tok = rng.integers(0, 9, 6)
     lp, _ = oracle.token_logprob(H, W, tok)
     # append a hidden unit equal to 1 whose weight is the same for every
-    # vocab row: adds a per-row constant (here 500) to all logits.
+    # vocab row: adds a per-row constant (here 1000, past the largest
+    # argument of a finite fp64 exp, ~709) to all logits, so only a
+    # log-sum-exp taken relative to the row maximum stays finite.
     H2 = np.concatenate([H, np.ones((6, 1))], 1)
-    W2 = np.concatenate([W, np.full((9, 1), 500.0)], 1)
+    W2 = np.concatenate([W, np.full((9, 1), 1000.0)], 1)
     lp2, lse2 = oracle.token_logprob(H2, W2, tok)
     np.testing.assert_allclose(lp2, lp, atol=1e-10)
     assert np.all(np.isfinite(lse2))
