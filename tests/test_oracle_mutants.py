@@ -1,7 +1,8 @@
 """Mutation check of the oracle's pins, planted on the CPU: each mutant is
 the oracle's source with one plausible mistake (a sign, a wrong count, a
 wrong mean, a clipped weight, a missing term, ...), loaded as a module of its
-own and put in place of `oracle` while the fixed pins of test_oracle.py run.
+own and put in place of `oracle` while the fixed pins of test_oracle.py run
+(sampler mutants: in place of the sampler oracle, against its own pins).
 Every mutant must fail at least one pin; the unmutated source must fail
 none (so the harness itself is sound).  The oracle package is never
 modified."""
@@ -14,9 +15,12 @@ import pytest
 
 import oracle
 import oracle.rz_oracle
+import oracle.rz_sampler
 import test_oracle as pins
+import test_oracle_sampler as sampler_pins
 
 SRC = open(oracle.rz_oracle.__file__).read()
+SAMPLER_SRC = open(oracle.rz_sampler.__file__).read()
 
 # name -> [(fragment of the oracle's source, replacement)]; every fragment
 # must occur in the source (all occurrences are replaced).
@@ -49,6 +53,15 @@ MUTANTS = {
                                     "abar = A.mean() if B > 0 else 0.0")],
     "SC without centring": [("abar = A[nonempty].mean() if nonempty.any() else 0.0",
                              "abar = 0.0")],
+}
+
+
+# mistakes in the sampler oracle, against the sampler's pins
+SAMPLER_MUTANTS = {
+    "Gumbel noise with the wrong sign": [("- np.log(-np.log(u))", "+ np.log(-np.log(u))")],
+    "U on the closed interval": [("+ 0.5) * 2.0 ** -23", "+ 0.0) * 2.0 ** -23")],
+    "Philox with 7 rounds": [("    for _ in range(10):", "    for _ in range(7):")],
+    "recorded log mu of the wrong token": [("lmu[t] = z[a] - lse", "lmu[t] = z[int(np.argmin(k))] - lse")],
 }
 
 
@@ -94,3 +107,45 @@ def test_unmutated_source_passes_every_pin(monkeypatch):
 def test_every_mutant_fails_a_pin(name, monkeypatch):
     failed = _failing_pins(_module(MUTANTS[name]), monkeypatch)
     assert failed, "no pin catches the mutant %r" % name
+
+
+def _sampler_module(pairs):
+    src = SAMPLER_SRC
+    for old, new in pairs:
+        assert old in src, "mutation target not in the sampler source: %r" % old
+        src = src.replace(old, new)
+    mod = types.ModuleType("sampler_mutant")
+    exec(compile(src, "<sampler mutant>", "exec"), mod.__dict__)
+    return mod
+
+
+def _failing_sampler_pins(mod, monkeypatch, first_only=False):
+    """Sampler pins that fail with `mod` in place of the sampler oracle; the
+    cheap ones (known answers, the U grid) run before the sampling ones, and
+    first_only stops at the first failure."""
+    monkeypatch.setattr(sampler_pins, "rz_sampler", mod)
+    fns = [(n, f) for n, f in inspect.getmembers(sampler_pins, inspect.isfunction)
+           if n.startswith("test_") and not inspect.signature(f).parameters]
+    fns.sort(key=lambda nf: ("gumbel" in nf[0], nf[0]))
+    failed = []
+    with np.errstate(all="ignore"):
+        for name, fn in fns:
+            try:
+                fn()
+            except Exception:
+                failed.append(name)
+                if first_only:
+                    break
+    monkeypatch.undo()
+    return failed
+
+
+def test_unmutated_sampler_passes_every_pin(monkeypatch):
+    assert _failing_sampler_pins(_sampler_module([]), monkeypatch) == []
+
+
+@pytest.mark.parametrize("name", sorted(SAMPLER_MUTANTS))
+def test_every_sampler_mutant_fails_a_pin(name, monkeypatch):
+    failed = _failing_sampler_pins(_sampler_module(SAMPLER_MUTANTS[name]), monkeypatch,
+                                   first_only=True)
+    assert failed, "no sampler pin catches the mutant %r" % name

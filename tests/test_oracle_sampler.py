@@ -49,6 +49,19 @@ def test_gumbel_max_two_tokens_matches_softmax():
     np.testing.assert_allclose(lmu[tok == 0], math.log(0.25), atol=1e-14)
 
 
+def test_gumbel_max_three_tokens_matches_softmax():
+    # z = (0, log 2, log 5): softmax = (1/8, 2/8, 5/8).  Unlike two tokens or
+    # uniform logits, three unequal logits tell z + G from z - G apart
+    # (z - G gives about (0.084, 0.245, 0.671)).
+    n = 8000
+    H = np.ones((n, 1))
+    W = np.array([[0.0], [math.log(2.0)], [math.log(5.0)]])
+    tok, _, _ = rz_sampler.sample_rows(H, W, np.arange(n) * 5 + 11, seed=23)
+    counts = np.bincount(tok, minlength=3)
+    p = scipy.stats.chisquare(counts, n * np.array([1.0, 2.0, 5.0]) / 8.0).pvalue
+    assert p > 1e-4, counts
+
+
 def test_gumbel_max_uniform_logits_chi_square():
     V, n = 16, 16000
     H = np.ones((n, 1))
