@@ -53,6 +53,18 @@ MUTANTS = {
                                     "abar = A.mean() if B > 0 else 0.0")],
     "SC without centring": [("abar = A[nonempty].mean() if nonempty.any() else 0.0",
                              "abar = 0.0")],
+    "one-hot sign in the given-logits dz": [("p[np.arange(rr.shape[0]), tokens[rr]] -= 1.0",
+                                             "p[np.arange(rr.shape[0]), tokens[rr]] += 1.0")],
+    "dH sign": [("dH[s:e] = dz @ Wd", "dH[s:e] = -(dz @ Wd)")],
+    "k1 sign": [('"k1": float(np.mean(-d))', '"k1": float(np.mean(d))')],
+    "k2 without the 1/2": [("np.mean(d * d / 2.0)", "np.mean(d * d)")],
+    "mean in place of median": [("np.max(x) / np.median(x)", "np.max(x) / np.mean(x)")],
+    "SC counts ignore the mask": [("counts = np.array([int(valid[cu[i]:cu[i + 1]].sum())",
+                                   "counts = np.array([int(cu[i + 1] - cu[i])")],
+    "strided instead of contiguous groups": [("g = r.reshape(B // G, G)",
+                                              "g = r.reshape(G, B // G).T")],
+    "w without the exponential": [("    w = np.exp(lp - lm)\n    c = np.zeros",
+                                   "    w = 1.0 + (lp - lm)\n    c = np.zeros")],
 }
 
 
