@@ -94,8 +94,12 @@ def test_host_side_argument_checks(lib):
     # B % G != 0
     assert lib.rz_group_advantage(fake, 10, 4, fake, null) == 1
     assert lib.rz_group_advantage(fake, 8, 0, fake, null) == 1
+    # Checks that answer 2 (alignment, d % 8) come before the workspace
+    # check, so these calls pass no workspace: a missing check would answer 3
+    # here instead of 2 (without a GPU, a call that passes every check
+    # also answers 2).
     # d not a multiple of 8
-    assert lib.rz_token_logprob(fake, fake, fake, 5, 12, 100, fake, null, fake, 1 << 20,
+    assert lib.rz_token_logprob(fake, fake, fake, 5, 12, 100, fake, null, null, 0,
                                 null, null) == 2
     # missing pointers
     assert lib.rz_token_logprob(null, fake, fake, 5, 16, 100, fake, null, fake, 1 << 20,
@@ -104,8 +108,8 @@ def test_host_side_argument_checks(lib):
     assert lib.rz_token_logprob(fake, fake, fake, 5, 16, 0, fake, null, fake, 1 << 20,
                                 null, null) == 1
     # misaligned H
-    assert lib.rz_token_logprob(P((1 << 20) + 2), fake, fake, 5, 16, 100, fake, null, fake,
-                                1 << 20, null, null) == 2
+    assert lib.rz_token_logprob(P((1 << 20) + 2), fake, fake, 5, 16, 100, fake, null, null,
+                                0, null, null) == 2
     # workspace too small / missing
     assert lib.rz_token_logprob(fake, fake, fake, 5, 16, 100, fake, null, fake, 8,
                                 null, null) == 3
@@ -116,7 +120,7 @@ def test_host_side_argument_checks(lib):
                                fake, null, fake, fake, fake, 1 << 30, null, null) == 1
     # logits variant needs V % 8 == 0
     assert lib.rz_logits_loss_fwd_bwd(fake, fake, fake, fake, fake, null, 2, 10, 100, fake, fake,
-                                      fake, fake, 1 << 20, null, null) == 2
+                                      fake, null, 0, null, null) == 2
     # is_loss: missing outputs
     assert lib.rz_is_loss(fake, fake, fake, fake, null, 2, 10, null, fake, null, fake, 1 << 20,
                           null, null) == 1
@@ -177,10 +181,11 @@ def test_more_host_side_argument_checks(lib):
               fake, big, null, null) == 1
     assert sc(fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, fake, null,
               fake, big, null, null) == 1
+    # (the 2-answers pass no workspace, as above)
     assert sc(fake, fake, fake, fake, fake, null, 2, 5, 12, 100, fake, null, fake, fake,
-              fake, big, null, null) == 2
+              null, 0, null, null) == 2
     assert sc(fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, fake, odd,
-              fake, big, null, null) == 2
+              null, 0, null, null) == 2
     assert sc(fake, fake, fake, fake, fake, null, 2, 5, 16, 100, fake, null, fake, fake,
               fake, 64, null, null) == 3
     # IS learner: D3 output and log mu are required
@@ -192,7 +197,7 @@ def test_more_host_side_argument_checks(lib):
     # fused sampler: missing tokens_out, d % 8, missing workspace; T = 0 is a no-op
     smp = lib.rz_sample_logprob
     assert smp(fake, fake, null, 5, 16, 100, 1, null, fake, null, fake, big, null, null) == 1
-    assert smp(fake, fake, null, 5, 20, 100, 1, fake, fake, null, fake, big, null, null) == 2
+    assert smp(fake, fake, null, 5, 20, 100, 1, fake, fake, null, null, 0, null, null) == 2
     assert smp(fake, fake, null, 5, 16, 100, 1, fake, fake, null, null, big, null, null) == 3
     assert smp(null, null, null, 0, 16, 100, 1, null, null, null, null, 0, null, null) == 0
     # logits: missing output, misaligned W
