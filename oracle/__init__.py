@@ -23,7 +23,6 @@ from .rz_oracle import (  # noqa: F401
     sc_loss,
     sc_loss_fwd_bwd,
     logits_loss_fwd_bwd,
-    segment_ids,
     is_stats,
     peak_to_median,
 )

@@ -89,14 +89,6 @@ def token_logprob(H, W, tokens):
     return token_logprob_rows(H, W, tokens, np.arange(T))
 
 
-def segment_ids(cu_seqlens, T):
-    """Response index of every packed token (cu_seqlens is [B+1], monotone,
-    cu[0] = 0, cu[B] = T; response i owns tokens cu[i] .. cu[i+1]-1)."""
-    cu = np.asarray(cu_seqlens, dtype=np.int64)
-    lengths = np.diff(cu)
-    return np.repeat(np.arange(lengths.shape[0]), lengths)[:T]
-
-
 def group_advantage(rewards, G):
     """A_i = r_i - (1/G) sum_{j in group(i)} r_j, groups = contiguous blocks
     of G responses [vLLM-zh s.4 item 3: reward minus the group's mean reward;

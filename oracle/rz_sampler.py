@@ -91,7 +91,9 @@ def sample_rows(H, W, row_ids, seed):
     return tok, lmu, margin
 
 
-def key_of(H_row, W, row_id, seed, v):
-    """Gumbel key of token v for one row (fp64), for validating a sample."""
+def key_of(H_row, W, row_id, seed):
+    """Every token's Gumbel key z_v + G_v for one row (fp64) and the row's
+    logits z, for checking that a token drawn elsewhere holds the best key
+    (or one within a near-tie of it)."""
     z = np.asarray(W, np.float64) @ np.asarray(H_row, np.float64)
     return gumbel_keys(z, row_id, seed), z

@@ -74,6 +74,12 @@ SAMPLER_MUTANTS = {
     "U on the closed interval": [("+ 0.5) * 2.0 ** -23", "+ 0.0) * 2.0 ** -23")],
     "Philox with 7 rounds": [("    for _ in range(10):", "    for _ in range(7):")],
     "recorded log mu of the wrong token": [("lmu[t] = z[a] - lse", "lmu[t] = z[int(np.argmin(k))] - lse")],
+    "key_of draws the next row's noise": [("return gumbel_keys(z, row_id, seed), z",
+                                           "return gumbel_keys(z, row_id + 1, seed), z")],
+    "key_of ignores the seed's high half": [("return gumbel_keys(z, row_id, seed), z",
+                                             "return gumbel_keys(z, row_id, seed & 0xFFFFFFFF), z")],
+    "key_of with the transposed weight": [("z = np.asarray(W, np.float64) @ np.asarray(H_row, np.float64)\n    return gumbel_keys",
+                                           "z = np.asarray(W, np.float64).sum(axis=1) * np.asarray(H_row, np.float64).sum()\n    return gumbel_keys")],
 }
 
 

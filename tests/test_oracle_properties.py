@@ -98,7 +98,7 @@ def test_masked_token_equals_removed_token(p):
     keep = p["mask"] != 0
     lp = oracle.token_logprob(p["H"], p["W"], p["tok"])[0]
     full = oracle.is_loss(lp, p["logmu"], p["cu"], p["A"], p["mask"])
-    seg = oracle.segment_ids(p["cu"], p["T"])
+    seg = np.repeat(np.arange(p["B"]), np.diff(p["cu"]))  # response of each token
     counts = np.bincount(seg[keep], minlength=p["B"])
     cu_k = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     removed = oracle.is_loss(lp[keep], p["logmu"][keep], cu_k, p["A"])

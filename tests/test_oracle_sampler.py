@@ -85,3 +85,40 @@ def test_recorded_logmu_is_the_logprob_of_the_sampled_token():
     perm = rng.permutation(40)
     tok2, _, _ = rz_sampler.sample_rows(H[perm], W, rid[perm], seed=2**40 + 17)
     np.testing.assert_array_equal(tok2, tok[perm])
+
+
+def test_key_of_at_the_zero_counter_uses_the_published_words():
+    # row id 0 and seed 0 put tokens 0..3 at Philox counter (0, 0, 0, 0) under
+    # key (0, 0): the first known-answer vector.  Their keys minus the logits
+    # are the Gumbel draws -log(-log U) of those four published words.
+    ctr, key, want = _kat()[0]
+    assert ctr == [0, 0, 0, 0] and key == [0, 0]
+    h = np.array([1.0, -2.0])
+    W = np.array([[0.5, 0.0], [0.0, 1.0], [3.0, 1.0], [-1.0, -1.0], [2.0, 2.0]])
+    keys, z = rz_sampler.key_of(h, W, 0, 0)
+    np.testing.assert_array_equal(z, W @ h)
+    u = np.array([((x >> 9) + 0.5) * 2.0 ** -23 for x in want])
+    np.testing.assert_allclose(keys[:4] - z[:4], -np.log(-np.log(u)), rtol=0, atol=1e-12)
+
+
+def test_key_of_agrees_with_the_sampled_rows():
+    # row ids and a seed with both 32-bit halves non-zero: the token each row
+    # draws holds the largest key that key_of gives for that row, and the
+    # recorded margin is that key's lead over the runner-up
+    rng = np.random.default_rng(11)
+    H = rng.standard_normal((24, 5))
+    W = rng.standard_normal((37, 5))
+    rid = rng.integers(2**33, 2**62, 24)
+    seed = (0x89ABCDEF << 32) | 0x01234567
+    tok, _, margin = rz_sampler.sample_rows(H, W, rid, seed)
+    for t in range(24):
+        keys, z = rz_sampler.key_of(H[t], W, int(rid[t]), seed)
+        np.testing.assert_allclose(z, oracle.lmhead_logits(H[t:t + 1], W)[0], atol=1e-12)
+        assert int(np.argmax(keys)) == tok[t]
+        srt = np.sort(keys)
+        assert srt[-1] - srt[-2] == pytest.approx(margin[t], abs=1e-12)
+    # another row id or seed draws other noise
+    k0, _ = rz_sampler.key_of(H[0], W, int(rid[0]), seed)
+    k1, _ = rz_sampler.key_of(H[0], W, int(rid[0]) + 1, seed)
+    k2, _ = rz_sampler.key_of(H[0], W, int(rid[0]), seed ^ (1 << 40))
+    assert not np.allclose(k0, k1) and not np.allclose(k0, k2)
