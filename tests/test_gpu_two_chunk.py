@@ -1,0 +1,143 @@
+"""Learner parity past one backward chunk, at the full vocabulary.
+
+The learner runs its backward pass in chunks of rows (38,912 at
+V = 151936; fewer at very large vocabularies, where the chunk's kept terms
+would pass 40 GiB), while the rollout's logprob GEMM runs in launch blocks
+of 38,912 rows whatever V is.  These tests cross those boundaries:
+
+  * V = 151936, d = 1536, ~43,000 rows (two chunks, the second ragged): log pi,
+    the loss, D3, and dH and dW element by element against the fp64 oracle,
+    as whole tensors (relative L2) and row by row (every dH row, every dW
+    vocabulary row);
+  * V = 151936, more than two chunks of rows: the learner's log pi equals
+    the rollout's bit for bit at the same weights, so w == 1 and D3 == 0.0
+    exactly ("diff 0", the Zero Mismatch post s.5);
+  * a vocabulary large enough that the learner's chunk is capped below the
+    rollout's launch block, so their boundaries fall on different rows: the
+    same bitwise equality.
+
+log mu for the parity case comes from torch's bf16 matmul + log_softmax
+under the lagged weights (the behaviour policy of the workload), never from
+this library; the advantages are the oracle's, rounded to fp32.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_logprobs_gb300 import synth
+from helpers import (TOL_GRAD_REL_L2, TOL_LOGPI, bits, f64, rel_l2, scalar_close)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+CHUNK_ROWS = 38912          # learner chunk and rollout launch block at V = 151936
+ROW_REL_L2 = 2e-2           # per dH row and per dW vocabulary row (see row_errors)
+
+
+def _behaviour_logprob(H, W_mu, tokens, chunk=4096):
+    out = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
+    for s in range(0, H.shape[0], chunk):
+        e = min(H.shape[0], s + chunk)
+        z = torch.log_softmax((H[s:e] @ W_mu.t()).float(), dim=-1)
+        out[s:e] = z.gather(1, tokens[s:e].long()[:, None])[:, 0]
+    return out
+
+
+def row_errors(got, want):
+    """Relative L2 error of every row, with a floor of 1e-3 of the root mean
+    square row norm (a row whose reference is ~0 is judged on absolute
+    error).  bf16 outputs and a bf16 dz give ~2-4e-3 per row; 2e-2 leaves
+    room for the worst of ~150,000 rows."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    num = np.linalg.norm(got - want, axis=1)
+    den = np.linalg.norm(want, axis=1)
+    floor = 1e-3 * np.sqrt(np.mean(den ** 2))
+    return num / np.maximum(den, floor)
+
+
+def test_two_chunk_full_vocab_gradients_vs_oracle(rz):
+    wl = synth.scaled(synth.WORKLOADS["qwen1p5b_lag2"], n_prompts=2, len_lo=2600,
+                      len_hi=2800, seed=2203)
+    b = synth.make_batch(wl, device=DEV)
+    T, d, V, B = b["T"], b["d"], b["V"], b["B"]
+    assert (d, V) == (1536, 151936)
+    assert CHUNK_ROWS < T < 2 * CHUNK_ROWS and (T - CHUNK_ROWS) % 128 != 0
+    logmu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
+    A32 = oracle.group_advantage(f64(b["rewards"]), b["G"]).astype(np.float32)
+    err = rz.new_err_flag(DEV)
+    out = rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"],
+                             torch.tensor(A32, device=DEV), err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = {k: f64(out[k]) for k in ("logprob", "dH", "dW")}
+    loss, d3 = out["loss"].item(), out["d3"].item()
+    del out
+    torch.cuda.empty_cache()
+
+    ref = oracle.loss_fwd_bwd(f64(b["H"]), f64(b["W"]), f64(b["tokens"]), f64(logmu),
+                              f64(b["cu"]), A32.astype(np.float64))
+    assert np.max(np.abs(got["logprob"] - ref["logpi"])) <= TOL_LOGPI
+    assert scalar_close(loss, ref["loss"]), (loss, ref["loss"])
+    assert scalar_close(d3, ref["d3"]), (d3, ref["d3"])
+    e_dH, e_dW = rel_l2(got["dH"], ref["dH"]), rel_l2(got["dW"], ref["dW"])
+    assert e_dH <= TOL_GRAD_REL_L2 and e_dW <= TOL_GRAD_REL_L2, (e_dH, e_dW)
+    # row by row: a mis-addressed tile in either chunk, or in the ragged tail
+    # of the second, shows up in its own rows even where the totals pass
+    r_dH = row_errors(got["dH"], ref["dH"])
+    r_dW = row_errors(got["dW"], ref["dW"])
+    assert r_dH.max() <= ROW_REL_L2, (int(r_dH.argmax()), r_dH.max(), np.median(r_dH))
+    assert r_dW.max() <= ROW_REL_L2, (int(r_dW.argmax()), r_dW.max(), np.median(r_dW))
+    # both chunks are held to the same bar
+    assert r_dH[:CHUNK_ROWS].max() <= ROW_REL_L2 and r_dH[CHUNK_ROWS:].max() <= ROW_REL_L2
+    print("two-chunk T=%d: |dlogpi| max %.2e; loss rel %.2e; d3 rel %.2e; dH rel L2 %.2e "
+          "(rows: median %.2e, max %.2e); dW rel L2 %.2e (vocab rows: median %.2e, max %.2e)"
+          % (T, np.max(np.abs(got["logprob"] - ref["logpi"])),
+             abs(loss - ref["loss"]) / abs(ref["loss"]), abs(d3 - ref["d3"]) / abs(ref["d3"]),
+             e_dH, np.median(r_dH), r_dH.max(), e_dW, np.median(r_dW), r_dW.max()))
+
+
+def _zero_mismatch(rz, T, d, V, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    H = (torch.randn(T, d, generator=g, device=DEV)).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    tokens = torch.randint(0, V, (T,), generator=g, device=DEV, dtype=torch.int32)
+    n_resp = 24
+    cuts = torch.sort(torch.randperm(T - 1, generator=g, device=DEV)[:n_resp - 1] + 1).values
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64, device=DEV), cuts.to(torch.int64),
+                    torch.full((1,), T, dtype=torch.int64, device=DEV)])
+    adv = rz.rz_group_advantage(torch.rand(n_resp, generator=g, device=DEV), 8)
+    err = rz.new_err_flag(DEV)
+    # the rollout records log mu with the same weights the learner holds
+    logmu, _ = rz.rz_token_logprob(H, W, tokens, err_flag=err)
+    ws_bytes = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, n_resp)
+    out = rz.rz_loss_fwd_bwd(H, W, tokens, logmu, cu, adv, err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(bits(out["logprob"]), bits(logmu))
+    assert out["d3"].item() == 0.0
+    # w == 1 exactly: the loss is -(1/B) sum_i A_i, the same as rz_is_loss
+    # gives for log pi == log mu
+    loss2, d32, _ = rz.rz_is_loss(logmu, logmu, cu, adv)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(loss2), bits(out["loss"])) and d32.item() == 0.0
+    return ws_bytes
+
+
+def test_zero_mismatch_past_two_chunks_full_vocab(rz):
+    T = 2 * CHUNK_ROWS + 3001
+    _zero_mismatch(rz, T, 1536, 151936, 41)
+
+
+def test_zero_mismatch_when_the_learner_chunk_is_capped(rz):
+    # At V = 600,000 a 38,912-row chunk would keep 2.125 B x 38,912 x V > 40 GiB
+    # of terms, so the learner's chunk shrinks (to 33,664 rows) while the
+    # rollout still launches blocks of 38,912 rows.
+    V, d = 600000, 128
+    per_row = (V + 7) // 8 * 8 * 2 + (V + 127) // 128 * 4 * 4
+    chunk = (40 << 30) // per_row // 128 * 128
+    assert chunk < CHUNK_ROWS
+    T = 2 * chunk + 5000
+    ws_bytes = _zero_mismatch(rz, T, d, V, 43)
+    assert ws_bytes >= chunk * per_row  # the workspace holds one capped chunk
