@@ -27,22 +27,20 @@ if ROOT not in sys.path:
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one logprob-GEMM launch of the 4B-shaped
-# workload (one 38,912-row block of the 1,083,112 rows; median of the 27 full
-# blocks of one call), from the 1-pass ncu capture summarised in
-# profiles/logprob_gemm_dram_traffic_fullsize.md.  Valid only while the GEMM
-# sources hash to the value recorded with it; otherwise reported as null.
-TRAFFIC_CAPTURE = {"workload": "qwen4b_lag64", "bytes": 4.3941e9 + 0.0495e9,
-                   "rows_per_launch": 38912, "sources_sha256_16": "2b3585dd752b3c93"}
+# DRAM bytes (read + write) per launch of the roofline kernel of each bench
+# workload, from an ncu capture of that kernel (the committed ncu summary
+# gives the command).  A figure is reported only while the kernel's sources
+# hash to the value recorded with it; otherwise the line carries null.
 GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_math.cuh",
                 "rz_internal.h"]
-
-# DRAM bytes (read + write) of one launch of the given-logits kernel over the
-# 262,144-row MoE-shaped workload (1-pass ncu capture summarised in
-# profiles/logits_row_kernel_moe30b_8192rows.md), tied to its sources' hash.
-LOGITS_TRAFFIC_CAPTURE = {"workload": "moe30b_logits", "bytes": 106.960e9 + 79.575e9,
-                          "sources_sha256_16": "d67650bec883fd47"}
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
+TRAFFIC_CAPTURES = {
+    # learner logits+LSE keep GEMM, one 38,912-row chunk at the 4B shape
+    "qwen4b_lag64": {"bytes": None, "sources": GEMM_SOURCES, "sources_sha256_16": None},
+    # given-logits row kernel over the 262,144-row MoE-shaped workload
+    "moe30b_logits": {"bytes": 106.960e9 + 79.575e9, "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "d67650bec883fd47"},
+}
 
 
 def sources_hash(files):
@@ -54,18 +52,12 @@ def sources_hash(files):
     return h.hexdigest()[:16]
 
 
-def gemm_sources_hash():
-    return sources_hash(GEMM_SOURCES)
-
-
 def captured_traffic(workload):
-    cap, files = {TRAFFIC_CAPTURE["workload"]: (TRAFFIC_CAPTURE, GEMM_SOURCES),
-                  LOGITS_TRAFFIC_CAPTURE["workload"]: (LOGITS_TRAFFIC_CAPTURE, LOGITS_SOURCES)
-                  }.get(workload, (None, None))
+    cap = TRAFFIC_CAPTURES.get(workload)
     if cap is None or cap["bytes"] is None:
         return None
     try:
-        ok = sources_hash(files) == cap["sources_sha256_16"]
+        ok = sources_hash(cap["sources"]) == cap["sources_sha256_16"]
     except OSError:
         ok = False
     return cap["bytes"] if ok else None
@@ -254,7 +246,6 @@ def build_learner_batch(name, dev, rank):
 
 
 def run_ours(args):
-    import numpy as np
     import torch
     import invariant_logprobs_gb300 as rz
 
@@ -263,12 +254,57 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     rz.load()
     peaks, peak_src = load_peaks()
-    stream = torch.cuda.current_stream()
 
     if args.config == "moe30b_logits":
-        return run_logits(args, world, rank, dev, peaks, peak_src)
+        out = measure_logits(args, world, rank, dev, peaks, peak_src, args.steps, args.warmup)
+    else:
+        out = measure_learner(args, world, rank, local, dev, peaks, peak_src)
+    if world == 1 and not args.no_other_workloads:
+        torch.cuda.empty_cache()
+        out["other_workloads"] = other_workloads(args, rank, dev, peaks, peak_src)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
 
-    wl, b = build_learner_batch(args.config, dev, rank)
+
+def other_workloads(args, rank, dev, peaks, peak_src):
+    """The other two bench workloads, shorter (3 warm-ups, up to 5 timed
+    steps each), so that one default run records all three: the 1.5B-shaped
+    learner step and the HBM-bound given-logits step."""
+    import torch
+    steps = max(2, min(args.steps, 5))
+    res = {}
+    for name in ("qwen4b_lag64", "qwen1p5b_lag2", "moe30b_logits"):
+        if name == args.config:
+            continue
+        if name == "moe30b_logits":
+            r = measure_logits(args, 1, rank, dev, peaks, peak_src, steps, 3, full=False)
+            res[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup",
+                                           "roofline", "step_breakdown", "config")}
+        else:
+            r = measure_learner(args, 1, rank, dev.index, dev, peaks, peak_src, name=name,
+                                steps=steps, warmup=3, full=False)
+            res[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup",
+                                           "algorithmic_tflops",
+                                           "algorithmic_frac_of_sustained_bf16", "roofline",
+                                           "step_breakdown", "config")}
+        torch.cuda.empty_cache()
+    return res
+
+
+def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, steps=None,
+                    warmup=None, full=True):
+    """The learner step on one workload: `steps` timed steps after `warmup`
+    untimed ones, then the per-class breakdown of two more; with `full`, also
+    clocks, the rollout entry points, the same-box cuBLAS comparison, the
+    end-to-end run and the CPU baseline."""
+    import torch
+    import invariant_logprobs_gb300 as rz
+    name = name or args.config
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    stream = torch.cuda.current_stream()
+    wl, b = build_learner_batch(name, dev, rank)
     T, d, V, B = b["T"], b["d"], b["V"], b["B"]
     ws = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
     dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
@@ -285,31 +321,88 @@ def run_ours(args):
                            logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
                            err_flag=err)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
+    if full:
+        clk.start()
+        time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ev[0].record(stream)
-    for k in range(args.steps):
+    for k in range(steps):
         step()
         ev[k + 1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    per_step = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
+    per_step = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
 
-    # dominant kernel, timed live: the LM-head logprob GEMM (rollout entry point,
-    # one tcgen05 GEMM launch per 38,912 rows + a tiny merge) over the same rows
+    # the step split by kernel class: two more (untimed) steps with the
+    # library's launch-class timing on (CUDA events on the launching stream)
+    breakdown = profile_steps(rz, step, stream, 2)
+    ms = max_over_ranks(total_ms / steps, world)
+    value = T * world / (ms / 1e3)
+    flop_alg = 6.0 * d * V * T
+    keep_ms, keep_launches = breakdown["classes"]["keep_gemm"]["ms"], \
+        breakdown["classes"]["keep_gemm"]["launches"]
+    keep_tf = 2.0 * d * V * T / (keep_ms / 1e3) / 1e12
+    for cname in ("keep_gemm", "dH_gemm", "dW_gemm"):
+        c = breakdown["classes"][cname]
+        c["tflops"] = 2.0 * d * V * T / (c["ms"] / 1e3) / 1e12
+    breakdown["classes"]["dz"]["gbs"] = T * 4.125 * V / (breakdown["classes"]["dz"]["ms"] / 1e3) / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the workload, random-init weights)",
+        "config": {"workload": wl.name, "tokens_per_step": T, "responses": B, "group": wl.group,
+                   "d": d, "V": V, "lag_steps": wl.drift_steps,
+                   "l2": "inputs larger than L2 (H %.1f GB), no flush" % (T * d * 2 / 1e9),
+                   "parallelism": "dp%d replicas" % world},
+        "step_ms_median": statistics.median(per_step),
+        "algorithmic_tflops": flop_alg / (ms / 1e3) / 1e12,
+        "algorithmic_frac_of_sustained_bf16": flop_alg / (ms / 1e3) / 1e12 /
+        peaks["bf16_tflops_sustained"],
+        # the dominant kernel of the timed step: the learner's logits +
+        # log-sum-exp GEMM that keeps the softmax terms (2dV flop per token),
+        # timed per launch by the launch-class events of the profiled steps
+        "roofline": {
+            "kernel": "gemm_kernel<EpiLseKeep> (learner logits+LSE GEMM, one launch per "
+                      "38,912-row chunk)",
+            "bound": "tensor", "achieved": keep_tf,
+            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": keep_tf / peaks["bf16_tflops_sustained"],
+            "peak_source": "%s bf16_tflops_sustained (the kernel runs inside a %.1f s step under "
+                           "the power cap)" % (peak_src, ms / 1e3),
+            "frac_of_burst": keep_tf / peaks["bf16_tflops"],
+            "ms_per_launch": keep_ms / keep_launches, "launches_per_step": keep_launches,
+            "flop_per_launch": 2.0 * d * V * T / keep_launches,
+            "traffic": captured_traffic(wl.name),
+            "traffic_unit": "DRAM bytes per 38,912-row launch (ncu capture of a smaller chunk, "
+                            "scaled by rows; see the committed ncu summary)",
+            # H chunk + W + the chunk's split states read; fp16 terms, running
+            # maxima and split states written
+            "algorithmic_bytes_per_launch": 38912 * d * 2 + V * d * 2 +
+            38912 * (2 * ((V + 7) // 8 * 8) + 4 * ((V + 127) // 128 * 4)) +
+            rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 38912, d, V, 0)},
+        "step_breakdown": breakdown,
+        "gpu_launches": steps * launches_per_step(T, V),
+        "device_err_flag": int(err.item()),
+        "loss": float(loss.item()), "d3": float(d3.item()),
+    }
+    if not full:
+        return out
+
+    # the rollout's LM-head logprob GEMM (one tcgen05 GEMM launch per 38,912
+    # rows + a tiny merge) over the same rows, with the lagged weights
     lp2 = torch.empty(T, dtype=torch.float32, device=dev)
     ws_r = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, dev)
     rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], logprob_out=lp2, ws=ws_r)
     torch.cuda.synchronize()
-    kr = max(2, min(args.steps, 5))
+    kr = max(2, min(steps, 5))
     rev = [torch.cuda.Event(enable_timing=True) for _ in range(kr + 1)]
     rev[0].record(stream)
     for k in range(kr):
@@ -329,54 +422,28 @@ def run_ours(args):
         rev[k + 1].record(stream)
     torch.cuda.synchronize()
     samp_ms = statistics.mean(rev[k].elapsed_time(rev[k + 1]) for k in range(kr))
-    del ws_s, tok_s
+    del ws_s, tok_s, ws_r, lp2
     # same-box reference: cuBLAS bf16 GEMM of one chunk's shape, interleaved
     ours_tf, cub_tf = gemm_vs_cublas(b["H"], b["W_mu"], b["tokens"], rz, dev, stream)
-    clocks = clk.stop()
+    out["clocks"] = clk.stop()
 
     # end to end through the public API from pinned host buffers
-    e2e = run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err)
-
-    ms = max_over_ranks(total_ms / args.steps, world)
-    value = T * world / (ms / 1e3)
-    flop_alg = 6.0 * d * V * T
-    out = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; shapes and distributions of the workload, random-init weights)",
-        "config": {"workload": wl.name, "tokens_per_step": T, "responses": B, "group": wl.group,
-                   "d": d, "V": V, "lag_steps": wl.drift_steps,
-                   "l2": "inputs larger than L2 (H %.1f GB), no flush" % (T * d * 2 / 1e9),
-                   "parallelism": "dp%d replicas" % world},
-        "step_ms_median": statistics.median(per_step),
-        "algorithmic_tflops": flop_alg / (ms / 1e3) / 1e12,
-        "algorithmic_frac_of_sustained_bf16": flop_alg / (ms / 1e3) / 1e12 /
-        peaks["bf16_tflops_sustained"],
-        "roofline": {
-            "kernel": "gemm_kernel<EpiLsePartial> (LM-head logprob GEMM, timed via rz_token_logprob)",
-            "bound": "tensor", "achieved": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12,
-            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": 2.0 * d * V * T / (roll_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
-            "peak_source": "%s bf16_tflops_sustained" % peak_src,
-            "traffic": captured_traffic(wl.name),
-            "traffic_unit": "DRAM bytes per launch of 38,912 rows (ncu capture, see profiles/)",
-            # H block + W + the block's split states and gathered logits
-            "algorithmic_bytes_per_launch": 38912 * d * 2 + V * d * 2 +
-            rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 38912, d, V, 0),
-            "launches_per_call": (T + 38911) // 38912},
-        "same_box_interleaved": {"logprob_gemm_tflops": ours_tf, "cublas_bf16_tflops": cub_tf,
-                                 "ratio": ours_tf / cub_tf,
-                                 "note": "alternating 1.5 s runs, 3 rounds, medians; cuBLAS "
-                                         "[38912,d]x[d,V] bf16 with its output written"},
-        "rollout_tokens_per_s": T / (roll_ms / 1e3),
-        "rollout_sample_tokens_per_s": T / (samp_ms / 1e3),
-        "clocks": clocks,
-        "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step(T, V),
-        "device_err_flag": int(err.item()),
-        "loss": float(loss.item()), "d3": float(d3.item()),
-    }
+    out["e2e"] = run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err)
+    roll_tf = 2.0 * d * V * T / (roll_ms / 1e3) / 1e12
+    out["rollout_gemm"] = {
+        "kernel": "gemm_kernel<EpiLsePartial> (rollout logprob GEMM via rz_token_logprob)",
+        "achieved_tflops": roll_tf,
+        "frac_of_sustained": roll_tf / peaks["bf16_tflops_sustained"],
+        "frac_of_burst": roll_tf / peaks["bf16_tflops"],
+        "note": "timed back to back for about a second; the sustained peak is cuBLAS in a "
+                "4 s loop and the burst peak its best single run, so a kernel between the "
+                "two reads above 1.0 of sustained"}
+    out["same_box_interleaved"] = {
+        "logprob_gemm_tflops": ours_tf, "cublas_bf16_tflops": cub_tf, "ratio": ours_tf / cub_tf,
+        "note": "alternating 1.5 s runs, 3 rounds, medians; cuBLAS [38912,d]x[d,V] bf16 with "
+                "its output written"}
+    out["rollout_tokens_per_s"] = T / (roll_ms / 1e3)
+    out["rollout_sample_tokens_per_s"] = T / (samp_ms / 1e3)
     if rank == 0 and not args.no_cpu_baseline:
         s = oracle_sample(b, args.cpu_tokens)
         v, dt = time_oracle(s)
@@ -384,9 +451,7 @@ def run_ours(args):
                                "kind": "oracle",
                                "sample": "%d tokens (first responses) of the same batch at full "
                                          "d=%d, V=%d; fp64 numpy, %.1f s" % (s["T"], d, V, dt)}
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    return 0
+    return out
 
 
 def gemm_vs_cublas(H, W, tokens, rz, dev, stream, rows=155648, seconds=1.5, rounds=3):
@@ -430,6 +495,30 @@ def gemm_vs_cublas(H, W, tokens, rz, dev, stream, rows=155648, seconds=1.5, roun
             res[name].append(fl / (t / 1e3) / 1e12)
     del out, ws
     return statistics.median(res["ours"]), statistics.median(res["cublas"])
+
+
+def profile_steps(rz, step, stream, n):
+    """Run n more learner steps with the library's launch-class timing on;
+    returns per-step milliseconds and kernel launches of each class, their
+    sum, and the steps' own CUDA-event time for comparison."""
+    import torch
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    rz.rz_profile_begin()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    prof = rz.rz_profile_end()
+    total = e0.elapsed_time(e1) / n
+    classes = {k: {"ms": v[0] / n, "launches": v[1] // n} for k, v in prof.items() if v[1] > 0}
+    summed = sum(c["ms"] for c in classes.values())
+    for c in classes.values():
+        c["share"] = c["ms"] / summed
+    return {"classes": classes, "sum_ms": summed, "step_ms": total, "steps": n,
+            "note": "one CUDA event pair per launch class on the launching stream, two untimed "
+                    "steps after the timed region"}
 
 
 def launches_per_step(T, V):
@@ -495,11 +584,15 @@ def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err):
     ms = e0.elapsed_time(e1) / K
     return {"value": b["T"] / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "note": "inputs uploaded from pinned host memory every step; upload of step k+1 "
-                    "overlaps compute of step k"}
+            "note": "inputs (H, tokens, log mu, cu_seqlens, rewards) uploaded from pinned host "
+                    "memory every step, the upload of step k+1 overlapping the compute of step "
+                    "k; loss and D3 read back.  W stays resident and dH, dW stay on the device "
+                    "for an on-device optimiser, as in a training loop"}
 
 
-def run_logits(args, world, rank, dev, peaks, peak_src):
+def measure_logits(args, world, rank, dev, peaks, peak_src, steps, warmup, full=True):
+    """The given-logits step (rz_logits_loss_fwd_bwd) on the MoE-shaped
+    workload; with `full`, also clocks and the CPU baseline."""
     import torch
     import invariant_logprobs_gb300 as rz
     from invariant_logprobs_gb300 import synth
@@ -525,44 +618,52 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
         rz.rz_logits_loss_fwd_bwd(b["logits"], b["tokens"], logmu, b["cu"], adv,
                                   logprob_out=lp, loss_out=loss, d3_out=d3, ws=ws, err_flag=err)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     clk = ClockSampler(dev.index)
-    clk.start()
-    time.sleep(0.3)
+    if full:
+        clk.start()
+        time.sleep(0.3)
     barrier(world)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ev[0].record(stream)
-    for k in range(args.steps):
+    for k in range(steps):
         step()
         ev[k + 1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = clk.stop()
-    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]) / args.steps, world)
+    clocks = clk.stop() if full else None
+    breakdown = profile_steps(rz, step, stream, 2)
+    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]) / steps, world)
+    rows_ms = breakdown["classes"]["logits_rows"]["ms"]
     alg_bytes = T * (4.0 * V + 12.0)
     out = {
         "metric": METRIC, "value": T * world / (ms / 1e3), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic bf16 logits ~N(0,3) (in place: later steps read the previous dz)",
         "config": {"workload": wl.name, "tokens_per_step": T, "responses": B, "V": V,
                    "l2": "inputs larger than L2 (%.0f GB), no flush" % (T * V * 2 / 1e9),
                    "parallelism": "dp%d replicas" % world},
+        # one launch of the row kernel per step, timed by the launch-class
+        # events of the profiled steps
         "roofline": {"kernel": "logits_row_kernel", "bound": "hbm",
-                     "achieved": alg_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": alg_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "achieved": alg_bytes / (rows_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": alg_bytes / (rows_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                      "peak_source": "%s hbm_gbs" % peak_src,
+                     "ms_per_launch": rows_ms,
                      "traffic": captured_traffic(wl.name),
                      "traffic_unit": "DRAM bytes per launch (262,144 rows; ncu capture, "
-                                     "see profiles/)",
+                                     "see the committed ncu summary)",
                      "algorithmic_bytes_per_launch": alg_bytes},
-        "clocks": clocks,
-        "gpu_launches": 4 * args.steps,  # response factors, row kernel, loss (2)
+        "step_breakdown": breakdown,
+        "gpu_launches": 4 * steps,  # response factors, row kernel, loss (2)
         "device_err_flag": int(err.item()),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if clocks is not None:
+        out["clocks"] = clocks
+    if full and rank == 0 and not args.no_cpu_baseline:
         s = logits_oracle_sample(b["logits"], b["tokens"], logmu, b["cu"], b["rewards"], b["G"],
                                  args.cpu_tokens)
         v, dt = time_logits_oracle(s)
@@ -571,9 +672,7 @@ def run_logits(args, world, rank, dev, peaks, peak_src):
                                "sample": "first %d rows of the same logits at V=%d (log pi, "
                                          "loss, dz for every row); fp64 numpy, %.1f s"
                                          % (s["T"], V, dt)}
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    return 0
+    return out
 
 
 # ----------------------------------------------------------------- reference arm
@@ -727,6 +826,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=1024,
                     help="tokens of the CPU oracle's timed sample (about 10 s at the 4B shape)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only --config (by default the other two bench workloads follow, "
+                         "briefly, under other_workloads)")
     ap.add_argument("--profile", choices=["learner", "logits", "sample", "rollout"], default=None,
                     help="small fixed case for ncu captures (no timing output)")
     ap.add_argument("--rows", type=int, default=16384)

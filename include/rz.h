@@ -23,6 +23,9 @@
  *     never frees or keeps them.  Scalars are written to device pointers.
  *   - The library allocates no device memory.  Scratch space is the caller's
  *     `ws` buffer of at least rz_workspace_size(...) bytes (256-byte aligned).
+ *     One exception: rz_token_logprob_noalloc uses a 32 MiB array built into
+ *     the library, which every GPU that loads the library holds for the life
+ *     of the process (whether or not that entry point is called).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
  *     never synchronise the host.  A return of RZ_OK means the work was
  *     enqueued; faults found on the device are reported through `err_flag`.
@@ -296,6 +299,9 @@ RZ_API int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32
  *   - It never calls cudaMalloc/cudaFree or any allocating library routine.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.
+ *     The address is then kept for the life of the process: after a
+ *     cudaDeviceReset() of a device, do not call this entry point on it again
+ *     (the kept address would name memory of the destroyed context).
  *   - All calls on a device share the array, and it keeps the last call's
  *     contents (nothing in it needs zeroing).  Calls that overlap on the GPU
  *     (different streams, or threads without ordering) race on it and give
@@ -320,6 +326,35 @@ RZ_API int rz_selftest_wait_timeout(int32_t* err_flag, int32_t* done_out, uint32
 
 /* Size in bytes of the built-in scratch used by rz_token_logprob_noalloc. */
 RZ_API size_t rz_noalloc_scratch_bytes(void);
+
+/*
+ * Launch-class timing, a measurement aid (no counterpart on the pages).
+ * After rz_profile_begin(), every entry point brackets each class of its
+ * launches with a pair of CUDA events recorded on the stream it launches
+ * on, so one call's device time can be split by kernel without a profiler.
+ * rz_profile_end() waits (host-blocking) for the recorded events, writes
+ * the milliseconds of each class to ms_out[RZ_PROF_*] and the number of
+ * kernels launched in it to launches_out[RZ_PROF_*] (nullable), releases
+ * the events and stops recording.  n_classes >= RZ_PROF_CLASSES.
+ *   - Off by default: nothing is recorded and nothing is synchronised.
+ *   - The events sit between launches on one stream, so the classes add up
+ *     to the calls' device time (plus event gaps of a few microseconds).
+ *   - Calls on a stream that is being captured into a CUDA graph are not
+ *     recorded.  The recording is process-wide (a mutex guards it).
+ * Returns RZ_ERR_INVALID_ARG for a null ms_out or a short array, RZ_ERR_CUDA
+ * if an event could not be read (the other classes are still filled).
+ */
+#define RZ_PROF_LOGPROB_GEMM 0  /* rollout logprob GEMM; fused-sampling GEMM */
+#define RZ_PROF_KEEP_GEMM    1  /* learner logits + log-sum-exp GEMM keeping the terms */
+#define RZ_PROF_MERGE        2  /* split merges: log pi, lse, c_t, sampled token */
+#define RZ_PROF_DZ           3  /* dz pass over the kept terms */
+#define RZ_PROF_DH_GEMM      4  /* dH = dz W */
+#define RZ_PROF_DW_GEMM      5  /* dW = dz^T H, accumulated over chunks */
+#define RZ_PROF_LOGITS_ROWS  6  /* given-logits row kernel */
+#define RZ_PROF_SMALL        7  /* advantages, response factors, loss, D3, statistics */
+#define RZ_PROF_CLASSES      8
+RZ_API int rz_profile_begin(void);
+RZ_API int rz_profile_end(float* ms_out, int32_t* launches_out, int32_t n_classes);
 
 #ifdef __cplusplus
 }

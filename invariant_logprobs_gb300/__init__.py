@@ -28,6 +28,9 @@ RZ_DEVERR_TOKEN_RANGE = 1
 RZ_DEVERR_CU_SEQLENS = 2
 RZ_DEVERR_TIMEOUT = 4
 
+RZ_PROF_NAMES = ("logprob_gemm", "keep_gemm", "merge", "dz", "dH_gemm", "dW_gemm",
+                 "logits_rows", "small")  # index = RZ_PROF_* class
+
 RZ_OP_TOKEN_LOGPROB = 0
 RZ_OP_LOSS_FWD_BWD = 1
 RZ_OP_LOGITS_LOSS = 2
@@ -63,6 +66,8 @@ _SIGNATURES = {
     "rz_sample_logprob": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, ctypes.c_uint64,
                                          _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_peak_to_median": (ctypes.c_int, [_P, _I64, _P]),
+    "rz_profile_begin": (ctypes.c_int, []),
+    "rz_profile_end": (ctypes.c_int, [_P, _P, _I32]),
 }
 
 
@@ -544,3 +549,18 @@ def rz_selftest_wait_timeout(err_flag, done_out=None, limit_us=50000, stream=Non
     _same_device(err_flag, done_out)
     _check("rz_selftest_wait_timeout", load().rz_selftest_wait_timeout(
         _ptr(err_flag), _ptr(done_out), int(limit_us), _stream(stream)))
+
+
+def rz_profile_begin():
+    """Start launch-class timing (see rz_profile_begin in include/rz.h)."""
+    _check("rz_profile_begin", load().rz_profile_begin())
+
+
+def rz_profile_end():
+    """Stop launch-class timing; blocks until the recorded events complete.
+    Returns {class name: (milliseconds, kernel launches)} for every class."""
+    n = len(RZ_PROF_NAMES)
+    ms = (ctypes.c_float * n)()
+    launches = (ctypes.c_int32 * n)()
+    _check("rz_profile_end", load().rz_profile_end(ms, launches, n))
+    return {name: (float(ms[i]), int(launches[i])) for i, name in enumerate(RZ_PROF_NAMES)}

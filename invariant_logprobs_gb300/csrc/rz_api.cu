@@ -78,20 +78,6 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
 namespace {
 
 // ------------------------------------------------------------------ workspace
-inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
-
-struct FwdLayout {  // logprob pass scratch
-  size_t part, zg, total;
-};
-FwdLayout fwd_layout(int64_t T, int32_t V) {
-  FwdLayout L{};
-  const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
-  L.part = 0;
-  L.zg = al256(t * vocab_splits(V) * sizeof(float2));
-  L.total = L.zg + al256(t * sizeof(float));
-  return L;
-}
-
 struct SampleLayout {
   size_t part, idx, total;
 };
@@ -128,13 +114,6 @@ LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
   return L;
 }
 
-inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool a256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
-
-bool sizes_ok(int64_t T, int32_t d, int32_t V) {
-  return T >= 0 && T < (int64_t(1) << 31) && V >= 1 && V <= (1 << 24) && d >= 8 && d <= 65536;
-}
-
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RZ_OK : RZ_ERR_CUDA; }
 
 #define RZ_TRY(expr)                                  \
@@ -154,7 +133,12 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
   const FwdLayout L = fwd_layout(T, V);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
   float* zg = reinterpret_cast<float*>(ws + L.zg);
-  RZ_TRY(launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err, st));
+  {
+    ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax),
+                 st);
+    RZ_TRY(launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err, st));
+  }
+  ProfScope ps(RZ_PROF_MERGE, 1, st);
   RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse_ws, err, st));
   return RZ_OK;
 }
@@ -179,6 +163,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   float2* fac = reinterpret_cast<float2*>(w8 + L.fac);
 
   if (T == 0) {
+    ProfScope ps(RZ_PROF_SMALL, sc ? 3 : 2, st);
     RZ_TRY(cudaMemsetAsync(dW, 0, size_t(V) * size_t(d) * sizeof(float), st));
     if (sc) {
       RZ_TRY(launch_resp_factors(cu_seqlens, adv, nullptr, B, 0, fac, st));
@@ -208,8 +193,11 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
 
   // (A_i, 1/(B T_i)) per response: all the coefficient needs besides w_t
   // (Score Centering: A_i - Abar).
-  RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
-  if (sc) RZ_TRY(launch_sc_centre(fac, B, st));
+  {
+    ProfScope ps(RZ_PROF_SMALL, sc ? 2 : 1, st);
+    RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+    if (sc) RZ_TRY(launch_sc_centre(fac, B, st));
+  }
 
   // Chunk by chunk in row order: logits once, folded exactly as the rollout
   // folds them, keeping the fold's terms; merge + c_t; dz in place; dH, dW.
@@ -223,19 +211,33 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
     CUtensorMap tmE16;
     if (!make_tmap_bf16(&tmE16, dz, V, rows, uint64_t(ldz) * 2, 64, 32))
       return RZ_ERR_UNSUPPORTED;
-    RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, tmE16, emax, ldm,
-                           err_flag, st));
-    RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
-                                 sc ? nullptr : logmu + r0, cu_seqlens, fac,
-                                 action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
-                                 st));
-    RZ_TRY(launch_dz_rows(dz, ldz, emax, ldm, rows, V, tokens + r0, lse_c, coef_c, logpi + r0,
-                          st));
-    RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
+    {
+      ProfScope ps(RZ_PROF_KEEP_GEMM, 1, st);
+      RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, tmE16, emax, ldm,
+                             err_flag, st));
+    }
+    {
+      ProfScope ps(RZ_PROF_MERGE, 1, st);
+      RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
+                                   sc ? nullptr : logmu + r0, cu_seqlens, fac,
+                                   action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
+                                   st));
+    }
+    {
+      ProfScope ps(RZ_PROF_DZ, 1, st);
+      RZ_TRY(launch_dz_rows(dz, ldz, emax, ldm, rows, V, tokens + r0, lse_c, coef_c, logpi + r0,
+                            st));
+    }
+    {
+      ProfScope ps(RZ_PROF_DH_GEMM, 1, st);
+      RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
+    }
+    ProfScope ps(RZ_PROF_DW_GEMM, 1, st);
     RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
   }
 
   // Loss (and D3) over all rows (fixed-order reductions).
+  ProfScope ps(RZ_PROF_SMALL, 2, st);
   if (sc) {
     RZ_TRY(launch_sc_loss(logpi, cu_seqlens, action_mask, fac, B, T, loss_out, w8 + L.resp,
                           err_flag, st));
@@ -310,6 +312,8 @@ int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
+  ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax) + 1,
+               reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(launch_sample(tmH, tmW, T, d, V, row_ids, seed,
                                    reinterpret_cast<float4*>(w8 + L.part),
                                    reinterpret_cast<int*>(w8 + L.idx), tokens_out, logprob_out,
@@ -322,6 +326,7 @@ int rz_group_advantage(const float* rewards, int32_t B, int32_t G, float* adv_ou
   if (B == 0) return RZ_OK;
   if (!rewards || !adv_out) return RZ_ERR_INVALID_ARG;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  ProfScope ps(RZ_PROF_SMALL, 1, reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(
       launch_group_advantage(rewards, B, G, adv_out, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -337,6 +342,7 @@ int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens
   const size_t need = rz_workspace_size(RZ_OP_IS_LOSS, T, 0, 0, B);
   if (need > 0 && (!ws || ws_bytes < need || !a256(ws))) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  ProfScope ps(RZ_PROF_SMALL, 2, reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out,
                                     d3_out, coef_out, ws, err_flag,
                                     reinterpret_cast<cudaStream_t>(stream)));
@@ -346,6 +352,7 @@ int rz_d3(const float* logpi, const float* logmu, int64_t T, float* d3_out, rz_s
   if (T < 0 || !d3_out) return RZ_ERR_INVALID_ARG;
   if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  ProfScope ps(RZ_PROF_SMALL, 1, reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(launch_d3(logpi, logmu, T, d3_out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -354,6 +361,7 @@ int rz_is_stats(const float* logpi, const float* logmu, int64_t T, float* stats_
   if (T < 0 || !stats_out) return RZ_ERR_INVALID_ARG;
   if (T > 0 && (!logpi || !logmu)) return RZ_ERR_INVALID_ARG;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  ProfScope ps(RZ_PROF_SMALL, 1, reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(
       launch_is_stats(logpi, logmu, T, stats_out, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -405,9 +413,16 @@ int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const f
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   float2* fac = reinterpret_cast<float2*>(w8 + is_loss_ws_bytes(B));
-  RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
-  RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, fac, action_mask, B,
-                            logprob_out, err_flag, st));
+  {
+    ProfScope ps(RZ_PROF_SMALL, 1, st);
+    RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+  }
+  {
+    ProfScope ps(RZ_PROF_LOGITS_ROWS, 1, st);
+    RZ_TRY(launch_logits_rows(logits_inout, T, V, tokens, logmu, cu_seqlens, fac, action_mask, B,
+                              logprob_out, err_flag, st));
+  }
+  ProfScope ps(RZ_PROF_SMALL, 2, st);
   RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
                         nullptr, ws, err_flag, st));
   return RZ_OK;

@@ -35,11 +35,47 @@ int64_t chunk_rows(int32_t V);
 inline int64_t dz_ld(int32_t V) { return (static_cast<int64_t>(V) + 7) / 8 * 8; }
 inline int64_t emax_ld(int32_t V) { return (static_cast<int64_t>(V) + 127) / 128 * 4; }
 
+// ---- argument checks and the logprob pass's scratch layout, shared by
+// every entry point that runs that pass (rz_api.cu, rz_noalloc.cu)
+inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool a256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline bool sizes_ok(int64_t T, int32_t d, int32_t V) {
+  return T >= 0 && T < (int64_t(1) << 31) && V >= 1 && V <= (1 << 24) && d >= 8 && d <= 65536;
+}
+struct FwdLayout {  // logprob pass scratch: split states [T, S], gathered logit [T]
+  size_t part, zg, total;
+};
+inline FwdLayout fwd_layout(int64_t T, int32_t V) {
+  FwdLayout L{};
+  const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
+  L.part = 0;
+  L.zg = al256(t * vocab_splits(V) * sizeof(float2));
+  L.total = L.zg + al256(t * sizeof(float));
+  return L;
+}
+
 int num_sms();
 bool device_ok();  // current device is sm_103 (or newer family member we compiled for)
 
 bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---- launch-class timing (rz_profile.cu): while rz_profile_begin() is in
+// effect, brackets the launches made in its lifetime with CUDA events on
+// `st` (classes RZ_PROF_*, `launches` kernels); otherwise does nothing.
+class ProfScope {
+ public:
+  ProfScope(int cls, int launches, cudaStream_t st);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  int cls_, launches_;
+  cudaStream_t st_;
+  void* e0_;
+};
 
 // ---- lm-head kernels (rz_lmhead.cu)
 cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,

@@ -51,8 +51,6 @@ void* scratch_on_current_device() {
   return g_scratch_ptr[dev];
 }
 
-inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
-
 }  // namespace
 }  // namespace rz
 
@@ -65,19 +63,16 @@ size_t rz_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int64_t T,
                              int32_t d, int32_t V, float* logprob_out, float* lse_out,
                              int32_t* err_flag, rz_stream_t stream) {
-  if (T < 0 || T >= (int64_t(1) << 31) || V < 1 || V > (1 << 24) || d < 8 || d > 65536)
-    return RZ_ERR_INVALID_ARG;
+  if (!sizes_ok(T, d, V)) return RZ_ERR_INVALID_ARG;
   if (T > 0 && (!H || !W || !tokens || !logprob_out)) return RZ_ERR_INVALID_ARG;
   if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
   if (T == 0) return RZ_OK;
-  if ((reinterpret_cast<uintptr_t>(H) & 15u) || (reinterpret_cast<uintptr_t>(W) & 15u))
-    return RZ_ERR_UNSUPPORTED;
-  // Same layout as the workspace of rz_token_logprob: per-row split states,
-  // then the gathered logit of each row.  Nothing in it needs zeroing: every
-  // entry the merge reads is written by the GEMM earlier in the same call.
-  const size_t part_bytes = al256(size_t(T) * size_t(vocab_splits(V)) * sizeof(float2));
-  const size_t need = part_bytes + al256(size_t(T) * sizeof(float));
-  if (need > kNoAllocScratchBytes) return RZ_ERR_TOO_LARGE;
+  if (!a16(H) || !a16(W)) return RZ_ERR_UNSUPPORTED;
+  // The workspace layout of rz_token_logprob: per-row split states, then the
+  // gathered logit of each row.  Nothing in it needs zeroing: every entry
+  // the merge reads is written by the GEMM earlier in the same call.
+  const FwdLayout L = fwd_layout(T, V);
+  if (L.total > kNoAllocScratchBytes) return RZ_ERR_TOO_LARGE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   uint8_t* scratch = static_cast<uint8_t*>(scratch_on_current_device());
   if (!scratch) return RZ_ERR_CUDA;
@@ -86,8 +81,8 @@ int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const int32_t* 
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  float2* part = reinterpret_cast<float2*>(scratch);
-  float* zg = reinterpret_cast<float*>(scratch + part_bytes);
+  float2* part = reinterpret_cast<float2*>(scratch + L.part);
+  float* zg = reinterpret_cast<float*>(scratch + L.zg);
   if (launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err_flag, st) != cudaSuccess)
     return RZ_ERR_CUDA;
   if (launch_lse_merge(T, V, tokens, part, zg, logprob_out, lse_out, nullptr, err_flag, st) !=

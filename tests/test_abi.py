@@ -238,3 +238,22 @@ def test_vocab_splits_depend_on_v_only(lib):
         assert splits(V) == want == rule(V), V
     for T in (32, 64, 320):
         assert splits(151936, T) == 60
+
+
+def test_profile_classes_and_host_side_behaviour(lib):
+    """The timing hook's class ids match the binding's names; without a
+    recorded call it returns zeros; a short output array is refused."""
+    import invariant_logprobs_gb300 as rz
+    src = open(HEADER).read()
+    ids = {m.group(1): int(m.group(2))
+           for m in re.finditer(r"#define RZ_PROF_(\w+)\s+(\d+)", src)}
+    assert ids.pop("CLASSES") == len(rz.RZ_PROF_NAMES)
+    assert sorted(ids.values()) == list(range(len(rz.RZ_PROF_NAMES)))
+    assert [n.lower() for n, _ in sorted(ids.items(), key=lambda kv: kv[1])] == \
+        [n.lower() for n in rz.RZ_PROF_NAMES]
+    rz.rz_profile_begin()
+    got = rz.rz_profile_end()
+    assert got == {n: (0.0, 0) for n in rz.RZ_PROF_NAMES}
+    ms = (ctypes.c_float * 3)()
+    assert lib.rz_profile_end(ms, None, 3) == rz.RZ_ERR_INVALID_ARG
+    assert lib.rz_profile_end(None, None, len(rz.RZ_PROF_NAMES)) == rz.RZ_ERR_INVALID_ARG

@@ -58,3 +58,30 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(rz):
     assert e.value.status == rz.RZ_ERR_TOO_LARGE
     torch.cuda.synchronize()
     assert float(out.abs().max()) == 0.0  # nothing was launched
+
+
+def test_noalloc_replays_in_a_captured_graph(rz):
+    """The first call on the device (outside capture) looks up the scratch
+    address; later calls may then be captured.  The replayed graph matches
+    rz_token_logprob bit for bit, also after its inputs are rewritten."""
+    T, d, V = 2000, 256, 151936
+    H, W, tok = _case(T, d, V, 21)
+    got = torch.empty(T, device=DEV)
+    rz.rz_token_logprob_noalloc(H, W, tok, got)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            rz.rz_token_logprob_noalloc(H, W, tok, got)
+    for k in range(2):
+        if k:
+            H2, _, tok2 = _case(T, d, V, 22)
+            H.copy_(H2)
+            tok.copy_(tok2)
+        got.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        want, _ = rz.rz_token_logprob(H, W, tok)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(got), bits(want))
