@@ -324,6 +324,18 @@ RZ_API int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const in
 RZ_API int rz_selftest_wait_timeout(int32_t* err_flag, int32_t* done_out, uint32_t limit_us,
                                     rz_stream_t stream);
 
+/*
+ * Debug build only (compiled with -DRZ_CHECKS; no counterpart on the pages):
+ * the kernels then check their computed indices (task coordinates, split
+ * states, running-max and dz offsets, tensor-store coordinates, output
+ * tiles) against the sizes of the call; a failed check skips the access,
+ * counts itself and records its site (a small integer naming the check).
+ * This call waits for the device, writes the number of failed checks since
+ * the last read and the site of the first, and clears both.  The normal
+ * build returns RZ_ERR_UNSUPPORTED (it has no checks).
+ */
+RZ_API int rz_debug_check_failures(uint32_t* count_out, int32_t* first_site_out);
+
 /* Size in bytes of the built-in scratch used by rz_token_logprob_noalloc. */
 RZ_API size_t rz_noalloc_scratch_bytes(void);
 

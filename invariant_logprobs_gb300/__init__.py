@@ -16,6 +16,9 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librz.so")
+# the debug build with device bounds checks (build.build(checks=True)); used
+# instead of librz.so when the environment sets RZ_LIB_VARIANT=checks
+LIB_PATH_CHECKS = os.path.join(_HERE, "librz_checks.so")
 
 RZ_OK = 0
 RZ_ERR_INVALID_ARG = 1
@@ -67,6 +70,7 @@ _SIGNATURES = {
                                          _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_peak_to_median": (ctypes.c_int, [_P, _I64, _P]),
     "rz_profile_begin": (ctypes.c_int, []),
+    "rz_debug_check_failures": (ctypes.c_int, [_P, _P]),
     "rz_profile_end": (ctypes.c_int, [_P, _P, _I32]),
 }
 
@@ -82,7 +86,7 @@ def load(path=None):
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    p = path or (LIB_PATH_CHECKS if os.environ.get("RZ_LIB_VARIANT") == "checks" else LIB_PATH)
     if not os.path.exists(p):
         raise RuntimeError("librz.so not built at %s: run invariant_logprobs_gb300.build" % p)
     lib = ctypes.CDLL(p)
@@ -564,3 +568,16 @@ def rz_profile_end():
     launches = (ctypes.c_int32 * n)()
     _check("rz_profile_end", load().rz_profile_end(ms, launches, n))
     return {name: (float(ms[i]), int(launches[i])) for i, name in enumerate(RZ_PROF_NAMES)}
+
+
+def rz_debug_check_failures():
+    """(failed device bounds checks since the last read, site of the first)
+    from the debug build, cleared on read; None with the normal build, which
+    has no checks."""
+    n = ctypes.c_uint32(0)
+    site = ctypes.c_int32(0)
+    st = load().rz_debug_check_failures(ctypes.byref(n), ctypes.byref(site))
+    if st == RZ_ERR_UNSUPPORTED:
+        return None
+    _check("rz_debug_check_failures", st)
+    return int(n.value), int(site.value)

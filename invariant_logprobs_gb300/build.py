@@ -15,6 +15,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librz.so")
+# the debug build: every device bounds check compiled in (-DRZ_CHECKS)
+BUILD_CHECKS = os.path.join(HERE, "_build_checks")
+LIB_CHECKS = os.path.join(HERE, "librz_checks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
@@ -42,43 +45,47 @@ def _stale(obj, src):
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    if not _stale(obj, src) and not extra:
+def _compile(src, flags, build_dir, force):
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    if not force and not _stale(obj, src):
         return obj, ""
-    cmd = [_nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
+    cmd = [_nvcc()] + ARCH + NVCC_FLAGS + flags + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stderr))
     return obj, r.stderr
 
 
-def build(verbose=False, extra=()):
-    """Compile every .cu under csrc/ and link librz.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    extra = list(extra)
+def build(verbose=False, extra=(), checks=False):
+    """Compile every .cu under csrc/ and link librz.so (with checks=True the
+    debug build librz_checks.so, device bounds checks compiled in); returns
+    the library's path.  Objects are rebuilt when a source is newer, or
+    always when extra flags are given."""
+    build_dir, lib = (BUILD_CHECKS, LIB_CHECKS) if checks else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
+    flags = list(extra) + (["-DRZ_CHECKS"] if checks else [])
     srcs = sources()
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, flags, build_dir, bool(extra)), srcs))
     objs = [o for o, _ in results]
     if verbose:
         for _, log in results:
             if log:
                 sys.stderr.write(log)
-    need_link = (not os.path.exists(LIB) or
-                 any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs))
+    need_link = (not os.path.exists(lib) or
+                 any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs))
     if need_link:
-        tmp = LIB + ".tmp"
+        tmp = lib + ".tmp"
         cmd = [_nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static",
                                                                   "-ldl", "-lpthread", "-lrt"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
     ex = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []
-    print(build(verbose=v or bool(ex), extra=ex))
+    print(build(verbose=v or bool(ex), extra=ex, checks="--checks" in sys.argv))

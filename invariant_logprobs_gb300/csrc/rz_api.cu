@@ -428,6 +428,21 @@ int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const f
   return RZ_OK;
 }
 
+int rz_debug_check_failures(uint32_t* count_out, int32_t* first_site_out) {
+  if (!count_out || !first_site_out) return RZ_ERR_INVALID_ARG;
+#ifndef RZ_CHECKS
+  return RZ_ERR_UNSUPPORTED;
+#else
+  unsigned int c1 = 0, c2 = 0;
+  int s1 = 0, s2 = 0;
+  if (check_read_lmhead(&c1, &s1) != cudaSuccess || check_read_logits(&c2, &s2) != cudaSuccess)
+    return RZ_ERR_CUDA;
+  *count_out = c1 + c2;
+  *first_site_out = c1 ? s1 : s2;
+  return RZ_OK;
+#endif
+}
+
 int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32_t d, int32_t V,
                      float* logits_out, int32_t* err_flag, rz_stream_t stream) {
   if (!sizes_ok(T, d, V)) return RZ_ERR_INVALID_ARG;

@@ -25,6 +25,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "rz_check.cuh"
 #include "rz_ptx.cuh"
 
 namespace rz {
@@ -192,6 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int task = blockIdx.x; ok && task < sched.num_tasks; task += gridDim.x) {
         int m_blk, grp, nb, ne;
         task_coords(sched, task, m_blk, grp, nb, ne);
+        if (!RZ_DCHECK(m_blk >= 0 && m_blk < sched.m_blocks && nb >= 0 && nb < ne &&
+                           ne <= sched.n_tiles && grp >= 0 && grp < sched.n_groups,
+                       1))
+          ne = nb;  // (debug build) a task outside the problem loads nothing
         const int m0 = m_blk * kBM + sched.a_m_off;
         for (int n = nb; ok && n < ne; ++n) {
           for (int kb = 0; kb < sched.k_blocks; ++kb) {

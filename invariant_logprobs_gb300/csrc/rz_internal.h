@@ -77,6 +77,12 @@ class ProfScope {
   void* e0_;
 };
 
+// ---- debug build (-DRZ_CHECKS): each unit's count of failed device bounds
+// checks and the site of the first one, read and cleared (0 and 0 in the
+// normal build)
+cudaError_t check_read_lmhead(unsigned int* count, int* site);
+cudaError_t check_read_logits(unsigned int* count, int* site);
+
 // ---- lm-head kernels (rz_lmhead.cu)
 cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                                int V, const int32_t* tokens, float2* part, float* zgather,

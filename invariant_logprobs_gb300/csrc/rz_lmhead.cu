@@ -24,6 +24,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "rz_check.cuh"
 #include "rz_gemm.cuh"
 #include "rz_internal.h"
 #include "rz_lse.cuh"
@@ -99,6 +100,7 @@ struct EpiLsePartial {
                                                   int row) {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
     if (g >= p.T) return;
+    if (!RZ_DCHECK(g >= 0 && grp >= 0 && grp < p.S, 10)) return;
     p.part[g * p.S + grp] = make_float2(st.m, st.s);
     if (st.found) p.zgather[g] = st.za;
   }
@@ -182,7 +184,8 @@ struct EpiLseKeep {
         chunk(p, st, r1, col0 + c + 32, w + 16);
         m1 = st.m;
       }
-      if (grow < p.lse.T) {
+      if (grow < p.lse.T &&
+          RZ_DCHECK(grow >= 0 && ((col0 + c) >> 5) + (col0 + c + 32 < V ? 2 : 1) <= p.ldm, 11)) {
         float* em = p.emax + grow * p.ldm + ((col0 + c) >> 5);
         if (col0 + c + 32 < V) {
           *reinterpret_cast<float2*>(em) = make_float2(m0, m1);
@@ -197,7 +200,8 @@ struct EpiLseKeep {
         mine[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && rbase < p.lse.T) {
+      if (lane == 0 && rbase < p.lse.T &&
+          RZ_DCHECK(rbase >= 0 && col0 + c >= 0 && col0 + c < V && ((col0 + c) & 7) == 0, 12)) {
         tma_store_2d_hint(&p.tm_e16, stage, col0 + c, rbase, pol);
         bulk_commit();
       }
@@ -405,6 +409,7 @@ struct EpiSample {
                                                   int row) {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
     if (g >= p.T) return;
+    if (!RZ_DCHECK(g >= 0 && grp >= 0 && grp < p.S, 13)) return;
     p.part[g * p.S + grp] = make_float4(st.m, st.s, st.bk, st.bz);
     p.part_idx[g * p.S + grp] = st.bi;
   }
@@ -429,6 +434,8 @@ struct EpiStore {
 
   static __device__ __forceinline__ void chunk(const Params& p, const uint32_t (&r)[32], long long rr,
                                                int cbase) {
+    if (!RZ_DCHECK(rr >= 0 && rr < p.rows && cbase >= 0 && cbase < p.cols && p.cols <= p.ld, 14))
+      return;
     if (kMode == 0) {
       uint16_t* dst = static_cast<uint16_t*>(p.out) + (p.row0 + rr) * p.ld + cbase;
       if (cbase + 32 <= p.cols) {
@@ -604,6 +611,7 @@ __global__ void __launch_bounds__(kDzThreads)
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int k = i + u * kDzThreads;
+      if (!RZ_DCHECK(8ll * k + 8 <= lde && (k >> 2) < ldm, 16)) return;
       q[u] = __ldcs(er + k);
       sc[u] = __fmul_rn(c, ex2_approx(__fmul_rn(__fsub_rn(__ldg(mr + (k >> 2)), l), kLog2e)));
     }
@@ -818,6 +826,16 @@ cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t
   GemmSched s = sched_of(rows, d, nt, V, err);
   EpiStore<0>::Params p{dH, d, row0, rows, d, 0};
   return run_gemm<EpiStore<0>, false, true>(tmDz, tmWmn, s, p, st);
+}
+
+cudaError_t check_read_lmhead(unsigned int* count, int* site) {
+#ifdef RZ_CHECKS
+  return check_read_and_clear(count, site);
+#else
+  *count = 0;
+  *site = 0;
+  return cudaSuccess;
+#endif
 }
 
 cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t row0,

@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "rz_check.cuh"
 #include "rz_internal.h"
 #include "rz_math.cuh"
 #include "rz_ptx.cuh"
@@ -38,36 +39,50 @@ constexpr size_t kRowSmem = kStashVec * sizeof(uint4);
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-__device__ __forceinline__ void fold8(const uint4& q, float& m2, float& s) {
+// Online (m, s): m = the largest logit so far (natural units, an exact
+// logit value), s = sum 2^((z - m) log2 e).  z - m is taken first, so the
+// maximum's own term is exactly 1 and a peaked row keeps its precision.
+__device__ __forceinline__ void fold8(const uint4& q, float& m, float& s) {
   const float v[8] = {bf_lo(q.x), bf_hi(q.x), bf_lo(q.y), bf_hi(q.y),
                       bf_lo(q.z), bf_hi(q.z), bf_lo(q.w), bf_hi(q.w)};
-  float cm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
-                   fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
-  const float cm2 = cm * kLog2e;
-  if (cm2 > m2) {
-    s *= ex2_approx(m2 - cm2);
-    m2 = cm2;
+  const float cm = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+                         fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+  if (cm > m) {
+    s *= ex2_approx((m - cm) * kLog2e);
+    m = cm;
   }
-  const float nm = -m2;
   float a0 = 0.f, a1 = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; j += 2) {
-    a0 += ex2_approx(fmaf(v[j], kLog2e, nm));
-    a1 += ex2_approx(fmaf(v[j + 1], kLog2e, nm));
+    a0 += ex2_approx((v[j] - m) * kLog2e);
+    a1 += ex2_approx((v[j + 1] - m) * kLog2e);
   }
   s += a0 + a1;
 }
 
-__device__ __forceinline__ uint4 dz8(const uint4& q, float nl, float c, int rel) {
+// Merge two (m, s) states of fold8.
+__device__ __forceinline__ void lse_merge_nat(float& m, float& s, float m_o, float s_o) {
+  if (m_o > m) {
+    s = s * ex2_approx((m - m_o) * kLog2e) + s_o;
+    m = m_o;
+  } else if (m_o > -INFINITY) {
+    s = s + s_o * ex2_approx((m_o - m) * kLog2e);
+  }
+}
+
+// dz of 8 columns: c p_v = c 2^((z_v - M) log2 e - log2 S), and at the
+// sampled column c expm1(log pi) (no cancellation of p - 1 as p -> 1).
+__device__ __forceinline__ uint4 dz8(const uint4& q, float M, float nl2s, float c,
+                                     float c_onehot, int rel) {
   const float v[8] = {bf_lo(q.x), bf_hi(q.x), bf_lo(q.y), bf_hi(q.y),
                       bf_lo(q.z), bf_hi(q.z), bf_lo(q.w), bf_hi(q.w)};
   float g[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) g[j] = c * ex2_approx(fmaf(v[j], kLog2e, nl));
+  for (int j = 0; j < 8; ++j) g[j] = c * ex2_approx(fmaf(v[j] - M, kLog2e, nl2s));
   if (static_cast<unsigned>(rel) < 8u) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (rel == j) g[j] -= c;
+      if (rel == j) g[j] = c_onehot;
   }
   uint4 o;
   o.x = pack_bf16x2(g[0], g[1]);
@@ -85,7 +100,7 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
                       int* err) {
   extern __shared__ uint4 stash[];
   __shared__ float red_m[kRowThreads / 32], red_s[kRowThreads / 32];
-  __shared__ float bc[3];
+  __shared__ float bc[4];
   __shared__ int bci;
   const long long row = blockIdx.x;
   uint4* rowp = reinterpret_cast<uint4*>(logits + row * static_cast<long long>(V));
@@ -95,7 +110,7 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
   const uint64_t keep = l2_policy_last();
   const uint64_t drop = l2_policy_first();
 
-  // ---- pass 1: online (max, sum exp) in base 2
+  // ---- pass 1: online (max, sum exp)
   float m2 = -INFINITY, s = 0.f;
   int i = threadIdx.x;
   // four independent 16-byte loads in flight per thread
@@ -122,7 +137,7 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
   for (int o = 16; o > 0; o >>= 1) {
     const float mo = __shfl_xor_sync(0xffffffffu, m2, o);
     const float so = __shfl_xor_sync(0xffffffffu, s, o);
-    lse2_merge(m2, s, mo, so);
+    lse_merge_nat(m2, s, mo, so);
   }
   const int warp = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
@@ -132,9 +147,8 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
   __syncthreads();
   if (threadIdx.x == 0) {
     float M = red_m[0], S = red_s[0];
-    for (int w = 1; w < kRowThreads / 32; ++w) lse2_merge(M, S, red_m[w], red_s[w]);
-    const float l2 = M + log2f(S);
-    const float l = l2 * kLn2;
+    for (int w = 1; w < kRowThreads / 32; ++w) lse_merge_nat(M, S, red_m[w], red_s[w]);
+    const float log2s = log2f(S);
     const int a = tokens[row];
     float lp, c = 0.f;
     if (a < 0 || a >= V) {
@@ -142,7 +156,9 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
       if (err) atomicOr(err, 1);
     } else {
       const uint16_t zb = logits[row * static_cast<long long>(V) + a];
-      lp = __uint_as_float(static_cast<uint32_t>(zb) << 16) - l;
+      // log pi = (z_a - M) - ln S: z_a - M is exact, so a peaked row's
+      // log pi near 0 keeps its relative precision
+      lp = (__uint_as_float(static_cast<uint32_t>(zb) << 16) - M) - log2s * kLn2;
       // response of this row: the last i with cu[i] <= row
       int lo = 0, hi = B;  // invariant cu[lo] <= row < cu[hi]
       while (hi - lo > 1) {
@@ -157,13 +173,17 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
       c = act ? fac[lo].x * is_weight(lp, logmu[row]) * fac[lo].y : 0.f;
     }
     logprob[row] = lp;
-    bc[0] = -l2;
-    bc[1] = c;
+    bc[0] = M;
+    bc[1] = -log2s;
+    bc[2] = c;
+    bc[3] = c * expm1f(lp);  // 0 for a masked token; unused for a bad one
     bci = a;
   }
   __syncthreads();
-  const float nl = bc[0];
-  const float c = bc[1];
+  const float M = bc[0];
+  const float nl2s = bc[1];
+  const float c = bc[2];
+  const float c1 = bc[3];
   const int a = bci;
 
   // ---- pass 2: dz = c (softmax - onehot), in place.  The part re-read from
@@ -178,18 +198,30 @@ __global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 r
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int jj = nvec - 1 - (k + u * kRowThreads);
-      st_l2hint(rowp + jj, dz8(q[u], nl, c, a - 8 * jj), drop);
+      if (!RZ_DCHECK(jj >= nstash && jj < nvec, 20)) continue;
+      st_l2hint(rowp + jj, dz8(q[u], M, nl2s, c, c1, a - 8 * jj), drop);
     }
   }
   for (; k < R; k += kRowThreads) {
     const int jj = nvec - 1 - k;
-    st_l2hint(rowp + jj, dz8(ld_l2hint(rowp + jj, drop), nl, c, a - 8 * jj), drop);
+    st_l2hint(rowp + jj, dz8(ld_l2hint(rowp + jj, drop), M, nl2s, c, c1, a - 8 * jj), drop);
   }
   for (int j = threadIdx.x; j < nstash; j += kRowThreads)
-    st_l2hint(rowp + j, dz8(stash[j], nl, c, a - 8 * j), drop);
+    if (RZ_DCHECK(j < kStashVec && j < nvec, 21))
+      st_l2hint(rowp + j, dz8(stash[j], M, nl2s, c, c1, a - 8 * j), drop);
 }
 
 }  // namespace
+
+cudaError_t check_read_logits(unsigned int* count, int* site) {
+#ifdef RZ_CHECKS
+  return check_read_and_clear(count, site);
+#else
+  *count = 0;
+  *site = 0;
+  return cudaSuccess;
+#endif
+}
 
 cudaError_t launch_logits_rows(uint16_t* logits, int64_t T, int V, const int32_t* tokens,
                                const float* logmu, const int64_t* cu, const float2* fac,

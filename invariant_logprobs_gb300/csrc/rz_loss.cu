@@ -16,6 +16,7 @@
 // over responses with T_i > 0; the first sum is exact for centred rewards
 // and the second keeps full relative precision of the (small) lag term.
 // All reductions run in a fixed order: results are bitwise reproducible.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -24,6 +25,8 @@
 #include "rz_internal.h"
 #include "rz_math.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace rz {
 
 namespace {
@@ -31,6 +34,12 @@ namespace {
 constexpr int kRespThreads = 256;
 constexpr int kFinalThreads = 1024;
 constexpr int kD3Threads = 1024;
+// The whole-call reductions of rz_d3 and rz_is_stats run as one cluster of
+// kStatBlocks CTAs: CTA r reduces tokens r*1024 + k*8192 + lane, then CTA 0
+// adds the CTAs' partial sums in rank order through distributed shared
+// memory.  The split depends on nothing but the token index, so the result
+// is the same on every run.
+constexpr int kStatBlocks = 8;
 
 struct RespPart {
   double lag;   // A_i (1/T_i) sum_t expm1(d_t)
@@ -190,27 +199,48 @@ __global__ void __launch_bounds__(kFinalThreads)
   }
 }
 
-__global__ void __launch_bounds__(kD3Threads)
+__global__ void __cluster_dims__(kStatBlocks, 1, 1) __launch_bounds__(kD3Threads)
     d3_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu, long long T,
               float* d3) {
   __shared__ double red[kD3Threads / 32];
+  __shared__ double part;
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
   float acc = 0.f;
-  for (long long t = threadIdx.x; t < T; t += kD3Threads) acc += d3_term(logpi[t] - logmu[t]);
+  for (long long t = static_cast<long long>(rank) * kD3Threads + threadIdx.x; t < T;
+       t += kStatBlocks * kD3Threads)
+    acc += d3_term(logpi[t] - logmu[t]);
   const double tot = block_sum<double, kD3Threads>(static_cast<double>(acc), red);
-  if (threadIdx.x == 0) *d3 = T > 0 ? static_cast<float>(tot / static_cast<double>(T)) : 0.f;
+  if (threadIdx.x == 0) part = tot;
+  cluster.sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    double sum = 0.0;
+    for (int r = 0; r < kStatBlocks; ++r) sum += *cluster.map_shared_rank(&part, r);
+    *d3 = T > 0 ? static_cast<float>(sum / static_cast<double>(T)) : 0.f;
+  }
+  cluster.sync();  // keep every CTA's partial alive until CTA 0 has read it
 }
 
-// Per-update diagnostics over all T tokens, one block, fixed order:
+// Per-update diagnostics over all T tokens, one cluster, fixed order:
 // out = {D3 (= k3), k1 = mean(-d), k2 = mean(d^2/2), mean w, max w, min w,
 // max |d|}.
-__global__ void __launch_bounds__(kD3Threads)
+struct StatPart {
+  double s3, s1, s2, sw;
+  float wmax, wmin, dmax;
+};
+
+__global__ void __cluster_dims__(kStatBlocks, 1, 1) __launch_bounds__(kD3Threads)
     is_stats_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu,
                     long long T, float* out) {
   __shared__ double red[kD3Threads / 32];
   __shared__ float redf[kD3Threads / 32];
+  __shared__ StatPart part;
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
   float s3 = 0.f, s1 = 0.f, s2 = 0.f, sw = 0.f;
   float wmax = 0.f, wmin = INFINITY, dmax = 0.f;
-  for (long long t = threadIdx.x; t < T; t += kD3Threads) {
+  for (long long t = static_cast<long long>(rank) * kD3Threads + threadIdx.x; t < T;
+       t += kStatBlocks * kD3Threads) {
     const float d = logpi[t] - logmu[t];
     const float w = expf(d);
     s3 += d3_term(d);
@@ -228,16 +258,30 @@ __global__ void __launch_bounds__(kD3Threads)
   const float mx = block_extreme<kD3Threads, true>(wmax, redf);
   const float mn = block_extreme<kD3Threads, false>(wmin, redf);
   const float dm = block_extreme<kD3Threads, true>(dmax, redf);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) part = StatPart{t3, t1, t2, tw, mx, mn, dm};
+  cluster.sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    StatPart a = part;
+    for (int r = 1; r < kStatBlocks; ++r) {
+      const StatPart b = *cluster.map_shared_rank(&part, r);
+      a.s3 += b.s3;
+      a.s1 += b.s1;
+      a.s2 += b.s2;
+      a.sw += b.sw;
+      a.wmax = fmaxf(a.wmax, b.wmax);
+      a.wmin = fminf(a.wmin, b.wmin);
+      a.dmax = fmaxf(a.dmax, b.dmax);
+    }
     const double inv = T > 0 ? 1.0 / static_cast<double>(T) : 0.0;
-    out[0] = static_cast<float>(t3 * inv);
-    out[1] = static_cast<float>(t1 * inv);
-    out[2] = static_cast<float>(t2 * inv);
-    out[3] = static_cast<float>(tw * inv);
-    out[4] = T > 0 ? mx : 0.f;
-    out[5] = T > 0 ? mn : 0.f;
-    out[6] = T > 0 ? dm : 0.f;
+    out[0] = static_cast<float>(a.s3 * inv);
+    out[1] = static_cast<float>(a.s1 * inv);
+    out[2] = static_cast<float>(a.s2 * inv);
+    out[3] = static_cast<float>(a.sw * inv);
+    out[4] = T > 0 ? a.wmax : 0.f;
+    out[5] = T > 0 ? a.wmin : 0.f;
+    out[6] = T > 0 ? a.dmax : 0.f;
   }
+  cluster.sync();  // keep every CTA's partial alive until CTA 0 has read it
 }
 
 __global__ void group_advantage_kernel(const float* __restrict__ r, int B, int G,
@@ -311,13 +355,13 @@ cudaError_t launch_sc_loss(const float* logpi, const int64_t* cu, const uint8_t*
 
 cudaError_t launch_is_stats(const float* logpi, const float* logmu, int64_t T, float* out,
                             cudaStream_t st) {
-  is_stats_kernel<<<1, kD3Threads, 0, st>>>(logpi, logmu, T, out);
+  is_stats_kernel<<<kStatBlocks, kD3Threads, 0, st>>>(logpi, logmu, T, out);
   return cudaGetLastError();
 }
 
 cudaError_t launch_d3(const float* logpi, const float* logmu, int64_t T, float* d3,
                       cudaStream_t st) {
-  d3_kernel<<<1, kD3Threads, 0, st>>>(logpi, logmu, T, d3);
+  d3_kernel<<<kStatBlocks, kD3Threads, 0, st>>>(logpi, logmu, T, d3);
   return cudaGetLastError();
 }
 

@@ -22,3 +22,16 @@ def rz():
     import invariant_logprobs_gb300 as rzmod
     rzmod.load()  # raises if the library is missing: no silent fallback
     return rzmod
+
+
+@pytest.fixture(autouse=True)
+def _device_bounds_checks(request):
+    """With the debug build loaded (RZ_LIB_VARIANT=checks), every GPU test
+    must leave no failed device bounds check behind."""
+    yield
+    if os.environ.get("RZ_LIB_VARIANT") != "checks" or "rz" not in request.fixturenames:
+        return
+    import invariant_logprobs_gb300 as rzmod
+    res = rzmod.rz_debug_check_failures()
+    assert res is not None, "RZ_LIB_VARIANT=checks but the loaded library has no checks"
+    assert res[0] == 0, "failed device bounds checks: %d (first at site %d)" % res

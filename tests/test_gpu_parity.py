@@ -350,3 +350,41 @@ def test_learner_peaked_softmax_vs_oracle(rz, std):
     want = ref["dH"][rows]
     per_row = np.linalg.norm(got - want, axis=1) / np.linalg.norm(want, axis=1)
     assert per_row.max() <= 2e-2, per_row.max()
+
+
+@pytest.mark.parametrize("std", [6.0, 14.0])
+def test_logits_variant_peaked_softmax_vs_oracle(rz, std):
+    """Given logits with standard deviation 6 and 14 and tokens drawn from
+    their own softmax: the sampled token's probability is often close to 1,
+    where log pi is near 0 and dz_a = c (p_a - 1) must keep its digits (the
+    kernel forms c expm1(log pi) there).  Whole-batch parity, and per row for
+    the rows with 1e-4 < 1 - p_a < 0.1."""
+    g = torch.Generator().manual_seed(int(std) + 100)
+    T, V, B = 1200, 151936, 6
+    logits = (torch.randn(T, V, generator=g) * std).to(torch.bfloat16)
+    tok = torch.multinomial(torch.softmax(logits.double(), 1), 1, generator=g)
+    tok = tok.squeeze(1).to(torch.int32)
+    cu = torch.linspace(0, T, B + 1).round().to(torch.int64)
+    adv = torch.randn(B, generator=g)
+    lp64 = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), np.zeros(T), f64(cu), f64(adv),
+                                      rows=np.zeros(0, np.int64))["logpi"]
+    logmu = torch.tensor(lp64, dtype=torch.float32) + torch.randn(T, generator=g) * 0.05
+    ref = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), f64(logmu), f64(cu), f64(adv))
+    buf = logits.to(DEV)
+    out = rz.rz_logits_loss_fwd_bwd(buf, tok.to(DEV), logmu.to(DEV), cu.to(DEV), adv.to(DEV))
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(out["logprob"]) - ref["logpi"])) <= TOL_LOGPI
+    assert scalar_close(out["loss"].item(), ref["loss"]), (out["loss"].item(), ref["loss"])
+    assert scalar_close(out["d3"].item(), ref["d3"]), (out["d3"].item(), ref["d3"])
+    dz = f64(buf)
+    assert rel_l2(dz, ref["dz"]) <= TOL_GRAD_REL_L2
+    gap = -np.expm1(ref["logpi"])                        # 1 - p_a
+    rows = np.nonzero((gap > 1e-4) & (gap < 0.1))[0]
+    assert len(rows) >= 20, len(rows)
+    per_row = np.linalg.norm(dz[rows] - ref["dz"][rows], axis=1) / \
+        np.linalg.norm(ref["dz"][rows], axis=1)
+    assert per_row.max() <= 2e-2, per_row.max()
+    # the sampled column itself, where the old p - 1 form lost its digits
+    a_got = dz[rows, f64(tok)[rows]]
+    a_want = ref["dz"][rows, f64(tok)[rows]]
+    assert np.max(np.abs(a_got - a_want) / np.abs(a_want)) <= 2e-2
