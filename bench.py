@@ -145,6 +145,25 @@ def barrier(world):
         dist.barrier()
 
 
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
+
+
+def gather_over_ranks(x, world):
+    if world == 1:
+        return [x]
+    import torch.distributed as dist
+    out = [None] * world
+    dist.all_gather_object(out, x)
+    return out
+
+
 def max_over_ranks(x, world):
     if world == 1:
         return x
@@ -314,12 +333,38 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     d3 = torch.empty(1, dtype=torch.float32, device=dev)
     adv = torch.empty(B, dtype=torch.float32, device=dev)
     err = rz.new_err_flag(dev)
+    # data-parallel over responses: each rank holds B of the batch's
+    # B * world responses, normalises by the batch's count and joins the one
+    # exchange step (dW in rank order, the loss share and D3 per rank)
+    B_total = B * world
+    ex_ev = []
+    scal = torch.empty(2, dtype=torch.float32, device=dev)
+    gathered = torch.empty((world, 2), dtype=torch.float32, device=dev)
+    state = {"dW_sum": dW}
+
+    def exchange():
+        from invariant_logprobs_gb300 import shard
+        import torch.distributed as dist
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        state["dW_sum"] = shard.fixed_order_allreduce(dW, rz.rz_sum_partials)
+        scal[0:1].copy_(loss)
+        scal[1:2].copy_(d3)
+        dist.all_gather_into_tensor(gathered.view(-1), scal)
+        e1.record(stream)
+        ex_ev.append((e0, e1))
 
     def step():
         rz.rz_group_advantage(b["rewards"], b["G"], adv_out=adv)
-        rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
-                           logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
-                           err_flag=err)
+        if world == 1:
+            rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
+                               logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
+                               err_flag=err)
+        else:
+            rz.rz_loss_fwd_bwd_shard(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
+                                     B_total, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
+                                     d3_out=d3, ws=ws, err_flag=err)
+            exchange()
 
     for _ in range(warmup):
         step()
@@ -339,12 +384,15 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     barrier(world)
     per_step = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
+    exchange_ms = (statistics.mean(a.elapsed_time(z) for a, z in ex_ev[-steps:])
+                   if world > 1 else None)
 
     # the step split by kernel class: two more (untimed) steps with the
     # library's launch-class timing on (CUDA events on the launching stream)
     breakdown = profile_steps(rz, step, stream, 2)
     ms = max_over_ranks(total_ms / steps, world)
-    value = T * world / (ms / 1e3)
+    T_all = sum_over_ranks(T, world)
+    value = T_all / (ms / 1e3)
     flop_alg = 6.0 * d * V * T
     keep_ms, keep_launches = breakdown["classes"]["keep_gemm"]["ms"], \
         breakdown["classes"]["keep_gemm"]["launches"]
@@ -358,10 +406,11 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
         "steps": steps, "warmup": warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload, random-init weights)",
-        "config": {"workload": wl.name, "tokens_per_step": T, "responses": B, "group": wl.group,
-                   "d": d, "V": V, "lag_steps": wl.drift_steps,
+        "config": {"workload": wl.name, "tokens_per_step": T_all, "responses": B_total,
+                   "group": wl.group, "d": d, "V": V, "lag_steps": wl.drift_steps,
                    "l2": "inputs larger than L2 (H %.1f GB), no flush" % (T * d * 2 / 1e9),
-                   "parallelism": "dp%d replicas" % world},
+                   "parallelism": ("dp%d over responses, dW exchanged in rank order every step"
+                                   % world) if world > 1 else "dp1"},
         "step_ms_median": statistics.median(per_step),
         "algorithmic_tflops": flop_alg / (ms / 1e3) / 1e12,
         "algorithmic_frac_of_sustained_bf16": flop_alg / (ms / 1e3) / 1e12 /
@@ -389,10 +438,20 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
             38912 * (2 * ((V + 7) // 8 * 8) + 4 * ((V + 127) // 128 * 4)) +
             rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 38912, d, V, 0)},
         "step_breakdown": breakdown,
-        "gpu_launches": steps * launches_per_step(T, V),
+        "gpu_launches": steps * (launches_per_step(T, V) + (1 if world > 1 else 0)),
         "device_err_flag": int(err.item()),
         "loss": float(loss.item()), "d3": float(d3.item()),
     }
+    if world > 1:
+        g = gathered.double().cpu()
+        T_r = gather_over_ranks(T, world)
+        out["exchange"] = {
+            "ms_per_step": exchange_ms, "share_of_step": exchange_ms / ms,
+            "what": "dW [V, d] fp32 added in rank order (NCCL all-to-all of 1/N slices, "
+                    "rz_sum_partials, NCCL all-gather) + the loss shares and D3 of every rank",
+            "bytes_per_rank": 2.0 * (world - 1) / world * V * d * 4}
+        out["loss"] = float(g[:, 0].sum())
+        out["d3"] = float(sum(g[r, 1] * T_r[r] for r in range(world)) / sum(T_r))
     if not full:
         return out
 
@@ -428,7 +487,8 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     out["clocks"] = clk.stop()
 
     # end to end through the public API from pinned host buffers
-    out["e2e"] = run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err)
+    out["e2e"] = run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err,
+                         B_total if world > 1 else None, exchange)
     roll_tf = 2.0 * d * V * T / (roll_ms / 1e3) / 1e12
     out["rollout_gemm"] = {
         "kernel": "gemm_kernel<EpiLsePartial> (rollout logprob GEMM via rz_token_logprob)",
@@ -529,7 +589,8 @@ def launches_per_step(T, V):
     return 1 + 1 + 5 * n_chunks + 2
 
 
-def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err):
+def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err, B_total=None,
+            exchange=None):
     """The learner step through the public API from pinned host buffers:
     every step copies its inputs (H, tokens, log mu, cu_seqlens, rewards)
     host -> device and reads its loss and D3 back.  Two device input slots
@@ -556,9 +617,15 @@ def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err):
         stream.wait_event(copied[i])
         x = slots[i]
         rz.rz_group_advantage(x["rewards"], b["G"], adv_out=adv)
-        rz.rz_loss_fwd_bwd(x["H"], b["W"], x["tokens"], x["logmu"], x["cu"], adv,
-                           logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
-                           err_flag=err)
+        if B_total is None:
+            rz.rz_loss_fwd_bwd(x["H"], b["W"], x["tokens"], x["logmu"], x["cu"], adv,
+                               logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
+                               err_flag=err)
+        else:  # one shard of the data-parallel step, then the exchange
+            rz.rz_loss_fwd_bwd_shard(x["H"], b["W"], x["tokens"], x["logmu"], x["cu"], adv,
+                                     B_total, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
+                                     d3_out=d3, ws=ws, err_flag=err)
+            exchange()
         consumed[i].record(stream)
         res[0:1].copy_(loss, non_blocking=True)
         res[1:2].copy_(d3, non_blocking=True)

@@ -230,6 +230,47 @@ RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* to
                     rz_stream_t stream);
 
 /*
+ * One shard of a data-parallel learner step [RZ-page s.04: the method runs on
+ * 16 GPUs].  The loss averages tokens within a response and responses within
+ * the batch (s.02 objective), so the batch is split over ranks by whole
+ * responses: this call gets B of the batch's B_total responses (contiguous;
+ * cu_seqlens, adv, tokens, ... are the shard's own) and normalises by B_total:
+ *   c_t = A_i w_t / (B_total T_i),
+ *   loss_out = -(1/B_total) sum_{i in shard} A_i (1/T_i) sum_t w_t  (the shard's
+ *              share: the batch's loss is the sum over shards),
+ *   d3_out   = the mean of w - 1 - log w over the shard's valid tokens (the
+ *              batch's D3 is the token-weighted mean over shards),
+ *   dH       = the shard's rows of the batch's dH, bitwise what one
+ *              rz_loss_fwd_bwd call over the whole batch gives for them,
+ *   dW       = the shard's partial; the batch's dW is the sum of the partials
+ *              over shards (add them in a fixed order, e.g. with
+ *              rz_sum_partials, for a result independent of the backend).
+ * Everything else (arguments, layouts, workspace RZ_OP_LOSS_FWD_BWD with the
+ * shard's B, errors) as rz_loss_fwd_bwd; B_total = B is rz_loss_fwd_bwd.
+ * B_total < B returns RZ_ERR_INVALID_ARG.
+ */
+RZ_API int rz_loss_fwd_bwd_shard(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                                 const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                                 const uint8_t* action_mask,
+                                 int32_t B, int32_t B_total, int64_t T, int32_t d, int32_t V,
+                                 float* loss_out, float* d3_out, float* logprob_out,
+                                 rz_bf16* dH, float* dW,
+                                 void* ws, size_t ws_bytes, int32_t* err_flag,
+                                 rz_stream_t stream);
+
+/*
+ * The exchange step of the data-parallel learner: the fixed-order sum of n
+ * partials.  parts [n_parts, count] fp32 (device, row r = rank r's partial,
+ * e.g. gathered by a collective), out [count] fp32 (device; may not overlap
+ * parts):  out[i] = ((parts[0][i] + parts[1][i]) + parts[2][i]) + ..., added
+ * in row order in fp32, so every rank that sums the same gathered partials
+ * gets the same bits, independent of any collective's own reduction order.
+ * No workspace.  n_parts >= 1.
+ */
+RZ_API int rz_sum_partials(const float* parts, int32_t n_parts, int64_t count, float* out,
+                           rz_stream_t stream);
+
+/*
  * Comparison estimator: Score Centering (SC), the learner step WITHOUT
  * importance weights ["REINFORCE Zero" project page, "The full IS
  * correction", items 02-03: the update on sampler tokens carries the drift

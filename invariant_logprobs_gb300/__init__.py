@@ -57,6 +57,9 @@ _SIGNATURES = {
     "rz_d3": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
     "rz_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
                                        _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_loss_fwd_bwd_shard": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I64, _I32,
+                                             _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_sum_partials": (ctypes.c_int, [_P, _I32, _I64, _P, _P]),
     "rz_sc_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
                                           _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_logits_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32,
@@ -292,6 +295,45 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
                     want_logprob=True, action_mask=None):
     """Learner-side fused logprob + loss forward/backward (see include/rz.h).
     Returns dict(loss, d3, logprob, dH, dW) of device tensors."""
+    return _learner(None, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW, loss_out,
+                    d3_out, ws, err_flag, stream, want_logprob, action_mask)
+
+
+def rz_loss_fwd_bwd_shard(H, W, tokens, logmu, cu_seqlens, adv, B_total, logprob_out=None,
+                          dH=None, dW=None, loss_out=None, d3_out=None, ws=None, err_flag=None,
+                          stream=None, want_logprob=True, action_mask=None):
+    """One shard (contiguous whole responses) of a data-parallel learner step,
+    normalised by the batch's B_total responses (see include/rz.h).  Returns
+    dict(loss, d3, logprob, dH, dW): the shard's loss share, its D3, its dH
+    rows and its dW partial."""
+    load()
+    return _learner(int(B_total), H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
+                    loss_out, d3_out, ws, err_flag, stream, want_logprob, action_mask)
+
+
+def rz_sum_partials(parts, out=None, stream=None):
+    """out[i] = parts[0][i] + parts[1][i] + ... in row order (fp32): the
+    fixed-order sum of the data-parallel exchange.  parts: [n, ...] fp32."""
+    torch = _torch()
+    lib = load()
+    _need(parts, torch.float32, "parts")
+    if parts.dim() < 1 or parts.shape[0] < 1:
+        raise ValueError("parts must have a leading rank dimension of at least 1")
+    shape = tuple(parts.shape[1:])
+    count = 1
+    for x in shape:
+        count *= int(x)
+    _out(out, torch.float32, "out", shape)
+    _same_device(parts, out)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=parts.device)
+    st = lib.rz_sum_partials(_ptr(parts), int(parts.shape[0]), count, _ptr(out), _stream(stream))
+    _check("rz_sum_partials", st)
+    return out
+
+
+def _learner(B_total, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW, loss_out,
+             d3_out, ws, err_flag, stream, want_logprob, action_mask):
     torch = _torch()
     lib = load()
     _need(H, torch.bfloat16, "H")
@@ -331,11 +373,20 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
         ws = alloc_workspace(RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
     if action_mask is not None:
         _need(action_mask, torch.uint8, "action_mask")
-    st = lib.rz_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(cu_seqlens),
-                             _ptr(adv), _ptr(action_mask), B, T, d, V, _ptr(loss_out), _ptr(d3_out),
-                             _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws), _ws_bytes(ws),
-                             _ptr(err_flag), _stream(stream))
-    _check("rz_loss_fwd_bwd", st)
+    if B_total is None:
+        name = "rz_loss_fwd_bwd"
+        st = lib.rz_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(cu_seqlens),
+                                 _ptr(adv), _ptr(action_mask), B, T, d, V, _ptr(loss_out),
+                                 _ptr(d3_out), _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws),
+                                 _ws_bytes(ws), _ptr(err_flag), _stream(stream))
+    else:
+        name = "rz_loss_fwd_bwd_shard"
+        st = lib.rz_loss_fwd_bwd_shard(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu),
+                                       _ptr(cu_seqlens), _ptr(adv), _ptr(action_mask), B,
+                                       B_total, T, d, V, _ptr(loss_out), _ptr(d3_out),
+                                       _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws),
+                                       _ws_bytes(ws), _ptr(err_flag), _stream(stream))
+    _check(name, st)
     return {"loss": loss_out, "d3": d3_out, "logprob": logprob_out, "dH": dH, "dW": dW}
 
 

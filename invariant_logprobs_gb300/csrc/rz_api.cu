@@ -145,12 +145,15 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
 
 // The learner step shared by the IS loss and, with sc set, the Score
 // Centering loss (no weight, advantages centred, no log mu, no D3).
+// Bn is the response count the loss averages over: B, or the whole batch's
+// count when this call holds one shard of it (rz_loss_fwd_bwd_shard).
 int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
                  const float* logmu, const int64_t* cu_seqlens, const float* adv,
-                 const uint8_t* action_mask, int32_t B, int64_t T, int32_t d, int32_t V,
+                 const uint8_t* action_mask, int32_t B, int32_t Bn, int64_t T, int32_t d,
+                 int32_t V,
                  float* loss_out, float* d3_out, float* logprob_out, rz_bf16* dH, float* dW,
                  void* ws, size_t ws_bytes, int32_t* err_flag, cudaStream_t st) {
-  if (!sizes_ok(T, d, V) || B < 0 || (B == 0 && T > 0)) return RZ_ERR_INVALID_ARG;
+  if (!sizes_ok(T, d, V) || B < 0 || (B == 0 && T > 0) || Bn < B) return RZ_ERR_INVALID_ARG;
   if (!W || !dW || !loss_out || !cu_seqlens) return RZ_ERR_INVALID_ARG;
   if (T > 0 && (!H || !tokens || !dH)) return RZ_ERR_INVALID_ARG;
   if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
@@ -166,11 +169,11 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
     ProfScope ps(RZ_PROF_SMALL, sc ? 3 : 2, st);
     RZ_TRY(cudaMemsetAsync(dW, 0, size_t(V) * size_t(d) * sizeof(float), st));
     if (sc) {
-      RZ_TRY(launch_resp_factors(cu_seqlens, adv, nullptr, B, 0, fac, st));
+      RZ_TRY(launch_resp_factors(cu_seqlens, adv, nullptr, B, Bn, 0, fac, st));
       RZ_TRY(launch_sc_loss(nullptr, cu_seqlens, nullptr, fac, B, 0, loss_out, w8 + L.resp,
                             err_flag, st));
     } else {
-      RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, nullptr, B, 0, loss_out, d3_out,
+      RZ_TRY(launch_is_loss(nullptr, nullptr, cu_seqlens, adv, nullptr, B, Bn, 0, loss_out, d3_out,
                             nullptr, w8 + L.resp, err_flag, st));
     }
     return RZ_OK;
@@ -195,7 +198,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   // (Score Centering: A_i - Abar).
   {
     ProfScope ps(RZ_PROF_SMALL, sc ? 2 : 1, st);
-    RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+    RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, Bn, T, fac, st));
     if (sc) RZ_TRY(launch_sc_centre(fac, B, st));
   }
 
@@ -242,7 +245,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
     RZ_TRY(launch_sc_loss(logpi, cu_seqlens, action_mask, fac, B, T, loss_out, w8 + L.resp,
                           err_flag, st));
   } else {
-    RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
+    RZ_TRY(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, Bn, T, loss_out, d3_out,
                           nullptr, w8 + L.resp, err_flag, st));
   }
   return RZ_OK;
@@ -343,7 +346,7 @@ int rz_is_loss(const float* logpi, const float* logmu, const int64_t* cu_seqlens
   if (need > 0 && (!ws || ws_bytes < need || !a256(ws))) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   ProfScope ps(RZ_PROF_SMALL, 2, reinterpret_cast<cudaStream_t>(stream));
-  return cuda_status(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, T, loss_out,
+  return cuda_status(launch_is_loss(logpi, logmu, cu_seqlens, adv, action_mask, B, B, T, loss_out,
                                     d3_out, coef_out, ws, err_flag,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -381,9 +384,33 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
                     float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
                     int32_t* err_flag, rz_stream_t stream) {
   if (!d3_out || (T > 0 && !logmu)) return RZ_ERR_INVALID_ARG;
-  return learner_step(false, H, W, tokens, logmu, cu_seqlens, adv, action_mask, B, T, d, V,
+  return learner_step(false, H, W, tokens, logmu, cu_seqlens, adv, action_mask, B, B, T, d, V,
                       loss_out, d3_out, logprob_out, dH, dW, ws, ws_bytes, err_flag,
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int rz_loss_fwd_bwd_shard(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                          const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                          const uint8_t* action_mask, int32_t B, int32_t B_total, int64_t T,
+                          int32_t d, int32_t V, float* loss_out, float* d3_out,
+                          float* logprob_out, rz_bf16* dH, float* dW, void* ws,
+                          size_t ws_bytes, int32_t* err_flag, rz_stream_t stream) {
+  if (!d3_out || (T > 0 && !logmu) || B_total < B || (B_total == 0 && B > 0))
+    return RZ_ERR_INVALID_ARG;
+  return learner_step(false, H, W, tokens, logmu, cu_seqlens, adv, action_mask, B, B_total, T,
+                      d, V, loss_out, d3_out, logprob_out, dH, dW, ws, ws_bytes, err_flag,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int rz_sum_partials(const float* parts, int32_t n_parts, int64_t count, float* out,
+                    rz_stream_t stream) {
+  if (n_parts < 1 || count < 0) return RZ_ERR_INVALID_ARG;
+  if (count == 0) return RZ_OK;
+  if (!parts || !out) return RZ_ERR_INVALID_ARG;
+  if (!device_ok()) return RZ_ERR_UNSUPPORTED;
+  ProfScope ps(RZ_PROF_SMALL, 1, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(
+      launch_sum_partials(parts, n_parts, count, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int rz_sc_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
@@ -391,7 +418,7 @@ int rz_sc_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens
                        int32_t B, int64_t T, int32_t d, int32_t V, float* loss_out,
                        float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
                        int32_t* err_flag, rz_stream_t stream) {
-  return learner_step(true, H, W, tokens, nullptr, cu_seqlens, adv, action_mask, B, T, d, V,
+  return learner_step(true, H, W, tokens, nullptr, cu_seqlens, adv, action_mask, B, B, T, d, V,
                       loss_out, nullptr, logprob_out, dH, dW, ws, ws_bytes, err_flag,
                       reinterpret_cast<cudaStream_t>(stream));
 }
@@ -415,7 +442,7 @@ int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const f
   float2* fac = reinterpret_cast<float2*>(w8 + is_loss_ws_bytes(B));
   {
     ProfScope ps(RZ_PROF_SMALL, 1, st);
-    RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, T, fac, st));
+    RZ_TRY(launch_resp_factors(cu_seqlens, adv, action_mask, B, B, T, fac, st));
   }
   {
     ProfScope ps(RZ_PROF_LOGITS_ROWS, 1, st);
@@ -423,7 +450,7 @@ int rz_logits_loss_fwd_bwd(rz_bf16* logits_inout, const int32_t* tokens, const f
                               logprob_out, err_flag, st));
   }
   ProfScope ps(RZ_PROF_SMALL, 2, st);
-  RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, action_mask, B, T, loss_out, d3_out,
+  RZ_TRY(launch_is_loss(logprob_out, logmu, cu_seqlens, adv, action_mask, B, B, T, loss_out, d3_out,
                         nullptr, ws, err_flag, st));
   return RZ_OK;
 }

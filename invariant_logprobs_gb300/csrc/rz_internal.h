@@ -117,13 +117,19 @@ cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64
 // ---- loss kernels (rz_loss.cu)
 size_t is_loss_ws_bytes(int32_t B);
 cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cudaStream_t st);
+// Bn: the number of responses the loss averages over (B, or the whole
+// batch's count when the call holds one shard of it).
 cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
-                           const float* adv, const uint8_t* mask, int B, int64_t T, float* loss,
-                           float* d3, float* coef, void* ws, int* err, cudaStream_t st);
-// Per-response factors (A_i, 1/(B T_i)) of the coefficient c_t = A_i w_t/(B T_i).
+                           const float* adv, const uint8_t* mask, int B, int Bn, int64_t T,
+                           float* loss, float* d3, float* coef, void* ws, int* err,
+                           cudaStream_t st);
+// Per-response factors (A_i, 1/(Bn T_i)) of the coefficient c_t = A_i w_t/(Bn T_i).
 size_t resp_factors_ws_bytes(int32_t B);
 cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
-                                int64_t T, float2* fac, cudaStream_t st);
+                                int Bn, int64_t T, float2* fac, cudaStream_t st);
+// out[i] = parts[0][i] + parts[1][i] + ... in that order (n_parts >= 1).
+cudaError_t launch_sum_partials(const float* parts, int n_parts, int64_t count, float* out,
+                                cudaStream_t st);
 // Score Centering: fac[i].x -= mean of A over responses with fac[i].y > 0;
 // the loss from log pi (ws: is_loss_ws_bytes(B)).
 cudaError_t launch_sc_centre(float2* fac, int B, cudaStream_t st);

@@ -60,7 +60,7 @@ __device__ __forceinline__ long long valid_count(const uint8_t* mask, long long 
 __global__ void __launch_bounds__(kRespThreads)
     is_loss_resp_kernel(const float* __restrict__ logpi, const float* __restrict__ logmu,
                         const int64_t* __restrict__ cu, const float* __restrict__ adv,
-                        const uint8_t* __restrict__ mask, int B, long long T,
+                        const uint8_t* __restrict__ mask, int B, int Bn, long long T,
                         float* __restrict__ coef, RespPart* __restrict__ part, int* err) {
   __shared__ float red[kRespThreads / 32];
   __shared__ int redi[kRespThreads / 32];
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kRespThreads)
   __syncthreads();
   const long long Ti = nvalid;
   const float A = adv[i];
-  const float inv_bt = Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f;
+  const float inv_bt = Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(Bn) * Ti)) : 0.f;
   float em1 = 0.f, d3s = 0.f;
   for (long long t = s + threadIdx.x; t < e; t += kRespThreads) {
     const bool ok = !mask || mask[t] != 0;
@@ -104,11 +104,13 @@ __global__ void __launch_bounds__(kRespThreads)
   }
 }
 
-// Per-response factors (A_i, 1/(B T_i)) (second 0 for an empty response), from
-// which the learner and the given-logits kernel form c_t = A_i w_t (1/(B T_i))
-// with the same rounding as is_loss_resp_kernel's coefficient.
+// Per-response factors (A_i, 1/(Bn T_i)) (second 0 for an empty response),
+// from which the learner and the given-logits kernel form
+// c_t = A_i w_t (1/(Bn T_i)) with the same rounding as is_loss_resp_kernel's
+// coefficient.  Bn is the number of responses the loss averages over: B, or
+// the whole batch's count when this call holds one shard of it.
 __global__ void resp_factors_kernel(const int64_t* __restrict__ cu, const float* __restrict__ adv,
-                                    const uint8_t* __restrict__ mask, int B, long long T,
+                                    const uint8_t* __restrict__ mask, int Bn, long long T,
                                     float2* __restrict__ fac) {
   __shared__ int redi[kRespThreads / 32];
   const int i = blockIdx.x;
@@ -119,7 +121,7 @@ __global__ void resp_factors_kernel(const int64_t* __restrict__ cu, const float*
   const long long Ti = valid_count(mask, s, e, redi);
   if (threadIdx.x == 0)
     fac[i] = make_float2(adv[i],
-                         Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(B) * Ti)) : 0.f);
+                         Ti > 0 ? static_cast<float>(1.0 / (static_cast<double>(Bn) * Ti)) : 0.f);
 }
 
 // Score Centering: Abar = mean of A_i over the responses with valid tokens
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(kFinalThreads)
 }
 
 __global__ void __launch_bounds__(kFinalThreads)
-    is_loss_final_kernel(const RespPart* __restrict__ part, int B, float* loss, float* d3) {
+    is_loss_final_kernel(const RespPart* __restrict__ part, int B, int Bn, float* loss,
+                         float* d3) {
   __shared__ double red[kFinalThreads / 32];
   double lag = 0.0, base = 0.0, dd = 0.0, cnt = 0.0;
   for (int i = threadIdx.x; i < B; i += kFinalThreads) {
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kFinalThreads)
   const double d3_t = block_sum<double, kFinalThreads>(dd, red);
   const double cnt_t = block_sum<double, kFinalThreads>(cnt, red);
   if (threadIdx.x == 0) {
-    if (loss) *loss = B > 0 ? static_cast<float>(-(base_t + lag_t) / B) : 0.f;
+    if (loss) *loss = Bn > 0 ? static_cast<float>(-(base_t + lag_t) / Bn) : 0.f;
     if (d3) *d3 = cnt_t > 0 ? static_cast<float>(d3_t / cnt_t) : 0.f;
   }
 }
@@ -309,16 +312,17 @@ cudaError_t launch_group_advantage(const float* r, int B, int G, float* adv, cud
 }
 
 cudaError_t launch_is_loss(const float* logpi, const float* logmu, const int64_t* cu,
-                           const float* adv, const uint8_t* mask, int B, int64_t T, float* loss,
-                           float* d3, float* coef, void* ws, int* err, cudaStream_t st) {
+                           const float* adv, const uint8_t* mask, int B, int Bn, int64_t T,
+                           float* loss, float* d3, float* coef, void* ws, int* err,
+                           cudaStream_t st) {
   RespPart* part = static_cast<RespPart*>(ws);
   if (B > 0) {
-    is_loss_resp_kernel<<<B, kRespThreads, 0, st>>>(logpi, logmu, cu, adv, mask, B, T, coef,
+    is_loss_resp_kernel<<<B, kRespThreads, 0, st>>>(logpi, logmu, cu, adv, mask, B, Bn, T, coef,
                                                     part, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, loss, d3);
+  is_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, B, Bn, loss, d3);
   return cudaGetLastError();
 }
 
@@ -328,9 +332,9 @@ size_t resp_factors_ws_bytes(int32_t B) {
 }
 
 cudaError_t launch_resp_factors(const int64_t* cu, const float* adv, const uint8_t* mask, int B,
-                                int64_t T, float2* fac, cudaStream_t st) {
+                                int Bn, int64_t T, float2* fac, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
-  resp_factors_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, B, T, fac);
+  resp_factors_kernel<<<B, kRespThreads, 0, st>>>(cu, adv, mask, Bn, T, fac);
   return cudaGetLastError();
 }
 
@@ -350,6 +354,54 @@ cudaError_t launch_sc_loss(const float* logpi, const int64_t* cu, const uint8_t*
     if (e != cudaSuccess) return e;
   }
   sc_loss_final_kernel<<<1, kFinalThreads, 0, st>>>(part, fac, B, loss);
+  return cudaGetLastError();
+}
+
+namespace {
+// The fixed-order sum of the data-parallel exchange: element i of the output
+// is parts[0][i] + parts[1][i] + ... + parts[n-1][i], added left to right in
+// fp32, so every rank that runs it on the same gathered partials gets the
+// same bits.  Four elements per thread when the rows allow 16-byte access.
+__global__ void sum_partials_kernel(const float* __restrict__ parts, int n, long long count,
+                                    float* __restrict__ out) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if ((count & 3) == 0 && (reinterpret_cast<uintptr_t>(parts) & 15u) == 0 &&
+      (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+    const long long n4 = count >> 2;
+    const float4* p4 = reinterpret_cast<const float4*>(parts);
+    float4* o4 = reinterpret_cast<float4*>(out);
+    for (long long i = i0; i < n4; i += stride) {
+      float4 a = __ldcs(p4 + i);
+      for (int r = 1; r < n; ++r) {
+        const float4 b = __ldcs(p4 + static_cast<long long>(r) * n4 + i);
+        a.x = __fadd_rn(a.x, b.x);
+        a.y = __fadd_rn(a.y, b.y);
+        a.z = __fadd_rn(a.z, b.z);
+        a.w = __fadd_rn(a.w, b.w);
+      }
+      __stcs(o4 + i, a);
+    }
+  } else {
+    for (long long i = i0; i < count; i += stride) {
+      float a = parts[i];
+      for (int r = 1; r < n; ++r) a = __fadd_rn(a, parts[static_cast<long long>(r) * count + i]);
+      out[i] = a;
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_sum_partials(const float* parts, int n_parts, int64_t count, float* out,
+                                cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (count / 4 + threads - 1) / threads;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  sum_partials_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(parts, n_parts, count,
+                                                                        out);
   return cudaGetLastError();
 }
 

@@ -13,9 +13,19 @@ same way, so dW = sum_r dW_r and each rank's dH is final.  D3 is a token
 mean: D3 = sum_r D3_r T_r / T.
 
 Only the sums cross ranks (dW, and two scalars), which is the one exchange
-step of the path.  Its order is fixed: fixed_order_sum gathers every rank's
-partial and adds them in rank order, so dW is bitwise the same on every rank
-and from run to run, whatever order the backend's own all-reduce would use.
+step of the path.  Its order is fixed: every element of dW is added in rank
+order 0, 1, ..., N-1, so dW is bitwise the same on every rank and from run to
+run, whatever order a backend's own all-reduce would use.  fixed_order_sum
+gathers all partials on every rank; fixed_order_allreduce moves 2(N-1)/N of
+the tensor per rank instead of N-1 copies: each rank receives one slice of
+every rank's partial (all-to-all), adds them in rank order (the caller's
+`sum_parts`, on the GPU the library's rz_sum_partials kernel) and the summed
+slices are all-gathered.
+
+On the GPU each rank calls rz_loss_fwd_bwd_shard with its own responses
+and the batch's response count (so its dH rows are final and bitwise the
+unsharded call's); scaling the advantages by B_r / B (advantage_scale) and
+calling rz_loss_fwd_bwd gives the same step up to rounding.
 """
 
 import numpy as np
@@ -77,3 +87,34 @@ def fixed_order_sum(t, group=None):
     for part in parts[1:]:
         out += part
     return out
+
+
+def fixed_order_allreduce(t, sum_parts, group=None):
+    """Sum of tensor t over the ranks of `group`, every element added in rank
+    order 0..N-1, bitwise the same on every rank as fixed_order_sum gives.
+
+    Element range j (of N about equal ranges) is owned by rank j: an
+    all-to-all hands rank j range j of every rank's partial as the rows of
+    an [N, n_j] tensor, sum_parts adds the rows in row order, and an
+    all-gather returns every owner's sum to every rank.  sum_parts(parts)
+    -> parts[0] + parts[1] + ... (left to right) is the only arithmetic; on
+    CUDA tensors pass the library's rz_sum_partials."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    flat = t.contiguous().view(-1)
+    if world == 1:
+        return sum_parts(flat.view(1, -1)).view_as(t)
+    n = flat.numel()
+    per = -(-n // world)
+    per = -(-per // 4) * 4  # 16-byte rows for the sum kernel
+    send = flat
+    if per * world != n:
+        send = torch.cat([flat, flat.new_zeros(per * world - n)])
+    recv = torch.empty(world * per, dtype=flat.dtype, device=flat.device)
+    dist.all_to_all_single(recv, send, group=group)
+    mine = sum_parts(recv.view(world, per)).contiguous()
+    out = torch.empty(world * per, dtype=flat.dtype, device=flat.device)
+    dist.all_gather_into_tensor(out, mine, group=group)
+    return out[:n].view_as(t)
+

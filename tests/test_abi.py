@@ -125,6 +125,20 @@ def test_host_side_argument_checks(lib):
     assert lib.rz_is_loss(fake, fake, fake, fake, null, 2, 10, null, fake, null, fake, 1 << 20,
                           null, null) == 1
     assert lib.rz_d3(fake, fake, -1, fake, null) == 1
+    # shard of a data-parallel step: the batch cannot hold fewer responses
+    # than the shard, nor none when the shard has some
+    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, fake, fake, null, 4, 3, 5, 16, 100,
+                                     fake, fake, null, fake, fake, fake, 1 << 30, null, null) == 1
+    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, fake, fake, null, 4, 0, 5, 16, 100,
+                                     fake, fake, null, fake, fake, fake, 1 << 30, null, null) == 1
+    # ... and is otherwise checked as rz_loss_fwd_bwd (d % 8 answers 2)
+    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, fake, fake, null, 4, 8, 5, 12, 100,
+                                     fake, fake, null, fake, fake, null, 0, null, null) == 2
+    # the exchange sum: at least one part, non-negative count, pointers
+    assert lib.rz_sum_partials(fake, 0, 10, fake, null) == 1
+    assert lib.rz_sum_partials(fake, 2, -1, fake, null) == 1
+    assert lib.rz_sum_partials(null, 2, 10, fake, null) == 1
+    assert lib.rz_sum_partials(null, 2, 0, null, null) == 0  # nothing to add
 
 
 def test_valid_call_without_gpu_reports_unsupported(lib):
