@@ -36,7 +36,10 @@ GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_m
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 TRAFFIC_CAPTURES = {
     # learner logits+LSE keep GEMM, one 38,912-row chunk at the 4B shape
-    "qwen4b_lag64": {"bytes": None, "sources": GEMM_SOURCES, "sources_sha256_16": None},
+    # (1.286 GB read + 3.120 GB written at 9,728 rows, one raster group of
+    # 76 m-blocks; a 38,912-row chunk is four such groups: x4)
+    "qwen4b_lag64": {"bytes": 4 * (1.286006e9 + 3.119965e9), "sources": GEMM_SOURCES,
+                     "sources_sha256_16": "6abae3cf0a78d27c"},
     # given-logits row kernel over the 262,144-row MoE-shaped workload
     "moe30b_logits": {"bytes": 106.960e9 + 79.575e9, "sources": LOGITS_SOURCES,
                       "sources_sha256_16": "d67650bec883fd47"},

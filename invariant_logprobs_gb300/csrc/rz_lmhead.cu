@@ -169,7 +169,10 @@ struct EpiLseKeep {
     const int rbase = m_blk * kBM + (row & ~31);
     const uint64_t pol = l2_policy_first();
     uint4* mine = reinterpret_cast<uint4*>(stage + lane * 128);
-#pragma unroll 1
+    float mt[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) mt[q] = 0.f;
+#pragma unroll
     for (int c = 0; c < kBN; c += 64) {
       if (col0 + c >= V) break;  // warp-uniform
       uint32_t r0[32], r1[32];
@@ -184,15 +187,8 @@ struct EpiLseKeep {
         chunk(p, st, r1, col0 + c + 32, w + 16);
         m1 = st.m;
       }
-      if (grow < p.lse.T &&
-          RZ_DCHECK(grow >= 0 && ((col0 + c) >> 5) + (col0 + c + 32 < V ? 2 : 1) <= p.ldm, 11)) {
-        float* em = p.emax + grow * p.ldm + ((col0 + c) >> 5);
-        if (col0 + c + 32 < V) {
-          *reinterpret_cast<float2*>(em) = make_float2(m0, m1);
-        } else {
-          em[0] = m0;
-        }
-      }
+      mt[(c >> 5)] = m0;
+      mt[(c >> 5) + 1] = m1;
       if (lane == 0) bulk_wait_read();  // the previous slab's store has read the stage
       __syncwarp();
 #pragma unroll
@@ -204,6 +200,20 @@ struct EpiLseKeep {
           RZ_DCHECK(rbase >= 0 && col0 + c >= 0 && col0 + c < V && ((col0 + c) & 7) == 0, 12)) {
         tma_store_2d_hint(&p.tm_e16, stage, col0 + c, rbase, pol);
         bulk_commit();
+      }
+    }
+    // the tile's running maxima, one per 32-column slice, written together
+    // (two 16-byte stores per row: ldm is a multiple of 4 and col0 / 32 of 8)
+    const int nsl = (V - col0 + 31) >> 5;  // valid 32-column slices of this tile
+    if (grow < p.lse.T && RZ_DCHECK(grow >= 0 && (col0 >> 5) + (nsl < 8 ? nsl : 8) <= p.ldm, 11)) {
+      float* em = p.emax + grow * p.ldm + (col0 >> 5);
+      if (nsl >= 8) {
+        reinterpret_cast<float4*>(em)[0] = make_float4(mt[0], mt[1], mt[2], mt[3]);
+        reinterpret_cast<float4*>(em)[1] = make_float4(mt[4], mt[5], mt[6], mt[7]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < nsl) em[q] = mt[q];
       }
     }
   }
@@ -290,25 +300,32 @@ struct PhiloxRow {
   }
 };
 
-__device__ __forceinline__ float lg2_approx(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// U in (0, 1) from a 32-bit word: ((x >> 9) + 1/2) 2^-23, exact in fp32.
+__device__ __forceinline__ float uniform_of(uint32_t x) {
+  return __fmul_rn(__fadd_rn(__uint2float_rn(x >> 9), 0.5f), 1.1920928955078125e-7f);
 }
 
-// Fused sampling in the rollout's logprob GEMM: besides the log-sum-exp state
-// (the very same arithmetic as EpiLsePartial) each row keeps the running
-// Gumbel-max winner over its split: key = z log2(e) - log2(-log2 U), which
-// orders tokens exactly as z + Gumbel noise does (the two differ by the
-// constant log2(ln 2) and the factor log2(e)).  U for (row, v) is word
-// v mod 4 of Philox4x32-10 at counter (v / 4, row id lo, row id hi, 0) under
-// the caller's 64-bit seed, mapped to ((x >> 9) + 1/2) 2^-23 in (0, 1).  Ties
-// go to the smaller vocabulary index.
+// Fused sampling in the rollout's logprob GEMM: a_t ~ softmax(z_t) drawn in
+// the same pass that folds the row's log-sum-exp, by a two-level weighted
+// reservoir over the vocabulary in ascending order.
+//   * Within a vocabulary split, the row's 32-column chunks come in order.
+//     With R the running sum of the fold's terms over the chunks seen so far
+//     (this one included) and W this chunk's sum, the split's candidate is
+//     replaced by a draw from this chunk when U1 R < W; the draw picks the
+//     first token, in the order (column mod 4, then column), at which the
+//     running sum of terms passes U2 W.  The terms are the fold's own
+//     2^((z - m) log2 e), so the (m, s) state is bitwise the rollout's.
+//   * The splits are merged the same way, in split order (sample_merge_kernel).
+// Each token is then drawn with probability exactly its softmax weight.  U1,
+// U2 are words 0 and 1 of Philox4x32-10 at counter (column / 32, row id lo,
+// row id hi, 0) under the caller's 64-bit seed, the split's U3 word 0 at
+// counter (split, row id lo, row id hi, 1), each mapped by uniform_of: a
+// row's sample depends on its own id, hidden state and W only.
 struct EpiSample {
   struct Params {
     const int64_t* row_ids;  // nullable: row index (row0 + local row)
-    float4* part;            // [T, S]: m, s, best key, z at best
-    int* part_idx;           // [T, S]: best vocabulary index
+    float4* part;            // [T, S]: m, s, z at the split's candidate, -
+    int* part_idx;           // [T, S]: the split's candidate (-1: none)
     long long row0;          // first row of this launch (row ids only)
     long long T;
     int V;
@@ -316,7 +333,7 @@ struct EpiSample {
     uint32_t k0, k1;
   };
   struct State {
-    float m, s, bk, bz;
+    float m, s, bz;
     int bi;
     PhiloxRow rng;
   };
@@ -326,7 +343,6 @@ struct EpiSample {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
     st.m = -INFINITY;
     st.s = 0.f;
-    st.bk = -INFINITY;
     st.bz = 0.f;
     st.bi = -1;
     const long long rid = g < p.T ? (p.row_ids ? __ldg(p.row_ids + g) : p.row0 + g) : 0;
@@ -334,29 +350,9 @@ struct EpiSample {
                 static_cast<uint32_t>(static_cast<unsigned long long>(rid) >> 32), p.k0, p.k1);
   }
 
-  // -log2(U) to full relative precision for U = (m + 1/2) 2^-23.  Next to 1
-  // (1 - U < 2^-6), where -log2 U is tiny and the largest Gumbel draws come
-  // from, the fast hardware log2 has only absolute accuracy, so the Taylor
-  // series -ln(1 - v) = v (1 + v/2 + v^2/3 + v^3/4 + v^4/5 + ...) is used
-  // (truncation < 2^-26 relative); elsewhere the hardware log2 is accurate
-  // to ~1e-5 relative or better.
-  static __device__ __forceinline__ float neg_log2_uniform(uint32_t bits) {
-    const uint32_t m = bits >> 9;
-    const float u = __fmul_rn(__fadd_rn(__uint2float_rn(m), 0.5f), 1.1920928955078125e-7f);
-    const float v = __fmul_rn(__fsub_rn(__uint2float_rn(8388608u - m), 0.5f),
-                              1.1920928955078125e-7f);  // 1 - u, exact
-    float ser = fmaf(v, 0.2f, 0.25f);
-    ser = fmaf(v, ser, 0.33333334f);
-    ser = fmaf(v, ser, 0.5f);
-    ser = fmaf(v, ser, 1.0f);
-    const float near1 = __fmul_rn(__fmul_rn(v, kLog2e), ser);
-    return v < 0.015625f ? near1 : -lg2_approx(u);
-  }
-
-  // 32 columns of this thread's row; `words` holds the row's 32 Philox
-  // words (8 pieces of 16 B, piece q at position q ^ (lane & 7)).
+  // 32 columns of this thread's row.
   static __device__ __forceinline__ void chunk(const Params& p, State& st, const uint32_t (&r)[32],
-                                               int cbase, const uint4* words, int sw) {
+                                               int cbase) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -365,43 +361,78 @@ struct EpiSample {
       for (int j = 0; j < 32; ++j)
         if (cbase + j >= p.V) v[j] = -INFINITY;
     }
-    lse_fold32(st.m, st.s, v);
+    float e[32], acc[4], W;
+    lse_fold32_terms(st.m, st.s, v, e, acc, W);
+    uint32_t x[4];
+    st.rng.words(static_cast<uint32_t>(cbase) >> 5, x);
+    const bool rep = __fmul_rn(uniform_of(x[0]), st.s) < W;
+    if (!__any_sync(0xffffffffu, rep)) return;  // the warp stays converged
+    // draw from this chunk: the class (column mod 4) by the class sums, then
+    // the member inside it; on rounding past the end, the last positive one
+    const float tgt = __fmul_rn(uniform_of(x[1]), W);
+    int k = -1, lastk = 0;
+    float cum = 0.f, base = 0.f, lastbase = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint4 x4 = words[q ^ sw];
-      const uint32_t x[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * q + e;
-        const float key = fmaf(v[j], kLog2e, -lg2_approx(neg_log2_uniform(x[e])));
-        if (key > st.bk) {  // -inf (masked) never wins; ties keep the smaller index
-          st.bk = key;
-          st.bz = v[j];
-          st.bi = cbase + j;
-        }
+    for (int q = 0; q < 4; ++q) {
+      const float prev = cum;
+      cum = __fadd_rn(cum, acc[q]);
+      if (acc[q] > 0.f) {
+        lastk = q;
+        lastbase = prev;
       }
+      if (k < 0 && cum > tgt) {
+        k = q;
+        base = prev;
+      }
+    }
+    if (k < 0) {
+      k = lastk;
+      base = lastbase;
+    }
+    const float t2 = __fsub_rn(tgt, base);
+    float ev[8], zv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ev[i] = k == 0 ? e[4 * i] : (k == 1 ? e[4 * i + 1] : (k == 2 ? e[4 * i + 2] : e[4 * i + 3]));
+      zv[i] = k == 0 ? v[4 * i] : (k == 1 ? v[4 * i + 1] : (k == 2 ? v[4 * i + 2] : v[4 * i + 3]));
+    }
+    int sel = -1, last = -1;
+    float zsel = 0.f, zlast = 0.f;
+    cum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cum = __fadd_rn(cum, ev[i]);
+      if (ev[i] > 0.f) {
+        last = i;
+        zlast = zv[i];
+      }
+      if (sel < 0 && cum > t2) {
+        sel = i;
+        zsel = zv[i];
+      }
+    }
+    if (sel < 0) {
+      sel = last;
+      zsel = zlast;
+    }
+    if (rep && sel >= 0) {
+      st.bi = cbase + 4 * sel + k;
+      st.bz = zsel;
     }
   }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, int, int n_tile,
-                                              uint32_t taddr, int row, uint8_t* stage) {
+                                              uint32_t taddr, int, uint8_t*) {
     const int col0 = n_tile * kBN;
-    const int lane = row & 31;
-    const int sw = lane & 7;
-    uint4* words = reinterpret_cast<uint4*>(stage + lane * 128);  // this row only
 #pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
+    for (int c = 0; c < kBN; c += 64) {
       if (col0 + c >= p.V) break;  // warp-uniform
-      uint32_t r0[32];
+      uint32_t r0[32], r1[32];
       tmem_ld32(taddr + c, r0);
-#pragma unroll 2  // two independent Philox blocks in flight: the chain is latency-bound
-      for (int q = 0; q < 8; ++q) {
-        uint32_t x[4];
-        st.rng.words(static_cast<uint32_t>((col0 + c) >> 2) + q, x);
-        words[q ^ sw] = make_uint4(x[0], x[1], x[2], x[3]);
-      }
+      tmem_ld32(taddr + c + 32, r1);
       tmem_ld_wait();
-      chunk(p, st, r0, col0 + c, words, sw);
+      chunk(p, st, r0, col0 + c);
+      if (col0 + c + 32 < p.V) chunk(p, st, r1, col0 + c + 32);
     }
   }
 
@@ -410,7 +441,7 @@ struct EpiSample {
     const long long g = static_cast<long long>(m_blk) * kBM + row;
     if (g >= p.T) return;
     if (!RZ_DCHECK(g >= 0 && grp >= 0 && grp < p.S, 13)) return;
-    p.part[g * p.S + grp] = make_float4(st.m, st.s, st.bk, st.bz);
+    p.part[g * p.S + grp] = make_float4(st.m, st.s, st.bz, 0.f);
     p.part_idx[g * p.S + grp] = st.bi;
   }
 };
@@ -640,24 +671,34 @@ __global__ void __launch_bounds__(kDzThreads)
   }
 }
 
-// One thread per row: log-sum-exp exactly as lse_merge_kernel, and the
-// Gumbel-max winner over the splits in split order (ties: earlier split,
-// i.e. smaller vocabulary index).
+// One thread per row: the log-sum-exp exactly as lse_merge_kernel, and the
+// split level of the sampler's reservoir: splits in order, the running sum R
+// of their totals (scaled to the row's maximum as the log-sum-exp scales
+// them), the sample replaced by split g's candidate when U3 R < its total.
 __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict__ part,
-                                    const int* __restrict__ part_idx, int32_t* __restrict__ tokens,
-                                    float* __restrict__ logprob, float* __restrict__ lse) {
+                                    const int* __restrict__ part_idx,
+                                    const int64_t* __restrict__ row_ids, uint32_t k0, uint32_t k1,
+                                    int32_t* __restrict__ tokens, float* __restrict__ logprob,
+                                    float* __restrict__ lse) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const float4* pp = part + t * S;
   float sum;
   const float M = lse_merge_parts(pp, S, &sum);
-  float bk = -INFINITY, bz = 0.f;
+  const unsigned long long rid =
+      static_cast<unsigned long long>(row_ids ? row_ids[t] : static_cast<int64_t>(t));
+  const uint32_t rlo = static_cast<uint32_t>(rid & 0xffffffffull);
+  const uint32_t rhi = static_cast<uint32_t>(rid >> 32);
+  float R = 0.f, bz = 0.f;
   int bi = 0;
   for (int g = 0; g < S; ++g) {
-    if (pp[g].z > bk) {
-      bk = pp[g].z;
-      bz = pp[g].w;
+    const float w = __fmul_rn(pp[g].y, exp2f(__fmul_rn(__fsub_rn(pp[g].x, M), kLog2e)));
+    R = __fadd_rn(R, w);
+    uint32_t x[4];
+    philox4x32_10(static_cast<uint32_t>(g), rlo, rhi, 1u, k0, k1, x);
+    if (__fmul_rn(uniform_of(x[0]), R) < w && part_idx[t * S + g] >= 0) {
       bi = part_idx[t * S + g];
+      bz = pp[g].z;
     }
   }
   tokens[t] = bi;
@@ -762,8 +803,9 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
   }
   const int threads = 256;
   const long long blocks = (T + threads - 1) / threads;
-  sample_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(T, S, part, part_idx,
-                                                                         tokens, logprob, lse);
+  sample_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      T, S, part, part_idx, row_ids, static_cast<uint32_t>(seed & 0xffffffffull),
+      static_cast<uint32_t>(seed >> 32), tokens, logprob, lse);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ namespace rz {
 // computed by the very same operations either way.
 template <bool kKeep>
 __device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float (&v)[32],
-                                                float (&e)[32]) {
+                                                float (&e)[32], float (&acc)[4], float& w) {
   float mx[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
   for (int j = 4; j < 32; j += 4) {
@@ -36,24 +36,35 @@ __device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float 
     s = __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, cm), kLog2e)));
     m = cm;
   }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = 0.f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float t = ex2_approx(__fmul_rn(__fsub_rn(v[j], m), kLog2e));
     if (kKeep) e[j] = t;
     acc[j & 3] = __fadd_rn(acc[j & 3], t);
   }
-  s = __fadd_rn(s, __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])));
+  w = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+  s = __fadd_rn(s, w);
 }
 
 __device__ __forceinline__ void lse_fold32(float& m, float& s, const float (&v)[32]) {
-  float unused[32];
-  lse_fold32_impl<false>(m, s, v, unused);
+  float unused[32], acc[4], w;
+  lse_fold32_impl<false>(m, s, v, unused, acc, w);
 }
 
 __device__ __forceinline__ void lse_fold32_keep(float& m, float& s, const float (&v)[32],
                                                 float (&e)[32]) {
-  lse_fold32_impl<true>(m, s, v, e);
+  float acc[4], w;
+  lse_fold32_impl<true>(m, s, v, e, acc, w);
+}
+
+// The same fold, also returning the terms e, their sums over the four
+// classes of columns j mod 4 (acc) and the chunk's total w (the amount added
+// to s): what the fused sampler draws from.
+__device__ __forceinline__ void lse_fold32_terms(float& m, float& s, const float (&v)[32],
+                                                 float (&e)[32], float (&acc)[4], float& w) {
+  lse_fold32_impl<true>(m, s, v, e, acc, w);
 }
 
 // Merge the partial states of a row in a fixed order.  P is any struct with

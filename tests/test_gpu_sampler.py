@@ -1,8 +1,9 @@
 """Fused rollout sampling (rz_sample_logprob) against the sampler oracle:
-same Philox stream and Gumbel-max rule, so the sampled tokens agree except
-where two keys are closer than fp32 can separate (checked to be such a
-near-tie); the recorded log mu is the learner's log pi bit for bit; samples
-are batch-invariant given row ids; frequencies follow softmax."""
+the same Philox stream and two-level reservoir, so the sampled tokens agree
+except where one of the row's decisions sits within rounding of its
+threshold (checked against the oracle's margin); the recorded log mu is the
+learner's log pi bit for bit; samples are batch-invariant given row ids;
+frequencies follow softmax."""
 
 import math
 
@@ -18,7 +19,11 @@ from helpers import TOL_LOGPI, bits, f64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-NEAR_TIE = 1e-3  # natural-log key units
+# A decision compares U * R with W (or U * W with a running sum): fp32 sums
+# of ex2 terms and fp32-accumulated logits carry ~1e-5 relative error, so a
+# row may sample differently from the fp64 oracle only where some decision
+# is that close to its threshold.
+NEAR_TIE = 1e-4
 
 
 def _check_against_oracle(H, W, row_ids, seed, tok, lmu):
@@ -28,8 +33,7 @@ def _check_against_oracle(H, W, row_ids, seed, tok, lmu):
     got = tok.cpu().numpy().astype(np.int64)
     same = got == want_tok
     for t in np.nonzero(~same)[0]:
-        keys, _ = rz_sampler.key_of(Hd[t], Wd, rid[t], seed)
-        assert keys[got[t]] >= keys.max() - NEAR_TIE, (t, keys[got[t]], keys.max())
+        assert margin[t] < NEAR_TIE, (t, got[t], want_tok[t], margin[t])
     assert same.mean() >= 0.99, same.mean()
     # the oracle's log-softmax of each row (from H and W only), read at the
     # token the GPU drew: the recorded log mu must be that token's log pi
@@ -37,6 +41,7 @@ def _check_against_oracle(H, W, row_ids, seed, tok, lmu):
     lp_rows = z - oracle.logsumexp_rows(z)[:, None]
     lp_gpu_tok = lp_rows[np.arange(got.shape[0]), got]
     assert np.max(np.abs(f64(lmu) - lp_gpu_tok)) <= TOL_LOGPI
+    return same.mean()
 
 
 @pytest.mark.parametrize("T,d,V", [(300, 256, 1000), (129, 2048, 151936), (40, 136, 77)])
@@ -102,3 +107,29 @@ def test_sampler_frequencies(rz):
     p1 = 1.0 / (1.0 + math.exp(-b))
     f1 = tok.float().mean().item()
     assert abs(f1 - p1) <= 4 * math.sqrt(p1 * (1 - p1) / T), (f1, p1)
+
+
+def test_sampler_frequencies_across_chunks_and_segments(rz):
+    # V = 600: three vocabulary splits and 19 chunks of 32 columns with
+    # unequal masses; chi-square over every token from 120,000 rows
+    V, T, d = 600, 120000, 8
+    v = np.arange(V)
+    zt = np.log1p(v % 7) + 0.6 * (v >= 256) - 0.4 * (v >= 512) + 0.3 * ((v // 32) % 3 == 1)
+    W = torch.zeros(V, d, dtype=torch.bfloat16, device=DEV)
+    W[:, 0] = torch.tensor(zt, dtype=torch.float32, device=DEV).to(torch.bfloat16)
+    H = torch.zeros(T, d, dtype=torch.bfloat16, device=DEV)
+    H[:, 0] = 1.0
+    z = W[:, 0].double().cpu().numpy()
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    tok, lmu = rz.rz_sample_logprob(H, W, 7, row_ids=torch.arange(T, device=DEV) * 11 + 3)
+    torch.cuda.synchronize()
+    counts = np.bincount(tok.cpu().numpy(), minlength=V)
+    assert counts.sum() == T and counts.shape[0] == V
+    assert scipy.stats.chisquare(counts, T * p).pvalue > 1e-4
+    np.testing.assert_allclose(lmu.cpu().double().numpy(), np.log(p[tok.cpu().numpy()]),
+                               atol=1e-5)
+    # the same rows drawn by the oracle agree token for token (near-ties aside)
+    rate = _check_against_oracle(H[:4000].cpu(), W.cpu(),
+                                 torch.arange(4000) * 11 + 3, 7, tok[:4000], lmu[:4000])
+    assert rate >= 0.995

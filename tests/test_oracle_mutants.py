@@ -70,16 +70,19 @@ MUTANTS = {
 
 # mistakes in the sampler oracle, against the sampler's pins
 SAMPLER_MUTANTS = {
-    "Gumbel noise with the wrong sign": [("- np.log(-np.log(u))", "+ np.log(-np.log(u))")],
     "U on the closed interval": [("+ 0.5) * 2.0 ** -23", "+ 0.0) * 2.0 ** -23")],
     "Philox with 7 rounds": [("    for _ in range(10):", "    for _ in range(7):")],
-    "recorded log mu of the wrong token": [("lmu[t] = z[a] - lse", "lmu[t] = z[int(np.argmin(k))] - lse")],
-    "key_of draws the next row's noise": [("return gumbel_keys(z, row_id, seed), z",
-                                           "return gumbel_keys(z, row_id + 1, seed), z")],
-    "key_of ignores the seed's high half": [("return gumbel_keys(z, row_id, seed), z",
-                                             "return gumbel_keys(z, row_id, seed & 0xFFFFFFFF), z")],
-    "key_of with the transposed weight": [("z = np.asarray(W, np.float64) @ np.asarray(H_row, np.float64)\n    return gumbel_keys",
-                                           "z = np.asarray(W, np.float64).sum(axis=1) * np.asarray(H_row, np.float64).sum()\n    return gumbel_keys")],
+    "recorded log mu of the wrong token": [("logmu = z[rows, final] - lse",
+                                            "logmu = z[rows, (final + 1) % V] - lse")],
+    "chunk kept against the sum before it": [("rep = u1 * R < Wc", "rep = u1 * (R - Wc) < Wc")],
+    "segment kept against the sum before it": [("rep = (u3 * Rp < Qg) & (cand >= 0)",
+                                                "rep = (u3 * (Rp - Qg) < Qg) & (cand >= 0)")],
+    "draw by column instead of by class": [
+        ("return np.array([j for k in range(4) for j in range(k, n, 4)], dtype=np.int64)",
+         "return np.arange(n, dtype=np.int64)")],
+    "one tile per segment": [("    tps = (nt + n - 1) // n\n", "    tps = 1\n")],
+    "both draws from word 0": [("u1, u2 = uniform_of(x[:, 0]), uniform_of(x[:, 1])",
+                                "u1, u2 = uniform_of(x[:, 0]), uniform_of(x[:, 0])")],
 }
 
 
@@ -144,7 +147,7 @@ def _failing_sampler_pins(mod, monkeypatch, first_only=False):
     monkeypatch.setattr(sampler_pins, "rz_sampler", mod)
     fns = [(n, f) for n, f in inspect.getmembers(sampler_pins, inspect.isfunction)
            if n.startswith("test_") and not inspect.signature(f).parameters]
-    fns.sort(key=lambda nf: ("gumbel" in nf[0], nf[0]))
+    fns.sort(key=lambda nf: ("sampling" in nf[0], nf[0]))
     failed = []
     with np.errstate(all="ignore"):
         for name, fn in fns:

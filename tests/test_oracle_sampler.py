@@ -33,12 +33,44 @@ def test_philox_known_answers():
 
 
 def test_uniforms_are_open_interval_and_23_bit():
-    u = rz_sampler.uniforms(12345, 4096, seed=99)
+    x = rz_sampler.row_words(12345, np.arange(4096) * 977 + 3, 0, seed=99)
+    u = rz_sampler.uniform_of(x.reshape(-1))
     assert np.all(u > 0) and np.all(u < 1)
     assert np.all((u * 2 ** 23 - 0.5) == np.floor(u * 2 ** 23))
+    assert rz_sampler.uniform_of(0) == 2.0 ** -24
+    assert rz_sampler.uniform_of(0xFFFFFFFF) == 1.0 - 2.0 ** -24
 
 
-def test_gumbel_max_two_tokens_matches_softmax():
+def test_draw_inside_one_chunk_uses_the_published_words():
+    # row id 0 and seed 0: the first chunk's uniforms are words 0 and 1 of the
+    # first known-answer vector (counter 0, key 0).  A one-chunk, one-segment
+    # row always takes the chunk's draw, which visits columns 0,4,1,5,2,6,3,7
+    # and stops where the running weight passes U2 * W.
+    ctr, key, want = _kat()[0]
+    assert ctr == [0, 0, 0, 0] and key == [0, 0]
+    q = np.arange(1.0, 9.0)                      # weights 1..8 (z = log q)
+    order = [0, 4, 1, 5, 2, 6, 3, 7]
+    u2 = ((want[1] >> 9) + 0.5) * 2.0 ** -23
+    cs = np.cumsum(q[order])
+    expect = order[int(np.argmax(cs > u2 * q.sum()))]
+    tok, lmu, _ = rz_sampler.sample_rows(np.ones((1, 1)), np.log(q)[:, None], [0], seed=0)
+    assert tok[0] == expect
+    assert lmu[0] == pytest.approx(math.log(q[expect] / q.sum()), abs=1e-14)
+    np.testing.assert_array_equal(rz_sampler.draw_order(8), order)
+    np.testing.assert_array_equal(rz_sampler.draw_order(6), [0, 4, 1, 5, 2, 3])
+
+
+def test_segments_cover_the_vocabulary_in_whole_tiles():
+    for V in (1, 8, 255, 256, 600, 4096, 16384, 16385, 151936):
+        seg = rz_sampler.segments(V)
+        assert seg[0][0] == 0 and seg[-1][1] == V
+        assert all(seg[i][1] == seg[i + 1][0] for i in range(len(seg) - 1))
+        assert len(seg) <= 64 and all(a % 256 == 0 for a, _ in seg)
+    assert len(rz_sampler.segments(151936)) == 60
+    assert rz_sampler.segments(600) == [(0, 256), (256, 512), (512, 600)]
+
+
+def test_sampling_two_tokens_matches_softmax():
     # z = (0, log 3): softmax = (1/4, 3/4)
     H = np.ones((20000, 1))
     W = np.array([[0.0], [math.log(3.0)]])
@@ -49,10 +81,8 @@ def test_gumbel_max_two_tokens_matches_softmax():
     np.testing.assert_allclose(lmu[tok == 0], math.log(0.25), atol=1e-14)
 
 
-def test_gumbel_max_three_tokens_matches_softmax():
-    # z = (0, log 2, log 5): softmax = (1/8, 2/8, 5/8).  Unlike two tokens or
-    # uniform logits, three unequal logits tell z + G from z - G apart
-    # (z - G gives about (0.084, 0.245, 0.671)).
+def test_sampling_three_tokens_matches_softmax():
+    # z = (0, log 2, log 5): softmax = (1/8, 2/8, 5/8)
     n = 8000
     H = np.ones((n, 1))
     W = np.array([[0.0], [math.log(2.0)], [math.log(5.0)]])
@@ -62,7 +92,7 @@ def test_gumbel_max_three_tokens_matches_softmax():
     assert p > 1e-4, counts
 
 
-def test_gumbel_max_uniform_logits_chi_square():
+def test_sampling_uniform_logits_chi_square():
     V, n = 16, 16000
     H = np.ones((n, 1))
     W = np.zeros((V, 1))
@@ -87,38 +117,20 @@ def test_recorded_logmu_is_the_logprob_of_the_sampled_token():
     np.testing.assert_array_equal(tok2, tok[perm])
 
 
-def test_key_of_at_the_zero_counter_uses_the_published_words():
-    # row id 0 and seed 0 put tokens 0..3 at Philox counter (0, 0, 0, 0) under
-    # key (0, 0): the first known-answer vector.  Their keys minus the logits
-    # are the Gumbel draws -log(-log U) of those four published words.
-    ctr, key, want = _kat()[0]
-    assert ctr == [0, 0, 0, 0] and key == [0, 0]
-    h = np.array([1.0, -2.0])
-    W = np.array([[0.5, 0.0], [0.0, 1.0], [3.0, 1.0], [-1.0, -1.0], [2.0, 2.0]])
-    keys, z = rz_sampler.key_of(h, W, 0, 0)
-    np.testing.assert_array_equal(z, W @ h)
-    u = np.array([((x >> 9) + 0.5) * 2.0 ** -23 for x in want])
-    np.testing.assert_allclose(keys[:4] - z[:4], -np.log(-np.log(u)), rtol=0, atol=1e-12)
-
-
-def test_key_of_agrees_with_the_sampled_rows():
-    # row ids and a seed with both 32-bit halves non-zero: the token each row
-    # draws holds the largest key that key_of gives for that row, and the
-    # recorded margin is that key's lead over the runner-up
-    rng = np.random.default_rng(11)
-    H = rng.standard_normal((24, 5))
-    W = rng.standard_normal((37, 5))
-    rid = rng.integers(2**33, 2**62, 24)
-    seed = (0x89ABCDEF << 32) | 0x01234567
-    tok, _, margin = rz_sampler.sample_rows(H, W, rid, seed)
-    for t in range(24):
-        keys, z = rz_sampler.key_of(H[t], W, int(rid[t]), seed)
-        np.testing.assert_allclose(z, oracle.lmhead_logits(H[t:t + 1], W)[0], atol=1e-12)
-        assert int(np.argmax(keys)) == tok[t]
-        srt = np.sort(keys)
-        assert srt[-1] - srt[-2] == pytest.approx(margin[t], abs=1e-12)
-    # another row id or seed draws other noise
-    k0, _ = rz_sampler.key_of(H[0], W, int(rid[0]), seed)
-    k1, _ = rz_sampler.key_of(H[0], W, int(rid[0]) + 1, seed)
-    k2, _ = rz_sampler.key_of(H[0], W, int(rid[0]), seed ^ (1 << 40))
-    assert not np.allclose(k0, k1) and not np.allclose(k0, k2)
+def test_sampling_across_chunks_and_segments_matches_softmax():
+    # V = 600: three segments (256, 256 and 88 columns) and 19 chunks, with
+    # unequal masses per chunk, per class inside a chunk and per segment;
+    # chi-square over every token
+    V, n = 600, 60000
+    v = np.arange(V)
+    z = np.log1p(v % 7) + 0.6 * (v >= 256) - 0.4 * (v >= 512) + 0.3 * ((v // 32) % 3 == 1)
+    H = np.ones((n, 1))
+    tok, lmu, _ = rz_sampler.sample_rows(H, z[:, None], np.arange(n) * 13 + 7, seed=2**33 + 5)
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    counts = np.bincount(tok, minlength=V)
+    assert scipy.stats.chisquare(counts, n * p).pvalue > 1e-4
+    # per chunk and per segment as well (coarser bins, more power per bin)
+    cb = np.bincount(tok // 32, minlength=19)
+    assert scipy.stats.chisquare(cb, n * np.bincount(v // 32, weights=p)).pvalue > 1e-4
+    np.testing.assert_allclose(lmu, np.log(p[tok]), atol=1e-12)
