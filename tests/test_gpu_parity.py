@@ -388,3 +388,26 @@ def test_logits_variant_peaked_softmax_vs_oracle(rz, std):
     a_got = dz[rows, f64(tok)[rows]]
     a_want = ref["dz"][rows, f64(tok)[rows]]
     assert np.max(np.abs(a_got - a_want) / np.abs(a_want)) <= 2e-2
+
+
+def test_logits_variant_beyond_the_cluster_vocabulary(rz):
+    """Above 204,800 columns a quarter row no longer fits two per SM, and the
+    given-logits step runs its two-pass row kernel instead of the one-pass
+    cluster kernel: the same parity."""
+    T, V, B = 70, 262144, 2
+    g = torch.Generator().manual_seed(5)
+    logits = (torch.randn(T, V, generator=g) * 3.0).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    cu = torch.tensor([0, 33, T], dtype=torch.int64)
+    adv = torch.tensor([0.6, -0.6])
+    lp64 = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), np.zeros(T), f64(cu), f64(adv),
+                                      rows=np.zeros(0, np.int64))["logpi"]
+    logmu = torch.tensor(lp64, dtype=torch.float32) + torch.randn(T, generator=g) * 0.05
+    ref = oracle.logits_loss_fwd_bwd(f64(logits), f64(tok), f64(logmu), f64(cu), f64(adv))
+    buf = logits.to(DEV)
+    out = rz.rz_logits_loss_fwd_bwd(buf, tok.to(DEV), logmu.to(DEV), cu.to(DEV), adv.to(DEV))
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(out["logprob"]) - ref["logpi"])) <= TOL_LOGPI
+    assert scalar_close(out["loss"].item(), ref["loss"])
+    assert scalar_close(out["d3"].item(), ref["d3"])
+    assert rel_l2(f64(buf), ref["dz"]) <= TOL_GRAD_REL_L2
