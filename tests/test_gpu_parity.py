@@ -390,10 +390,9 @@ def test_logits_variant_peaked_softmax_vs_oracle(rz, std):
     assert np.max(np.abs(a_got - a_want) / np.abs(a_want)) <= 2e-2
 
 
-def test_logits_variant_beyond_the_cluster_vocabulary(rz):
-    """Above 204,800 columns a quarter row no longer fits two per SM, and the
-    given-logits step runs its two-pass row kernel instead of the one-pass
-    cluster kernel: the same parity."""
+def test_logits_variant_large_vocabulary(rz):
+    """A 262,144-column row (512 KB of bf16): the row kernel's shared-memory
+    stash holds an eighth of it and the second pass re-reads the rest."""
     T, V, B = 70, 262144, 2
     g = torch.Generator().manual_seed(5)
     logits = (torch.randn(T, V, generator=g) * 3.0).to(torch.bfloat16)
