@@ -35,14 +35,15 @@ GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_m
                 "rz_internal.h"]
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 TRAFFIC_CAPTURES = {
-    # learner logits+LSE keep GEMM, one 38,912-row chunk at the 4B shape
-    # (1.286 GB read + 3.120 GB written at 9,728 rows, one raster group of
-    # 76 m-blocks; a 38,912-row chunk is four such groups: x4)
-    "qwen4b_lag64": {"bytes": 4 * (1.286006e9 + 3.119965e9), "sources": GEMM_SOURCES,
-                     "sources_sha256_16": "6abae3cf0a78d27c"},
-    # given-logits row kernel over the 262,144-row MoE-shaped workload
-    "moe30b_logits": {"bytes": 106.960e9 + 79.575e9, "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "d67650bec883fd47"},
+    # learner logits+LSE keep GEMM, one 38,912-row chunk at the 4B shape:
+    # 2.883 GB read + 3.140 GB written at 9,728 rows (one raster group of 76
+    # m-blocks); a 38,912-row chunk is four such groups (x4)
+    "qwen4b_lag64": {"bytes": 4 * (2.883214e9 + 3.140452e9), "sources": GEMM_SOURCES,
+                     "sources_sha256_16": "f06817c1790ee8e4"},
+    # given-logits row kernel: 6.567 GB read + 4.895 GB written at 16,384
+    # rows, scaled to the workload's 262,144 rows (x16)
+    "moe30b_logits": {"bytes": 16 * (6.566907e9 + 4.895203e9), "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "9d5758acdbfb6e15"},
 }
 
 
@@ -724,8 +725,8 @@ def measure_logits(args, world, rank, dev, peaks, peak_src, steps, warmup, full=
                      "peak_source": "%s hbm_gbs" % peak_src,
                      "ms_per_launch": rows_ms,
                      "traffic": captured_traffic(wl.name),
-                     "traffic_unit": "DRAM bytes per launch (262,144 rows; ncu capture, "
-                                     "see the committed ncu summary)",
+                     "traffic_unit": "DRAM bytes per launch (ncu capture of 16,384 rows scaled "
+                                     "to 262,144; see the committed ncu summary)",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "step_breakdown": breakdown,
         "gpu_launches": 4 * steps,  # response factors, row kernel, loss (2)
