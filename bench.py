@@ -287,6 +287,10 @@ def run_ours(args):
         out["other_workloads"] = other_workloads(args, rank, dev, peaks, peak_src)
     if rank == 0:
         print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
     return 0
 
 
@@ -342,19 +346,15 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     # exchange step (dW in rank order, the loss share and D3 per rank)
     B_total = B * world
     ex_ev = []
-    scal = torch.empty(2, dtype=torch.float32, device=dev)
     gathered = torch.empty((world, 2), dtype=torch.float32, device=dev)
     state = {"dW_sum": dW}
 
     def exchange():
         from invariant_logprobs_gb300 import shard
-        import torch.distributed as dist
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        state["dW_sum"] = shard.fixed_order_allreduce(dW, rz.rz_sum_partials)
-        scal[0:1].copy_(loss)
-        scal[1:2].copy_(d3)
-        dist.all_gather_into_tensor(gathered.view(-1), scal)
+        state["dW_sum"], g = shard.dp_exchange(dW, loss, d3, rz.rz_sum_partials)
+        gathered.copy_(g)
         e1.record(stream)
         ex_ev.append((e0, e1))
 

@@ -118,3 +118,19 @@ def fixed_order_allreduce(t, sum_parts, group=None):
     dist.all_gather_into_tensor(out, mine, group=group)
     return out[:n].view_as(t)
 
+
+def dp_exchange(dW, loss, d3, sum_parts, group=None):
+    """The data-parallel learner's exchange step after every rank has run
+    its shard (rz_loss_fwd_bwd_shard): dW summed over ranks in rank order
+    (fixed_order_allreduce) and every rank's (loss share, D3) gathered.
+    loss and d3 are 1-element tensors on dW's device.  Returns (dW_sum,
+    gathered [N, 2]); the batch's loss is gathered[:, 0].sum() and its D3
+    the token-weighted mean of gathered[:, 1] (combine_scalars)."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    dW_sum = fixed_order_allreduce(dW, sum_parts, group)
+    scal = torch.cat([loss.reshape(1), d3.reshape(1)]).to(torch.float32)
+    gathered = torch.empty((world, 2), dtype=torch.float32, device=scal.device)
+    dist.all_gather_into_tensor(gathered.view(-1), scal, group=group)
+    return dW_sum, gathered

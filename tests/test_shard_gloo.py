@@ -137,3 +137,46 @@ def test_fixed_order_sum_is_the_rank_order_sum_on_every_rank(tmp_path, world):
         got2 = torch.from_numpy(np.load(tmp_path / ("ar_%d.npy" % r)))
         assert got2.shape == want2.shape
         assert torch.equal(got2.view(torch.int32), want2.view(torch.int32)), r
+
+
+def _exchange_worker(rank, world, port, out_dir):
+    """Each rank: the oracle on its shard with the global normalisation
+    (advantages scaled by B_r/B), then the bench's exchange step."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    H, W, tok, lm, cu, A = _problem(5)
+    B = A.shape[0]
+    r0, r1 = shard.plan(cu, world)[rank]
+    t0, t1, cu_l = shard.local_batch(cu, (r0, r1))
+    A_l = A[r0:r1] * shard.advantage_scale(r1 - r0, B)
+    res = oracle.loss_fwd_bwd(H[t0:t1], W, tok[t0:t1], lm[t0:t1], cu_l, A_l)
+    dW = torch.tensor(res["dW"], dtype=torch.float32)
+    dW_sum, gathered = shard.dp_exchange(dW, torch.tensor([res["loss"]]),
+                                         torch.tensor([res["d3"]]), _serial_sum)
+    T_r = [None] * world
+    dist.all_gather_object(T_r, t1 - t0)
+    loss, d3 = shard.combine_scalars(gathered[:, 0].double().tolist(),
+                                     gathered[:, 1].double().tolist(), T_r)
+    np.save(os.path.join(out_dir, "ex_dW_%d.npy" % rank), dW_sum.numpy())
+    np.save(os.path.join(out_dir, "ex_sc_%d.npy" % rank), np.array([loss, d3]))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_dp_exchange_of_sharded_steps(tmp_path, world):
+    """The bench's exchange on gloo ranks: every rank ends with the same dW
+    bits, equal to the rank-order sum of the partials, and the batch's loss
+    and D3 match the unsharded oracle."""
+    mp.spawn(_exchange_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+             join=True)
+    H, W, tok, lm, cu, A = _problem(5)
+    ref = oracle.loss_fwd_bwd(H, W, tok, lm, cu, A)
+    dWs = [np.load(tmp_path / ("ex_dW_%d.npy" % r)) for r in range(world)]
+    for r in range(1, world):
+        assert np.array_equal(dWs[r].view(np.int32), dWs[0].view(np.int32))
+    np.testing.assert_allclose(dWs[0], ref["dW"], rtol=1e-5, atol=1e-6)
+    for r in range(world):
+        loss, d3 = np.load(tmp_path / ("ex_sc_%d.npy" % r))
+        assert loss == pytest.approx(ref["loss"], rel=1e-6, abs=1e-8)
+        assert d3 == pytest.approx(ref["d3"], rel=1e-6, abs=1e-8)
