@@ -141,3 +141,30 @@ def test_zero_mismatch_when_the_learner_chunk_is_capped(rz):
     T = 2 * chunk + 5000
     ws_bytes = _zero_mismatch(rz, T, d, V, 43)
     assert ws_bytes >= chunk * per_row  # the workspace holds one capped chunk
+
+
+def test_maximum_vocabulary(rz):
+    """V = 2^24, the largest vocabulary the boundary accepts: the learner's
+    chunk shrinks to 1,152 rows (40 GiB of kept terms), so 2,500 rows cross
+    three chunks.  Rollout and learner agree bit for bit (w == 1, D3 == 0),
+    sampled rows match the oracle's log pi, and the fused sampler records
+    the logprob of what it draws."""
+    V, d, T = 1 << 24, 16, 2500
+    per_row = (V + 7) // 8 * 8 * 2 + (V + 127) // 128 * 4 * 4
+    assert (40 << 30) // per_row // 128 * 128 == 1152
+    ws_bytes = _zero_mismatch(rz, T, d, V, 47)
+    assert ws_bytes >= 1152 * per_row
+    g = torch.Generator(device=DEV).manual_seed(48)
+    H = torch.randn(T, d, generator=g, device=DEV).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g, device=DEV) * 0.3).to(torch.bfloat16)
+    tok = torch.randint(0, V, (T,), generator=g, device=DEV, dtype=torch.int32)
+    lp, _ = rz.rz_token_logprob(H, W, tok)
+    stok, slmu = rz.rz_sample_logprob(H, W, 3)
+    lp_s, _ = rz.rz_token_logprob(H, W, stok)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(lp_s), bits(slmu))
+    assert int(stok.min()) >= 0 and int(stok.max()) < V
+    rows = np.array([0, 1151, 1152, T - 1])
+    r_t = torch.as_tensor(rows, device=DEV)
+    want, _ = oracle.token_logprob_rows(f64(H[r_t]), f64(W), f64(tok[r_t]), np.arange(4))
+    assert np.max(np.abs(f64(lp[r_t]) - want)) <= TOL_LOGPI
