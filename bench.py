@@ -347,13 +347,13 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     B_total = B * world
     ex_ev = []
     gathered = torch.empty((world, 2), dtype=torch.float32, device=dev)
-    state = {"dW_sum": dW}
+    dW_sum = {}  # the exchanged dW of the latest step (every rank holds all of it)
 
     def exchange():
         from invariant_logprobs_gb300 import shard
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        state["dW_sum"], g = shard.dp_exchange(dW, loss, d3, rz.rz_sum_partials)
+        dW_sum["dW"], g = shard.dp_exchange(dW, loss, d3, rz.rz_sum_partials)
         gathered.copy_(g)
         e1.record(stream)
         ex_ev.append((e0, e1))

@@ -555,7 +555,6 @@ def rz_is_stats(logpi, logmu, stats_out=None, stream=None):
 
 def rz_peak_to_median(series):
     """max/median of a host sequence of per-update values (host function)."""
-    import array
     buf = (ctypes.c_float * len(series))(*[float(x) for x in series])
     out = ctypes.c_double(0.0)
     _check("rz_peak_to_median", load().rz_peak_to_median(
