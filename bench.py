@@ -5,11 +5,15 @@ the pages' runs.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                   [--impl ours|reference]
 
-One step = group advantages + rz_loss_fwd_bwd over one batch already resident
-in HBM (H, W, tokens, recorded log mu, cu_seqlens, rewards).  Inputs (H alone
-is 3.3-5.7 GB) are far larger than L2, so no flush is needed between steps.
-Rank 0 prints one JSON line.  Under torchrun each rank runs its own batch
-(weak scaling, no data-path collective) and the max time over ranks counts.
+One step = group advantages + the learner step over one batch already
+resident in HBM (H, W, tokens, the rollout's recorded log mu and log-sum-exp
+of every row, cu_seqlens, rewards), through rz_loss_fwd_bwd_ref (the kept
+softmax terms taken against the recorded log-sum-exp: no dz pass); the same
+step through rz_loss_fwd_bwd is timed beside it (`plain_route`).  Inputs (H
+alone is 3.3-5.7 GB) are far larger than L2, so no flush is needed between
+steps.  Rank 0 prints one JSON line.  Under torchrun each rank runs its own
+shard of the batch (rz_loss_fwd_bwd_shard) and the step includes the
+fixed-order exchange of dW; the max time over ranks counts.
 """
 
 import argparse
@@ -35,15 +39,16 @@ GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_m
                 "rz_internal.h"]
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 TRAFFIC_CAPTURES = {
-    # learner logits+LSE keep GEMM, one 38,912-row chunk at the 4B shape:
-    # 2.883 GB read + 3.140 GB written at 9,728 rows (one raster group of 76
-    # m-blocks); a 38,912-row chunk is four such groups (x4)
-    "qwen4b_lag64": {"bytes": 4 * (2.883214e9 + 3.140452e9), "sources": GEMM_SOURCES,
-                     "sources_sha256_16": "f06817c1790ee8e4"},
-    # given-logits row kernel: 6.567 GB read + 4.895 GB written at 16,384
+    # learner keep GEMM taking the terms against the recorded log-sum-exp, one
+    # 38,912-row chunk at the 4B shape: 1.939 GB read + 2.946 GB written at
+    # 9,728 rows (one raster group of 76 m-blocks); a 38,912-row chunk is four
+    # such groups (x4)
+    "qwen4b_lag64": {"bytes": 4 * (1.939186688e9 + 2.946383872e9), "sources": GEMM_SOURCES,
+                     "sources_sha256_16": "2b95a6e69c093685"},
+    # given-logits row kernel: 6.545 GB read + 4.893 GB written at 16,384
     # rows, scaled to the workload's 262,144 rows (x16)
-    "moe30b_logits": {"bytes": 16 * (6.566907e9 + 4.895203e9), "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "9d5758acdbfb6e15"},
+    "moe30b_logits": {"bytes": 16 * (6.545230592e9 + 4.892545792e9), "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "b957b32599bf73bc"},
 }
 
 
@@ -261,8 +266,10 @@ def build_learner_batch(name, dev, rank):
     from invariant_logprobs_gb300 import synth
     wl = synth.WORKLOADS[name]
     b = synth.make_batch(wl, device=dev, seed=wl.seed + 7919 * rank)
-    # the rollout records log mu with its (lagged) weights: our own rollout path
-    b["logmu"], _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
+    # the rollout records log mu and the row's log-sum-exp with its (lagged)
+    # weights, in one pass: our own rollout path
+    b["lse"] = torch.empty(b["T"], dtype=torch.float32, device=dev)
+    b["logmu"], _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], lse_out=b["lse"])
     b["adv"] = rz.rz_group_advantage(b["rewards"], b["G"])
     torch.cuda.synchronize()
     return wl, b
@@ -333,7 +340,7 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     stream = torch.cuda.current_stream()
     wl, b = build_learner_batch(name, dev, rank)
     T, d, V, B = b["T"], b["d"], b["V"], b["B"]
-    ws = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
+    ws = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD_REF, T, d, V, B, dev)
     dH = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     dW = torch.empty((V, d), dtype=torch.float32, device=dev)
     lp = torch.empty(T, dtype=torch.float32, device=dev)
@@ -361,13 +368,13 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     def step():
         rz.rz_group_advantage(b["rewards"], b["G"], adv_out=adv)
         if world == 1:
-            rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
-                               logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
-                               err_flag=err)
+            rz.rz_loss_fwd_bwd_ref(b["H"], b["W"], b["tokens"], b["logmu"], b["lse"], b["cu"],
+                                   adv, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
+                                   d3_out=d3, ws=ws, err_flag=err)
         else:
             rz.rz_loss_fwd_bwd_shard(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
                                      B_total, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
-                                     d3_out=d3, ws=ws, err_flag=err)
+                                     d3_out=d3, ws=ws, err_flag=err, ref_lse=b["lse"])
             exchange()
 
     for _ in range(warmup):
@@ -404,7 +411,11 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
     for cname in ("keep_gemm", "dH_gemm", "dW_gemm"):
         c = breakdown["classes"][cname]
         c["tflops"] = 2.0 * d * V * T / (c["ms"] / 1e3) / 1e12
-    breakdown["classes"]["dz"]["gbs"] = T * 4.125 * V / (breakdown["classes"]["dz"]["ms"] / 1e3) / 1e9
+    # on this route the library's dz class is the H scaling (sigma_t h_t):
+    # 4 bytes per element of H moved
+    sc = breakdown["classes"].pop("dz")
+    sc["gbs"] = T * d * 4.0 / (sc["ms"] / 1e3) / 1e9
+    breakdown["classes"]["scale_rows"] = sc
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": ms,
@@ -423,8 +434,8 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
         # log-sum-exp GEMM that keeps the softmax terms (2dV flop per token),
         # timed per launch by the launch-class events of the profiled steps
         "roofline": {
-            "kernel": "gemm_kernel<EpiLseKeep> (learner logits+LSE GEMM, one launch per "
-                      "38,912-row chunk)",
+            "kernel": "gemm_kernel<EpiLseKeepT<true>> (learner logits+LSE GEMM keeping the "
+                      "terms against the recorded log-sum-exp, one launch per 38,912-row chunk)",
             "bound": "tensor", "achieved": keep_tf,
             "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
             "frac": keep_tf / peaks["bf16_tflops_sustained"],
@@ -436,10 +447,10 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
             "traffic": captured_traffic(wl.name),
             "traffic_unit": "DRAM bytes per 38,912-row launch (ncu capture of a smaller chunk, "
                             "scaled by rows; see the committed ncu summary)",
-            # H chunk + W + the chunk's split states read; fp16 terms, running
-            # maxima and split states written
-            "algorithmic_bytes_per_launch": 38912 * d * 2 + V * d * 2 +
-            38912 * (2 * ((V + 7) // 8 * 8) + 4 * ((V + 127) // 128 * 4)) +
+            # H chunk + W + the chunk's references read; bf16 terms and split
+            # states written
+            "algorithmic_bytes_per_launch": 38912 * d * 2 + V * d * 2 + 38912 * 4 +
+            38912 * 2 * ((V + 7) // 8 * 8) +
             rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, 38912, d, V, 0)},
         "step_breakdown": breakdown,
         "gpu_launches": steps * (launches_per_step(T, V) + (1 if world > 1 else 0)),
@@ -458,6 +469,13 @@ def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, s
         out["d3"] = float(sum(g[r, 1] * T_r[r] for r in range(world)) / sum(T_r))
     if not full:
         return out
+
+    # the same step through rz_loss_fwd_bwd (running maxima + the dz pass)
+    pr = time_plain_route(rz, b, adv, lp, dH, dW, loss, d3, err, stream, dev,
+                          max(2, min(steps, 5)))
+    pr["algorithmic_frac_of_sustained_bf16"] = flop_alg / (pr["ms_per_step"] / 1e3) / 1e12 / \
+        peaks["bf16_tflops_sustained"]
+    out["plain_route"] = pr
 
     # the rollout's LM-head logprob GEMM (one tcgen05 GEMM launch per 38,912
     # rows + a tiny merge) over the same rows, with the lagged weights
@@ -561,6 +579,35 @@ def gemm_vs_cublas(H, W, tokens, rz, dev, stream, rows=155648, seconds=1.5, roun
     return statistics.median(res["ours"]), statistics.median(res["cublas"])
 
 
+def time_plain_route(rz, b, adv, lp, dH, dW, loss, d3, err, stream, dev, steps):
+    """The learner step through rz_loss_fwd_bwd on the same batch: 2 warm-ups,
+    `steps` timed steps, and its launch-class breakdown."""
+    import torch
+    T, d, V, B = b["T"], b["d"], b["V"], b["B"]
+    ws = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
+
+    def step():
+        rz.rz_group_advantage(b["rewards"], b["G"], adv_out=adv)
+        rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], b["logmu"], b["cu"], adv,
+                           logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
+                           err_flag=err)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    br = profile_steps(rz, step, stream, 1)
+    del ws
+    return {"entry_point": "rz_loss_fwd_bwd", "value": T / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": steps,
+            "classes_ms": {k: v["ms"] for k, v in br["classes"].items()}}
+
+
 def profile_steps(rz, step, stream, n):
     """Run n more learner steps with the library's launch-class timing on;
     returns per-step milliseconds and kernel launches of each class, their
@@ -588,8 +635,8 @@ def profile_steps(rz, step, stream, n):
 def launches_per_step(T, V):
     chunk = 38912  # rows per backward chunk at V = 151936 (2.125 bytes per logit kept)
     n_chunks = (T + chunk - 1) // chunk
-    # advantage; response factors; per chunk: logits+lse GEMM, merge+coef, dz pass, dH, dW;
-    # loss (2)
+    # advantage; response factors; per chunk: logits+lse GEMM, merge+coef, the H
+    # row scaling, dH, dW; loss (2)
     return 1 + 1 + 5 * n_chunks + 2
 
 
@@ -601,7 +648,7 @@ def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err, B_tota
     and a copy stream let step k+1's upload overlap step k's compute, as a
     training loop would run it."""
     import torch
-    host = {k: b[k].cpu().pin_memory() for k in ("H", "tokens", "logmu", "cu", "rewards")}
+    host = {k: b[k].cpu().pin_memory() for k in ("H", "tokens", "logmu", "lse", "cu", "rewards")}
     slots = [{k: torch.empty_like(b[k]) for k in host} for _ in range(2)]
     res = torch.empty(2, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -622,13 +669,13 @@ def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err, B_tota
         x = slots[i]
         rz.rz_group_advantage(x["rewards"], b["G"], adv_out=adv)
         if B_total is None:
-            rz.rz_loss_fwd_bwd(x["H"], b["W"], x["tokens"], x["logmu"], x["cu"], adv,
-                               logprob_out=lp, dH=dH, dW=dW, loss_out=loss, d3_out=d3, ws=ws,
-                               err_flag=err)
+            rz.rz_loss_fwd_bwd_ref(x["H"], b["W"], x["tokens"], x["logmu"], x["lse"], x["cu"],
+                                   adv, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
+                                   d3_out=d3, ws=ws, err_flag=err)
         else:  # one shard of the data-parallel step, then the exchange
             rz.rz_loss_fwd_bwd_shard(x["H"], b["W"], x["tokens"], x["logmu"], x["cu"], adv,
                                      B_total, logprob_out=lp, dH=dH, dW=dW, loss_out=loss,
-                                     d3_out=d3, ws=ws, err_flag=err)
+                                     d3_out=d3, ws=ws, err_flag=err, ref_lse=x["lse"])
             exchange()
         consumed[i].record(stream)
         res[0:1].copy_(loss, non_blocking=True)
@@ -655,9 +702,9 @@ def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err, B_tota
     ms = e0.elapsed_time(e1) / K
     return {"value": b["T"] / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "note": "inputs (H, tokens, log mu, cu_seqlens, rewards) uploaded from pinned host "
-                    "memory every step, the upload of step k+1 overlapping the compute of step "
-                    "k; loss and D3 read back.  W stays resident and dH, dW stay on the device "
+            "note": "inputs (H, tokens, log mu, the recorded log-sum-exp, cu_seqlens, rewards) "
+                    "uploaded from pinned host memory every step, the upload of step k+1 "
+                    "overlapping the compute of step k; loss and D3 read back.  W stays resident and dH, dW stay on the device "
                     "for an on-device optimiser, as in a training loop"}
 
 
@@ -844,7 +891,9 @@ def run_profile(args):
     """Small fixed cases for ncu captures (not a benchmark), on `--rows`
     tokens of the workload's d and V: one rollout logprob call then `--steps`
     learner steps (learner), `--steps` given-logits steps (logits), fused
-    sampling calls (sample) or rollout logprob calls (rollout)."""
+    sampling calls (sample) or rollout logprob calls (rollout).  The learner
+    steps go through rz_loss_fwd_bwd_ref (learner) or rz_loss_fwd_bwd
+    (learner_plain)."""
     import dataclasses
     import torch
     import invariant_logprobs_gb300 as rz
@@ -877,12 +926,16 @@ def run_profile(args):
         torch.cuda.synchronize()
         print("profile rollout rows=%d ok" % b["T"])
         return 0
-    logmu, _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
+    lse = torch.empty(b["T"], dtype=torch.float32, device=dev)
+    logmu, _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], lse_out=lse)
     adv = rz.rz_group_advantage(b["rewards"], b["G"])
     for _ in range(args.steps):
-        rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv)
+        if args.profile == "learner_plain":
+            rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv)
+        else:
+            rz.rz_loss_fwd_bwd_ref(b["H"], b["W"], b["tokens"], logmu, lse, b["cu"], adv)
     torch.cuda.synchronize()
-    print("profile learner rows=%d ok" % b["T"])
+    print("profile %s rows=%d ok" % (args.profile, b["T"]))
     return 0
 
 
@@ -900,7 +953,7 @@ def main():
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="time only --config (by default the other two bench workloads follow, "
                          "briefly, under other_workloads)")
-    ap.add_argument("--profile", choices=["learner", "logits", "sample", "rollout"], default=None,
+    ap.add_argument("--profile", choices=["learner", "learner_plain", "logits", "sample", "rollout"], default=None,
                     help="small fixed case for ncu captures (no timing output)")
     ap.add_argument("--rows", type=int, default=16384)
     args = ap.parse_args()

@@ -77,6 +77,7 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
 #define RZ_DEVERR_TOKEN_RANGE  1  /* a token id outside [0, V) */
 #define RZ_DEVERR_CU_SEQLENS   2  /* cu_seqlens not 0 = cu[0] <= ... <= cu[B] = T */
 #define RZ_DEVERR_TIMEOUT      4  /* a pipeline wait gave up (kernel returned early) */
+#define RZ_DEVERR_RANGE        8  /* a reference log-sum-exp too far from the row's (rz_loss_fwd_bwd_ref) */
 
 /* Operation ids for rz_workspace_size(). */
 #define RZ_OP_TOKEN_LOGPROB   0
@@ -85,6 +86,7 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
 #define RZ_OP_IS_LOSS         3
 #define RZ_OP_SAMPLE          4
 #define RZ_OP_SC_LOSS_FWD_BWD 5
+#define RZ_OP_LOSS_FWD_BWD_REF 6  /* rz_loss_fwd_bwd_ref, and rz_loss_fwd_bwd_shard with ref_lse */
 
 /*
  * Bytes of scratch the operation needs for these sizes (0 if none).  Pure
@@ -230,6 +232,40 @@ RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* to
                     rz_stream_t stream);
 
 /*
+ * rz_loss_fwd_bwd with the rollout's log-sum-exp of every row as a reference
+ * (no counterpart on the pages; the same outputs by another route).
+ *   ref_lse [T] fp32: a per-row reference R_t, normally lse_out of the
+ *   rz_token_logprob / rz_sample_logprob call that recorded logmu (the
+ *   rollout computes it in the same pass).
+ * The forward pass keeps the chunk's softmax terms against R_t instead of a
+ * running maximum: e'_tv = exp(z_tv - R_t) in bf16, so the backward pass
+ * forms dz_tv = sigma_t e'_tv with one factor per row, sigma_t =
+ * c_t exp(R_t - lse_t).  dH applies sigma_t to its rows.  dW multiplies e'
+ * with the rows of H scaled by sigma_t.  The sampled column's term is set so
+ * that its dz is c_t expm1(log pi_t).  This removes the dz pass over the
+ * chunk's terms (4 bytes per logit of HBM traffic) and the running maxima.
+ * Results equal rz_loss_fwd_bwd's within the rounding of one more bf16 step
+ * (H scaled by sigma): log pi, the loss and D3 bit for bit, dH and dW to
+ * ~1e-3 relative.
+ * Range: needs max_v z_tv - R_t <= 80 and |lse_t - R_t| <= 60 (nats) for
+ * every row.  That holds whenever the learner's weights are those of the
+ * rollout or a few updates from them; otherwise RZ_DEVERR_RANGE is set and
+ * that row's gradients are undefined (use rz_loss_fwd_bwd).
+ * Everything else (arguments, layouts, errors, determinism) as
+ * rz_loss_fwd_bwd.  Workspace: rz_workspace_size(RZ_OP_LOSS_FWD_BWD_REF, T,
+ * d, V, B) (no running maxima; the chunk's rows of H scaled, [rows, d] bf16).
+ */
+RZ_API int rz_loss_fwd_bwd_ref(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                               const float* logmu, const float* ref_lse,
+                               const int64_t* cu_seqlens, const float* adv,
+                               const uint8_t* action_mask,
+                               int32_t B, int64_t T, int32_t d, int32_t V,
+                               float* loss_out, float* d3_out, float* logprob_out,
+                               rz_bf16* dH, float* dW,
+                               void* ws, size_t ws_bytes, int32_t* err_flag,
+                               rz_stream_t stream);
+
+/*
  * One shard of a data-parallel learner step [RZ-page s.04: the method runs on
  * 16 GPUs].  The loss averages tokens within a response and responses within
  * the batch (s.02 objective), so the batch is split over ranks by whole
@@ -245,12 +281,15 @@ RZ_API int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* to
  *   dW       = the shard's partial; the batch's dW is the sum of the partials
  *              over shards (add them in a fixed order, e.g. with
  *              rz_sum_partials, for a result independent of the backend).
- * Everything else (arguments, layouts, workspace RZ_OP_LOSS_FWD_BWD with the
- * shard's B, errors) as rz_loss_fwd_bwd; B_total = B is rz_loss_fwd_bwd.
- * B_total < B returns RZ_ERR_INVALID_ARG.
+ * ref_lse (nullable): as in rz_loss_fwd_bwd_ref (the shard's rows).
+ * Everything else (arguments, layouts, errors) as rz_loss_fwd_bwd; workspace
+ * RZ_OP_LOSS_FWD_BWD (RZ_OP_LOSS_FWD_BWD_REF with ref_lse) with the shard's
+ * B.  B_total = B is rz_loss_fwd_bwd (rz_loss_fwd_bwd_ref).  B_total < B
+ * returns RZ_ERR_INVALID_ARG.
  */
 RZ_API int rz_loss_fwd_bwd_shard(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
-                                 const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                                 const float* logmu, const float* ref_lse,
+                                 const int64_t* cu_seqlens, const float* adv,
                                  const uint8_t* action_mask,
                                  int32_t B, int32_t B_total, int64_t T, int32_t d, int32_t V,
                                  float* loss_out, float* d3_out, float* logprob_out,

@@ -30,6 +30,7 @@ RZ_ERR_TOO_LARGE = 5
 RZ_DEVERR_TOKEN_RANGE = 1
 RZ_DEVERR_CU_SEQLENS = 2
 RZ_DEVERR_TIMEOUT = 4
+RZ_DEVERR_RANGE = 8
 
 RZ_PROF_NAMES = ("logprob_gemm", "keep_gemm", "merge", "dz", "dH_gemm", "dW_gemm",
                  "logits_rows", "small")  # index = RZ_PROF_* class
@@ -40,6 +41,7 @@ RZ_OP_LOGITS_LOSS = 2
 RZ_OP_IS_LOSS = 3
 RZ_OP_SAMPLE = 4
 RZ_OP_SC_LOSS_FWD_BWD = 5
+RZ_OP_LOSS_FWD_BWD_REF = 6
 
 _lib = None
 
@@ -57,8 +59,10 @@ _SIGNATURES = {
     "rz_d3": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
     "rz_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
                                        _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
-    "rz_loss_fwd_bwd_shard": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I64, _I32,
-                                             _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_loss_fwd_bwd_shard": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I64,
+                                             _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "rz_loss_fwd_bwd_ref": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32,
+                                           _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "rz_sum_partials": (ctypes.c_int, [_P, _I32, _I64, _P, _P]),
     "rz_sc_loss_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32,
                                           _P, _P, _P, _P, _P, _SZ, _P, _P]),
@@ -295,20 +299,33 @@ def rz_loss_fwd_bwd(H, W, tokens, logmu, cu_seqlens, adv, logprob_out=None, dH=N
                     want_logprob=True, action_mask=None):
     """Learner-side fused logprob + loss forward/backward (see include/rz.h).
     Returns dict(loss, d3, logprob, dH, dW) of device tensors."""
-    return _learner(None, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW, loss_out,
-                    d3_out, ws, err_flag, stream, want_logprob, action_mask)
+    return _learner(None, None, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
+                    loss_out, d3_out, ws, err_flag, stream, want_logprob, action_mask)
+
+
+def rz_loss_fwd_bwd_ref(H, W, tokens, logmu, ref_lse, cu_seqlens, adv, logprob_out=None,
+                        dH=None, dW=None, loss_out=None, d3_out=None, ws=None, err_flag=None,
+                        stream=None, want_logprob=True, action_mask=None):
+    """rz_loss_fwd_bwd with the rollout's log-sum-exp of every row (ref_lse
+    [T] fp32, e.g. the lse rz_token_logprob returned with logmu) as the
+    reference of the kept softmax terms; no dz pass (see include/rz.h)."""
+    load()
+    if ref_lse is None:
+        raise TypeError("rz_loss_fwd_bwd_ref needs ref_lse (use rz_loss_fwd_bwd without one)")
+    return _learner(None, ref_lse, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
+                    loss_out, d3_out, ws, err_flag, stream, want_logprob, action_mask)
 
 
 def rz_loss_fwd_bwd_shard(H, W, tokens, logmu, cu_seqlens, adv, B_total, logprob_out=None,
                           dH=None, dW=None, loss_out=None, d3_out=None, ws=None, err_flag=None,
-                          stream=None, want_logprob=True, action_mask=None):
+                          stream=None, want_logprob=True, action_mask=None, ref_lse=None):
     """One shard (contiguous whole responses) of a data-parallel learner step,
-    normalised by the batch's B_total responses (see include/rz.h).  Returns
-    dict(loss, d3, logprob, dH, dW): the shard's loss share, its D3, its dH
-    rows and its dW partial."""
+    normalised by the batch's B_total responses (see include/rz.h); ref_lse
+    as in rz_loss_fwd_bwd_ref.  Returns dict(loss, d3, logprob, dH, dW): the
+    shard's loss share, its D3, its dH rows and its dW partial."""
     load()
-    return _learner(int(B_total), H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
-                    loss_out, d3_out, ws, err_flag, stream, want_logprob, action_mask)
+    return _learner(int(B_total), ref_lse, H, W, tokens, logmu, cu_seqlens, adv, logprob_out,
+                    dH, dW, loss_out, d3_out, ws, err_flag, stream, want_logprob, action_mask)
 
 
 def rz_sum_partials(parts, out=None, stream=None):
@@ -332,8 +349,8 @@ def rz_sum_partials(parts, out=None, stream=None):
     return out
 
 
-def _learner(B_total, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW, loss_out,
-             d3_out, ws, err_flag, stream, want_logprob, action_mask):
+def _learner(B_total, ref_lse, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
+             loss_out, d3_out, ws, err_flag, stream, want_logprob, action_mask):
     torch = _torch()
     lib = load()
     _need(H, torch.bfloat16, "H")
@@ -350,14 +367,17 @@ def _learner(B_total, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
     _shape(logmu, (T,), "logmu")
     _shape(adv, (B,), "adv")
     _shape(action_mask, (T,), "action_mask")
+    if ref_lse is not None:
+        _need(ref_lse, torch.float32, "ref_lse")
+        _shape(ref_lse, (T,), "ref_lse")
     _out(logprob_out, torch.float32, "logprob_out", (T,))
     _out(dH, torch.bfloat16, "dH", (T, d))
     _out(dW, torch.float32, "dW", (V, d))
     _out(loss_out, torch.float32, "loss_out")
     _out(d3_out, torch.float32, "d3_out")
     _out(err_flag, torch.int32, "err_flag")
-    _same_device(H, W, tokens, logmu, cu_seqlens, adv, action_mask, logprob_out, dH, dW,
-                 loss_out, d3_out, ws, err_flag)
+    _same_device(H, W, tokens, logmu, ref_lse, cu_seqlens, adv, action_mask, logprob_out, dH,
+                 dW, loss_out, d3_out, ws, err_flag)
     dev = H.device
     if want_logprob and logprob_out is None:
         logprob_out = torch.empty(T, dtype=torch.float32, device=dev)
@@ -370,19 +390,28 @@ def _learner(B_total, H, W, tokens, logmu, cu_seqlens, adv, logprob_out, dH, dW,
     if d3_out is None:
         d3_out = torch.empty(1, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = alloc_workspace(RZ_OP_LOSS_FWD_BWD, T, d, V, B, dev)
+        ws = alloc_workspace(RZ_OP_LOSS_FWD_BWD if ref_lse is None else RZ_OP_LOSS_FWD_BWD_REF,
+                             T, d, V, B, dev)
     if action_mask is not None:
         _need(action_mask, torch.uint8, "action_mask")
-    if B_total is None:
+    if B_total is None and ref_lse is None:
         name = "rz_loss_fwd_bwd"
         st = lib.rz_loss_fwd_bwd(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(cu_seqlens),
                                  _ptr(adv), _ptr(action_mask), B, T, d, V, _ptr(loss_out),
                                  _ptr(d3_out), _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws),
                                  _ws_bytes(ws), _ptr(err_flag), _stream(stream))
+    elif B_total is None:
+        name = "rz_loss_fwd_bwd_ref"
+        st = lib.rz_loss_fwd_bwd_ref(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu), _ptr(ref_lse),
+                                     _ptr(cu_seqlens), _ptr(adv), _ptr(action_mask), B, T, d, V,
+                                     _ptr(loss_out), _ptr(d3_out), _ptr(logprob_out), _ptr(dH),
+                                     _ptr(dW), _ptr(ws), _ws_bytes(ws), _ptr(err_flag),
+                                     _stream(stream))
     else:
         name = "rz_loss_fwd_bwd_shard"
         st = lib.rz_loss_fwd_bwd_shard(_ptr(H), _ptr(W), _ptr(tokens), _ptr(logmu),
-                                       _ptr(cu_seqlens), _ptr(adv), _ptr(action_mask), B,
+                                       _ptr(ref_lse), _ptr(cu_seqlens), _ptr(adv),
+                                       _ptr(action_mask), B,
                                        B_total, T, d, V, _ptr(loss_out), _ptr(d3_out),
                                        _ptr(logprob_out), _ptr(dH), _ptr(dW), _ptr(ws),
                                        _ws_bytes(ws), _ptr(err_flag), _stream(stream))

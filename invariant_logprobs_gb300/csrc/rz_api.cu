@@ -93,9 +93,11 @@ SampleLayout sample_layout(int64_t T, int32_t V) {
 struct LearnLayout {
   int64_t rows;  // rows per chunk
   FwdLayout fwd;  // split states of one chunk
-  size_t logpi, lse_ws, coef, resp, fac, emax, ez, total;
+  size_t logpi, lse_ws, coef, resp, fac, emax, ez, hs, total;
 };
-LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
+// ref: the kept terms are taken against a per-row reference (no running
+// maxima; the chunk's rows of H scaled by sigma, bf16, for the dW GEMM).
+LearnLayout learn_layout(int64_t T, int32_t V, int32_t B, bool ref = false, int32_t d = 0) {
   LearnLayout L{};
   const size_t t = T > 0 ? static_cast<size_t>(T) : 0;
   int64_t rows = chunk_rows(V);
@@ -109,8 +111,9 @@ LearnLayout learn_layout(int64_t T, int32_t V, int32_t B) {
   L.resp = L.coef + al256(r * 4);
   L.fac = L.resp + is_loss_ws_bytes(B);
   L.emax = L.fac + resp_factors_ws_bytes(B);
-  L.ez = L.emax + al256(r * static_cast<size_t>(emax_ld(V)) * 4);
-  L.total = L.ez + al256(r * static_cast<size_t>(dz_ld(V)) * 2);
+  L.ez = L.emax + (ref ? 0 : al256(r * static_cast<size_t>(emax_ld(V)) * 4));
+  L.hs = L.ez + al256(r * static_cast<size_t>(dz_ld(V)) * 2);
+  L.total = L.hs + (ref ? al256(r * static_cast<size_t>(d > 0 ? d : 0) * 2) : 0);
   return L;
 }
 
@@ -147,8 +150,12 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
 // Centering loss (no weight, advantages centred, no log mu, no D3).
 // Bn is the response count the loss averages over: B, or the whole batch's
 // count when this call holds one shard of it (rz_loss_fwd_bwd_shard).
+// ref_lse (nullable, [T]): a per-row reference for the kept terms (the
+// rollout's log-sum-exp of the row); with it the backward pass takes the
+// terms as they are (no dz pass).
 int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
-                 const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                 const float* logmu, const float* ref_lse, const int64_t* cu_seqlens,
+                 const float* adv,
                  const uint8_t* action_mask, int32_t B, int32_t Bn, int64_t T, int32_t d,
                  int32_t V,
                  float* loss_out, float* d3_out, float* logprob_out, rz_bf16* dH, float* dW,
@@ -159,7 +166,8 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   if (B > 0 && !adv) return RZ_ERR_INVALID_ARG;
   if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
   if (!a16(W) || !a16(dW) || (T > 0 && (!a16(H) || !a16(dH)))) return RZ_ERR_UNSUPPORTED;
-  const LearnLayout L = learn_layout(T, V, B);
+  const bool ref = ref_lse != nullptr;
+  const LearnLayout L = learn_layout(T, V, B, ref, d);
   if (!ws || ws_bytes < L.total || !a256(ws)) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -186,6 +194,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   float* zg = reinterpret_cast<float*>(w8 + L.fwd.zg);
   float* emax = reinterpret_cast<float*>(w8 + L.emax);
   uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.ez);  // kept terms, then dz in place
+  uint16_t* hs = ref ? reinterpret_cast<uint16_t*>(w8 + L.hs) : nullptr;
   const int64_t ldz = dz_ld(V);
   const int64_t ldm = emax_ld(V);
   CUtensorMap tmH, tmW, tmWmn, tmHmn;
@@ -204,9 +213,13 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
 
   // Chunk by chunk in row order: logits once, folded exactly as the rollout
   // folds them, keeping the fold's terms; merge + c_t; dz in place; dH, dW.
+  // With a reference: the terms against it; merge + sigma_t and the sampled
+  // column's term; H scaled by sigma; dH (scaled rows) and dW on the terms.
   for (int64_t r0 = 0; r0 < T; r0 += L.rows) {
     const int64_t rows = (T - r0) < L.rows ? (T - r0) : L.rows;
-    CUtensorMap tmDz, tmDzMn;
+    CUtensorMap tmDz, tmDzMn, tmHsMn;
+    if (ref && !make_tmap_bf16(&tmHsMn, hs, d, rows, uint64_t(d) * 2, 64, 64))
+      return RZ_ERR_UNSUPPORTED;
     if (!make_tmap_bf16(&tmDz, dz, V, rows, uint64_t(ldz) * 2, kBK, kBM))
       return RZ_ERR_UNSUPPORTED;
     if (!make_tmap_bf16(&tmDzMn, dz, V, rows, uint64_t(ldz) * 2, 64, 64))
@@ -217,26 +230,33 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
     {
       ProfScope ps(RZ_PROF_KEEP_GEMM, 1, st);
       RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, tmE16, emax, ldm,
-                             err_flag, st));
+                             ref ? ref_lse + r0 : nullptr, err_flag, st));
     }
     {
       ProfScope ps(RZ_PROF_MERGE, 1, st);
       RZ_TRY(launch_lse_merge_coef(r0, rows, V, tokens + r0, part, zg, logpi + r0, lse_c,
                                    sc ? nullptr : logmu + r0, cu_seqlens, fac,
-                                   action_mask ? action_mask + r0 : nullptr, B, coef_c, err_flag,
-                                   st));
+                                   action_mask ? action_mask + r0 : nullptr, B, coef_c,
+                                   ref ? ref_lse + r0 : nullptr, dz, ldz, err_flag, st));
     }
-    {
+    if (ref) {
+      ProfScope ps(RZ_PROF_DZ, 1, st);
+      RZ_TRY(launch_scale_rows(H, r0, rows, d, coef_c, hs, st));
+    } else {
       ProfScope ps(RZ_PROF_DZ, 1, st);
       RZ_TRY(launch_dz_rows(dz, ldz, emax, ldm, rows, V, tokens + r0, lse_c, coef_c, logpi + r0,
                             st));
     }
     {
       ProfScope ps(RZ_PROF_DH_GEMM, 1, st);
-      RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, err_flag, st));
+      RZ_TRY(launch_dH(tmDz, tmWmn, r0, rows, d, V, dH, ref ? coef_c : nullptr, err_flag, st));
     }
     ProfScope ps(RZ_PROF_DW_GEMM, 1, st);
-    RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
+    if (ref) {
+      RZ_TRY(launch_dW(tmDzMn, tmHsMn, 0, rows, d, V, dW, r0 > 0, err_flag, st));
+    } else {
+      RZ_TRY(launch_dW(tmDzMn, tmHmn, r0, rows, d, V, dW, r0 > 0, err_flag, st));
+    }
   }
 
   // Loss (and D3) over all rows (fixed-order reductions).
@@ -271,12 +291,12 @@ const char* rz_status_string(int status) {
 }
 
 size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
-  (void)d;
   if (T < 0) T = 0;
   switch (op) {
     case RZ_OP_TOKEN_LOGPROB: return fwd_layout(T, V > 0 ? V : 1).total;
     case RZ_OP_LOSS_FWD_BWD:
     case RZ_OP_SC_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
+    case RZ_OP_LOSS_FWD_BWD_REF: return learn_layout(T, V > 0 ? V : 1, B, true, d).total;
     case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B) + resp_factors_ws_bytes(B);
     case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
     case RZ_OP_SAMPLE: return sample_layout(T, V > 0 ? V : 1).total;
@@ -384,22 +404,35 @@ int rz_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, c
                     float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
                     int32_t* err_flag, rz_stream_t stream) {
   if (!d3_out || (T > 0 && !logmu)) return RZ_ERR_INVALID_ARG;
-  return learner_step(false, H, W, tokens, logmu, cu_seqlens, adv, action_mask, B, B, T, d, V,
-                      loss_out, d3_out, logprob_out, dH, dW, ws, ws_bytes, err_flag,
+  return learner_step(false, H, W, tokens, logmu, nullptr, cu_seqlens, adv, action_mask, B, B, T,
+                      d, V, loss_out, d3_out, logprob_out, dH, dW, ws, ws_bytes, err_flag,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
+int rz_loss_fwd_bwd_ref(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
+                        const float* logmu, const float* ref_lse, const int64_t* cu_seqlens,
+                        const float* adv, const uint8_t* action_mask, int32_t B, int64_t T,
+                        int32_t d, int32_t V, float* loss_out, float* d3_out, float* logprob_out,
+                        rz_bf16* dH, float* dW, void* ws, size_t ws_bytes, int32_t* err_flag,
+                        rz_stream_t stream) {
+  if (!d3_out || (T > 0 && (!logmu || !ref_lse))) return RZ_ERR_INVALID_ARG;
+  return learner_step(false, H, W, tokens, logmu, T > 0 ? ref_lse : nullptr, cu_seqlens, adv,
+                      action_mask, B, B, T, d, V, loss_out, d3_out, logprob_out, dH, dW, ws,
+                      ws_bytes, err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int rz_loss_fwd_bwd_shard(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens,
-                          const float* logmu, const int64_t* cu_seqlens, const float* adv,
+                          const float* logmu, const float* ref_lse, const int64_t* cu_seqlens,
+                          const float* adv,
                           const uint8_t* action_mask, int32_t B, int32_t B_total, int64_t T,
                           int32_t d, int32_t V, float* loss_out, float* d3_out,
                           float* logprob_out, rz_bf16* dH, float* dW, void* ws,
                           size_t ws_bytes, int32_t* err_flag, rz_stream_t stream) {
   if (!d3_out || (T > 0 && !logmu) || B_total < B || (B_total == 0 && B > 0))
     return RZ_ERR_INVALID_ARG;
-  return learner_step(false, H, W, tokens, logmu, cu_seqlens, adv, action_mask, B, B_total, T,
-                      d, V, loss_out, d3_out, logprob_out, dH, dW, ws, ws_bytes, err_flag,
-                      reinterpret_cast<cudaStream_t>(stream));
+  return learner_step(false, H, W, tokens, logmu, T > 0 ? ref_lse : nullptr, cu_seqlens, adv,
+                      action_mask, B, B_total, T, d, V, loss_out, d3_out, logprob_out, dH, dW, ws,
+                      ws_bytes, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int rz_sum_partials(const float* parts, int32_t n_parts, int64_t count, float* out,
@@ -418,7 +451,8 @@ int rz_sc_loss_fwd_bwd(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens
                        int32_t B, int64_t T, int32_t d, int32_t V, float* loss_out,
                        float* logprob_out, rz_bf16* dH, float* dW, void* ws, size_t ws_bytes,
                        int32_t* err_flag, rz_stream_t stream) {
-  return learner_step(true, H, W, tokens, nullptr, cu_seqlens, adv, action_mask, B, B, T, d, V,
+  return learner_step(true, H, W, tokens, nullptr, nullptr, cu_seqlens, adv, action_mask, B, B, T,
+                      d, V,
                       loss_out, nullptr, logprob_out, dH, dW, ws, ws_bytes, err_flag,
                       reinterpret_cast<cudaStream_t>(stream));
 }

@@ -93,24 +93,33 @@ cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const floa
 cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
                           int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st);
-// tmE16: the chunk's fp16 terms [rows, V] (row stride dz_ld(V)), box 64 x 32.
+// tmE16: the chunk's kept terms [rows, V] (row stride dz_ld(V)), box 64 x 32:
+// fp16 with running maxima in emax, or (ref != null) bf16 against the
+// per-row reference ref [rows] (chunk-local), no maxima.
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
                             float* zgather, const CUtensorMap& tmE16, float* emax, int64_t ldm,
-                            int* err, cudaStream_t st);
+                            const float* ref, int* err, cudaStream_t st);
+// Hs[r, :] = sigma[r] H[row0 + r, :] (bf16) for one chunk's rows.
+cudaError_t launch_scale_rows(const uint16_t* H, int64_t row0, int64_t rows, int d,
+                              const float* sigma, uint16_t* Hs, cudaStream_t st);
 cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32_t* tokens,
                                   const float2* part, const float* zgather, float* logprob,
                                   float* lse_ws, const float* logmu, const int64_t* cu,
                                   const float2* fac, const uint8_t* mask, int B, float* coef,
-                                  int* err, cudaStream_t st);
+                                  const float* ref, uint16_t* ez, int64_t lde, int* err,
+                                  cudaStream_t st);
 cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t ldm,
                            int64_t rows, int V, const int32_t* tokens, const float* lse,
                            const float* coef, const float* logpi, cudaStream_t st);
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                               int V, float* out, int* err, cudaStream_t st);
+// rowscale (nullable, [rows]): dH rows multiplied by it before rounding.
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
-                      int64_t rows, int d, int V, uint16_t* dH, int* err, cudaStream_t st);
-cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t row0,
+                      int64_t rows, int d, int V, uint16_t* dH, const float* rowscale, int* err,
+                      cudaStream_t st);
+// b_row0: the chunk's first row in the B operand (0 when it holds the chunk only).
+cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t b_row0,
                       int64_t rows, int d, int V, float* dW, bool accumulate, int* err,
                       cudaStream_t st);
 

@@ -108,29 +108,49 @@ struct EpiLsePartial {
 
 // Learner pass 1 for one chunk of rows: exactly the EpiLsePartial fold (so
 // log pi is the rollout's, bit for bit), keeping what the backward pass needs
-// to form the softmax without recomputing the logits: the fold's own terms
-// e_tv = 2^((z_tv - m) log2 e) in (0, 1] as fp16, and m, the running maximum
-// they were taken against, once per 32 columns.  p_tv = e_tv 2^((m - lse_t)
-// log2 e) then needs only the row's final log-sum-exp.
-struct EpiLseKeep {
+// to form the softmax without recomputing the logits.
+//   kRef = false: the fold's own terms e_tv = 2^((z_tv - m) log2 e) in (0, 1]
+//     as fp16, and m, the running maximum they were taken against, once per
+//     32 columns; p_tv = e_tv 2^((m - lse_t) log2 e) then needs only the
+//     row's final log-sum-exp (the dz pass forms it).
+//   kRef = true: the same terms taken against one reference R_t per row
+//     (the caller's, e.g. the rollout's log-sum-exp of the row), e'_tv =
+//     2^((z_tv - R_t) log2 e) = e_tv 2^((m - R_t) log2 e), as bf16 (whose
+//     range is fp32's); p_tv = e'_tv e^(R_t - lse_t), one factor per row, so
+//     the backward GEMMs take e' as it is.  m - R_t above kRefRange (e'
+//     would overflow) raises RZ_DEVERR_RANGE and is clamped.
+constexpr float kRefRange = 80.f;  // nats
+constexpr int kErrRange = 8;       // RZ_DEVERR_RANGE
+
+template <bool kRef>
+struct EpiLseKeepT {
   struct Params {
-    CUtensorMap tm_e16;         // the terms [rows, V] fp16, box 64 x 32, 128-byte swizzle
+    CUtensorMap tm_e16;         // the terms [rows, V], box 64 x 32, 128-byte swizzle
     EpiLsePartial::Params lse;  // chunk-local rows: T = rows of the chunk
-    float* emax;                // [rows, ldm] m per 32-column slice
+    float* emax;                // [rows, ldm] m per 32-column slice (kRef: unused)
     long long ldm;              // >= ceil(V / 32), even
+    const float* ref;           // [rows] R_t (kRef only; chunk-local)
+    int* err;
   };
-  using State = EpiLsePartial::State;
+  struct State : EpiLsePartial::State {
+    float R;
+  };
 
   static __device__ __forceinline__ void task_begin(const Params& p, State& st, int m_blk,
                                                     int grp, int row) {
     EpiLsePartial::task_begin(p.lse, st, m_blk, grp, row);
+    if (kRef) {
+      const long long g = static_cast<long long>(m_blk) * kBM + row;
+      st.R = g < p.lse.T ? __ldg(p.ref + g) : 0.f;
+    }
   }
   static __device__ __forceinline__ void task_end(const Params& p, State& st, int m_blk, int grp,
                                                   int row) {
     EpiLsePartial::task_end(p.lse, st, m_blk, grp, row);
   }
 
-  // EpiLsePartial::chunk with the terms kept, packed to 16 fp16 pairs.
+  // EpiLsePartial::chunk with the terms kept, packed to 16 pairs (fp16, or
+  // bf16 against the row's reference).
   static __device__ __forceinline__ void chunk(const Params& p, State& st, const uint32_t (&r)[32],
                                                int cbase, uint32_t* w) {
     float v[32];
@@ -150,8 +170,20 @@ struct EpiLseKeep {
         if (rel == static_cast<unsigned>(j)) st.za = v[j];
       st.found = true;
     }
+    if constexpr (kRef) {
+      float gap = __fsub_rn(st.m, st.R);
+      if (!(gap <= kRefRange)) {  // also NaN
+        if (p.err) atomicOr(p.err, kErrRange);
+        gap = gap > kRefRange ? kRefRange : 0.f;
+      }
+      const float f = ex2_approx(__fmul_rn(gap, kLog2e));
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_f16x2(e[2 * j], e[2 * j + 1]);
+      for (int j = 0; j < 16; ++j)
+        w[j] = pack_bf16x2(__fmul_rn(e[2 * j], f), __fmul_rn(e[2 * j + 1], f));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = pack_f16x2(e[2 * j], e[2 * j + 1]);
+    }
   }
 
   // A 64-column slab of the warp's 32 rows goes through the warp's stage
@@ -187,8 +219,10 @@ struct EpiLseKeep {
         chunk(p, st, r1, col0 + c + 32, w + 16);
         m1 = st.m;
       }
-      mt[(c >> 5)] = m0;
-      mt[(c >> 5) + 1] = m1;
+      if (!kRef) {
+        mt[(c >> 5)] = m0;
+        mt[(c >> 5) + 1] = m1;
+      }
       if (lane == 0) bulk_wait_read();  // the previous slab's store has read the stage
       __syncwarp();
 #pragma unroll
@@ -205,7 +239,8 @@ struct EpiLseKeep {
     // the tile's running maxima, one per 32-column slice, written together
     // (two 16-byte stores per row: ldm is a multiple of 4 and col0 / 32 of 8)
     const int nsl = (V - col0 + 31) >> 5;  // valid 32-column slices of this tile
-    if (grow < p.lse.T && RZ_DCHECK(grow >= 0 && (col0 >> 5) + (nsl < 8 ? nsl : 8) <= p.ldm, 11)) {
+    if (!kRef && grow < p.lse.T &&
+        RZ_DCHECK(grow >= 0 && (col0 >> 5) + (nsl < 8 ? nsl : 8) <= p.ldm, 11)) {
       float* em = p.emax + grow * p.ldm + (col0 >> 5);
       if (nsl >= 8) {
         reinterpret_cast<float4*>(em)[0] = make_float4(mt[0], mt[1], mt[2], mt[3]);
@@ -218,6 +253,9 @@ struct EpiLseKeep {
     }
   }
 };
+
+using EpiLseKeep = EpiLseKeepT<false>;
+using EpiLseKeepRef = EpiLseKeepT<true>;
 
 // Philox4x32 with 10 rounds (Salmon et al., "Parallel Random Numbers: As
 // Easy as 1, 2, 3", SC 2011): each round multiplies c0 and c2 by fixed odd
@@ -448,7 +486,8 @@ struct EpiSample {
 
 // Plain stores of the accumulator: bf16 (dH) or fp32 (logits), optionally
 // fp32 accumulate (dW over token chunks, in chunk order).
-template <int kMode>  // 0: bf16 store, 1: fp32 store, 2: fp32 accumulate-or-store
+template <int kMode>  // 0: bf16 store, 1: fp32 store, 2: fp32 accumulate-or-store,
+                     // 3: bf16 store of the row times rowscale[row]
 struct EpiStore {
   struct Params {
     void* out;
@@ -457,6 +496,7 @@ struct EpiStore {
     long long rows;  // valid rows (block-local numbering)
     int cols;        // valid columns
     int accumulate;  // mode 2 only
+    const float* rowscale;  // mode 3 only: [rows] (block-local)
   };
   struct State {};
 
@@ -467,20 +507,26 @@ struct EpiStore {
                                                int cbase) {
     if (!RZ_DCHECK(rr >= 0 && rr < p.rows && cbase >= 0 && cbase < p.cols && p.cols <= p.ld, 14))
       return;
-    if (kMode == 0) {
+    if (kMode == 0 || kMode == 3) {
+      const float sc = kMode == 3 ? p.rowscale[rr] : 1.f;
       uint16_t* dst = static_cast<uint16_t*>(p.out) + (p.row0 + rr) * p.ld + cbase;
       if (cbase + 32 <= p.cols) {
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          w[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          w[j] = kMode == 3 ? pack_bf16x2(__fmul_rn(sc, __uint_as_float(r[2 * j])),
+                                          __fmul_rn(sc, __uint_as_float(r[2 * j + 1])))
+                            : pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           st_global_v4(dst + 8 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       } else {
         for (int j = 0; j < 32; ++j)
           if (cbase + j < p.cols)
-            dst[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xffffu);
+            dst[j] = static_cast<uint16_t>(
+                pack_bf16x2(kMode == 3 ? __fmul_rn(sc, __uint_as_float(r[j])) : __uint_as_float(r[j]),
+                            0.f) &
+                0xffffu);
       }
     } else {
       float* dst = static_cast<float*>(p.out) + (p.row0 + rr) * p.ld + cbase;
@@ -565,6 +611,14 @@ __global__ void lse_merge_kernel(long long T, int V, int S, const int32_t* __res
 // holds the centred advantages), 0 for a masked token.
 // fac[i] = (A_i, 1/(B T_i)).  Response of a row: the last i with
 // cu[i] <= row (empty responses own no row).
+// With a per-row reference (ref, the kept terms e' = 2^((z - R) log2 e) in
+// bf16): coef becomes the row factor sigma_t = c_t e^(R_t - lse_t) of
+// dz_tv = sigma_t e'_tv, and the sampled column's term is overwritten with
+// expm1(log pi_t) e^(lse_t - R_t), so that sigma_t times it is
+// c_t expm1(log pi_t) (no cancellation of p - 1 as p -> 1).  |lse - R|
+// above kRefGap raises RZ_DEVERR_RANGE (sigma would lose its digits).
+constexpr float kRefGap = 60.f;  // nats
+
 __global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long row0,
                                       const int32_t* __restrict__ tokens,
                                       const float2* __restrict__ part,
@@ -574,7 +628,8 @@ __global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long ro
                                       const int64_t* __restrict__ cu,
                                       const float2* __restrict__ fac,
                                       const uint8_t* __restrict__ mask, int B,
-                                      float* __restrict__ coef, int* err) {
+                                      float* __restrict__ coef, const float* __restrict__ ref,
+                                      uint16_t* __restrict__ ez, long long lde, int* err) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= rows) return;
   float l;
@@ -591,7 +646,40 @@ __global__ void lse_merge_coef_kernel(long long rows, int V, int S, long long ro
   const bool act = !mask || mask[t] != 0;
   const float2 f = fac[lo];
   const float w = logmu ? is_weight(lp, logmu[t]) : 1.f;
-  coef[t] = act ? f.x * w * f.y : 0.f;
+  const float c = act ? f.x * w * f.y : 0.f;
+  if (!ref) {
+    coef[t] = c;
+    return;
+  }
+  const float R = ref[t];
+  const float gap = __fsub_rn(l, R);
+  if (!(fabsf(gap) <= kRefGap) && err) atomicOr(err, kErrRange);
+  coef[t] = __fmul_rn(c, expf(-gap));
+  const int a = tokens[t];
+  if (a >= 0 && a < V)
+    ez[t * lde + a] = static_cast<uint16_t>(pack_bf16x2(__fmul_rn(expm1f(lp), expf(gap)), 0.f) &
+                                            0xffffu);
+}
+
+// H'[r, :] = sigma_r H[row0 + r, :] in bf16 for the rows of one chunk: the B
+// operand of dW = e'^T H' when the kept terms are taken against a per-row
+// reference.  One CTA per row, 16-byte vectors (d % 8 == 0).
+__global__ void scale_rows_kernel(const uint16_t* __restrict__ H, long long row0, int d,
+                                  const float* __restrict__ sigma, uint16_t* __restrict__ Hs) {
+  const long long r = blockIdx.x;
+  const float sg = sigma[r];
+  const uint4* src = reinterpret_cast<const uint4*>(H + (row0 + r) * d);
+  uint4* dst = reinterpret_cast<uint4*>(Hs + r * d);
+  for (int i = threadIdx.x; i < (d >> 3); i += blockDim.x) {
+    const uint4 q = __ldg(src + i);
+    const uint32_t in[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = pack_bf16x2(__fmul_rn(sg, __uint_as_float(in[j] << 16)),
+                         __fmul_rn(sg, __uint_as_float(in[j] & 0xffff0000u)));
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // ============================================================== dz pass
@@ -812,28 +900,40 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
                             float* zgather, const CUtensorMap& tmE16, float* emax, int64_t ldm,
-                            int* err, cudaStream_t st) {
+                            const float* ref, int* err, cudaStream_t st) {
   const int S = vocab_splits(V);
   GemmSched s = sched_of(rows, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
   s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
-  EpiLseKeep::Params p{tmE16, {tokens, part, zgather, static_cast<long long>(rows), V, S}, emax,
-                       ldm};
+  const EpiLsePartial::Params lp{tokens, part, zgather, static_cast<long long>(rows), V, S};
+  if (ref) {
+    EpiLseKeepRef::Params p{tmE16, lp, nullptr, ldm, ref, err};
+    return run_gemm<EpiLseKeepRef, false, false>(tmH, tmW, s, p, st);
+  }
+  EpiLseKeep::Params p{tmE16, lp, emax, ldm, nullptr, err};
   return run_gemm<EpiLseKeep, false, false>(tmH, tmW, s, p, st);
+}
+
+cudaError_t launch_scale_rows(const uint16_t* H, int64_t row0, int64_t rows, int d,
+                              const float* sigma, uint16_t* Hs, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  scale_rows_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(H, row0, d, sigma, Hs);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge_coef(int64_t row0, int64_t rows, int V, const int32_t* tokens,
                                   const float2* part, const float* zgather, float* logprob,
                                   float* lse_ws, const float* logmu, const int64_t* cu,
                                   const float2* fac, const uint8_t* mask, int B, float* coef,
-                                  int* err, cudaStream_t st) {
+                                  const float* ref, uint16_t* ez, int64_t lde, int* err,
+                                  cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (rows + threads - 1) / threads;
   lse_merge_coef_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
       rows, V, vocab_splits(V), row0, tokens, part, zgather, logprob, lse_ws, logmu, cu, fac,
-      mask, B, coef, err);
+      mask, B, coef, ref, ez, lde, err);
   return cudaGetLastError();
 }
 
@@ -863,10 +963,15 @@ cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, in
 }
 
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
-                      int64_t rows, int d, int V, uint16_t* dH, int* err, cudaStream_t st) {
+                      int64_t rows, int d, int V, uint16_t* dH, const float* rowscale, int* err,
+                      cudaStream_t st) {
   const int nt = (d + kBN - 1) / kBN;
   GemmSched s = sched_of(rows, d, nt, V, err);
-  EpiStore<0>::Params p{dH, d, row0, rows, d, 0};
+  if (rowscale) {
+    EpiStore<3>::Params p{dH, d, row0, rows, d, 0, rowscale};
+    return run_gemm<EpiStore<3>, false, true>(tmDz, tmWmn, s, p, st);
+  }
+  EpiStore<0>::Params p{dH, d, row0, rows, d, 0, nullptr};
   return run_gemm<EpiStore<0>, false, true>(tmDz, tmWmn, s, p, st);
 }
 
@@ -880,12 +985,12 @@ cudaError_t check_read_lmhead(unsigned int* count, int* site) {
 #endif
 }
 
-cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t row0,
+cudaError_t launch_dW(const CUtensorMap& tmDzMn, const CUtensorMap& tmHmn, int64_t b_row0,
                       int64_t rows, int d, int V, float* dW, bool accumulate, int* err,
                       cudaStream_t st) {
   const int nt = (d + kBN - 1) / kBN;
   GemmSched s = sched_of(V, d, nt, rows, err);
-  s.b_k_off = static_cast<int>(row0);
+  s.b_k_off = static_cast<int>(b_row0);
   EpiStore<2>::Params p{dW, d, 0, V, d, accumulate ? 1 : 0};
   return run_gemm<EpiStore<2>, true, true>(tmDzMn, tmHmn, s, p, st);
 }

@@ -127,13 +127,26 @@ def test_host_side_argument_checks(lib):
     assert lib.rz_d3(fake, fake, -1, fake, null) == 1
     # shard of a data-parallel step: the batch cannot hold fewer responses
     # than the shard, nor none when the shard has some
-    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, fake, fake, null, 4, 3, 5, 16, 100,
-                                     fake, fake, null, fake, fake, fake, 1 << 30, null, null) == 1
-    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, fake, fake, null, 4, 0, 5, 16, 100,
-                                     fake, fake, null, fake, fake, fake, 1 << 30, null, null) == 1
+    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, null, fake, fake, null, 4, 3, 5, 16,
+                                     100, fake, fake, null, fake, fake, fake, 1 << 30, null,
+                                     null) == 1
+    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, null, fake, fake, null, 4, 0, 5, 16,
+                                     100, fake, fake, null, fake, fake, fake, 1 << 30, null,
+                                     null) == 1
     # ... and is otherwise checked as rz_loss_fwd_bwd (d % 8 answers 2)
-    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, fake, fake, null, 4, 8, 5, 12, 100,
-                                     fake, fake, null, fake, fake, null, 0, null, null) == 2
+    assert lib.rz_loss_fwd_bwd_shard(fake, fake, fake, fake, null, fake, fake, null, 4, 8, 5, 12,
+                                     100, fake, fake, null, fake, fake, null, 0, null, null) == 2
+    # the reference variant needs its reference rows
+    assert lib.rz_loss_fwd_bwd_ref(fake, fake, fake, fake, null, fake, fake, null, 2, 5, 16, 100,
+                                   fake, fake, null, fake, fake, fake, 1 << 30, null, null) == 1
+    assert lib.rz_loss_fwd_bwd_ref(fake, fake, fake, fake, fake, fake, fake, null, 2, 5, 12, 100,
+                                   fake, fake, null, fake, fake, null, 0, null, null) == 2
+    # its workspace has no running maxima but the chunk's rows of H scaled
+    T, d, V, B = 5000, 512, 151936, 8
+    plain = lib.rz_workspace_size(1, T, d, V, B)
+    ref = lib.rz_workspace_size(6, T, d, V, B)
+    rows = 5120  # the chunk of 5,000 rows, rounded to whole 128-row blocks
+    assert ref - plain == rows * d * 2 - rows * ((V + 127) // 128 * 4) * 4
     # the exchange sum: at least one part, non-negative count, pointers
     assert lib.rz_sum_partials(fake, 0, 10, fake, null) == 1
     assert lib.rz_sum_partials(fake, 2, -1, fake, null) == 1

@@ -11,8 +11,9 @@ identities that hold at any size:
   * the loss/D3 of the fused call equal rz_is_loss on its own log pi bit for
     bit, and D3 >= 0.
 
-log mu comes from torch's bf16 matmul + log_softmax with the lagged weights
-(the behaviour policy of the workload), never from this library.
+log mu (and, for the reference route, the row's log-sum-exp) comes from
+torch's bf16 matmul + log_softmax with the lagged weights (the behaviour
+policy of the workload), never from this library.
 """
 
 import numpy as np
@@ -28,24 +29,36 @@ DEV = "cuda"
 
 
 def _behaviour_logprob(H, W_mu, tokens, chunk=4096):
+    """log mu of each row's token and the row's log-sum-exp under the lagged
+    weights, from torch's bf16 matmul + log_softmax."""
     out = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
+    lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
     for s in range(0, H.shape[0], chunk):
         e = min(H.shape[0], s + chunk)
-        z = torch.log_softmax((H[s:e] @ W_mu.t()).float(), dim=-1)
+        zz = (H[s:e] @ W_mu.t()).float()
+        lse[s:e] = torch.logsumexp(zz, dim=-1)
+        z = torch.log_softmax(zz, dim=-1)
         out[s:e] = z.gather(1, tokens[s:e].long()[:, None])[:, 0]
-    return out
+    return out, lse
 
 
-@pytest.mark.parametrize("name", ["qwen1p5b_lag2", "qwen4b_lag64"])
-def test_learner_full_size_sampled(rz, name):
+@pytest.mark.parametrize("name,route", [("qwen1p5b_lag2", "plain"), ("qwen4b_lag64", "plain"),
+                                        ("qwen1p5b_lag2", "ref"), ("qwen4b_lag64", "ref")])
+def test_learner_full_size_sampled(rz, name, route):
+    """route "ref": rz_loss_fwd_bwd_ref with the behaviour policy's
+    log-sum-exp of every row as the reference (the bench's route)."""
     wl = synth.WORKLOADS[name]
     b = synth.make_batch(wl, device=DEV)
     T, d, V, B = b["T"], b["d"], b["V"], b["B"]
-    logmu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
+    logmu, lse_mu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
     A32 = oracle.group_advantage(f64(b["rewards"]), b["G"]).astype(np.float32)
     adv = torch.tensor(A32, device=DEV)
     err = rz.new_err_flag(DEV)
-    out = rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv, err_flag=err)
+    if route == "ref":
+        out = rz.rz_loss_fwd_bwd_ref(b["H"], b["W"], b["tokens"], logmu, lse_mu, b["cu"], adv,
+                                     err_flag=err)
+    else:
+        out = rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"], adv, err_flag=err)
     loss2, d32, _ = rz.rz_is_loss(out["logprob"], logmu, b["cu"], adv)
     torch.cuda.synchronize()
     assert err.item() == 0

@@ -36,12 +36,17 @@ ROW_REL_L2 = 2e-2           # per dH row and per dW vocabulary row (see row_erro
 
 
 def _behaviour_logprob(H, W_mu, tokens, chunk=4096):
+    """log mu of each row's token and the row's log-sum-exp under the lagged
+    weights, from torch's bf16 matmul + log_softmax."""
     out = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
+    lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
     for s in range(0, H.shape[0], chunk):
         e = min(H.shape[0], s + chunk)
-        z = torch.log_softmax((H[s:e] @ W_mu.t()).float(), dim=-1)
+        zz = (H[s:e] @ W_mu.t()).float()
+        lse[s:e] = torch.logsumexp(zz, dim=-1)
+        z = torch.log_softmax(zz, dim=-1)
         out[s:e] = z.gather(1, tokens[s:e].long()[:, None])[:, 0]
-    return out
+    return out, lse
 
 
 def row_errors(got, want):
@@ -64,7 +69,7 @@ def test_two_chunk_full_vocab_gradients_vs_oracle(rz):
     T, d, V, B = b["T"], b["d"], b["V"], b["B"]
     assert (d, V) == (1536, 151936)
     assert CHUNK_ROWS < T < 2 * CHUNK_ROWS and (T - CHUNK_ROWS) % 128 != 0
-    logmu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
+    logmu, lse_mu = _behaviour_logprob(b["H"], b["W_mu"], b["tokens"])
     A32 = oracle.group_advantage(f64(b["rewards"]), b["G"]).astype(np.float32)
     err = rz.new_err_flag(DEV)
     out = rz.rz_loss_fwd_bwd(b["H"], b["W"], b["tokens"], logmu, b["cu"],
@@ -73,6 +78,17 @@ def test_two_chunk_full_vocab_gradients_vs_oracle(rz):
     assert err.item() == 0
     got = {k: f64(out[k]) for k in ("logprob", "dH", "dW")}
     loss, d3 = out["loss"].item(), out["d3"].item()
+    del out
+    # the same step through the per-row reference route (the behaviour
+    # policy's log-sum-exp as the reference)
+    out = rz.rz_loss_fwd_bwd_ref(b["H"], b["W"], b["tokens"], logmu, lse_mu, b["cu"],
+                                 torch.tensor(A32, device=DEV), err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got_ref = {k: f64(out[k]) for k in ("dH", "dW")}
+    assert np.array_equal(bits(out["logprob"]), bits(torch.tensor(got["logprob"],
+                                                                  dtype=torch.float32)))
+    assert out["loss"].item() == loss and out["d3"].item() == d3
     del out
     torch.cuda.empty_cache()
 
@@ -91,6 +107,14 @@ def test_two_chunk_full_vocab_gradients_vs_oracle(rz):
     assert r_dW.max() <= ROW_REL_L2, (int(r_dW.argmax()), r_dW.max(), np.median(r_dW))
     # both chunks are held to the same bar
     assert r_dH[:CHUNK_ROWS].max() <= ROW_REL_L2 and r_dH[CHUNK_ROWS:].max() <= ROW_REL_L2
+    # the reference route, element by element and row by row as well
+    e2_dH, e2_dW = rel_l2(got_ref["dH"], ref["dH"]), rel_l2(got_ref["dW"], ref["dW"])
+    assert e2_dH <= TOL_GRAD_REL_L2 and e2_dW <= TOL_GRAD_REL_L2, (e2_dH, e2_dW)
+    r2_dH = row_errors(got_ref["dH"], ref["dH"])
+    r2_dW = row_errors(got_ref["dW"], ref["dW"])
+    assert r2_dH.max() <= ROW_REL_L2 and r2_dW.max() <= ROW_REL_L2, (r2_dH.max(), r2_dW.max())
+    print("two-chunk reference route: dH rel L2 %.2e (rows max %.2e); dW rel L2 %.2e "
+          "(vocab rows max %.2e)" % (e2_dH, r2_dH.max(), e2_dW, r2_dW.max()))
     print("two-chunk T=%d: |dlogpi| max %.2e; loss rel %.2e; d3 rel %.2e; dH rel L2 %.2e "
           "(rows: median %.2e, max %.2e); dW rel L2 %.2e (vocab rows: median %.2e, max %.2e)"
           % (T, np.max(np.abs(got["logprob"] - ref["logpi"])),

@@ -22,7 +22,8 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     for name in ("rz_token_logprob", "rz_loss_fwd_bwd", "rz_sc_loss_fwd_bwd",
                  "rz_logits_loss_fwd_bwd", "rz_group_advantage", "rz_is_loss", "rz_d3",
                  "rz_is_stats", "rz_lmhead_logits", "rz_sample_logprob",
-                 "rz_token_logprob_noalloc", "rz_loss_fwd_bwd_shard", "rz_sum_partials"):
+                 "rz_token_logprob_noalloc", "rz_loss_fwd_bwd_shard", "rz_sum_partials",
+                 "rz_loss_fwd_bwd_ref"):
         fn = getattr(rz, name)
         n_required = fn.__code__.co_argcount - len(fn.__defaults__ or ())
         with pytest.raises(RuntimeError, match="not built"):
