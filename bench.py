@@ -45,10 +45,11 @@ TRAFFIC_CAPTURES = {
     # such groups (x4)
     "qwen4b_lag64": {"bytes": 4 * (1.939186688e9 + 2.946383872e9), "sources": GEMM_SOURCES,
                      "sources_sha256_16": "2b95a6e69c093685"},
-    # given-logits row kernel: 6.545 GB read + 4.893 GB written at 16,384
-    # rows, scaled to the workload's 262,144 rows (x16)
-    "moe30b_logits": {"bytes": 16 * (6.545230592e9 + 4.892545792e9), "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "b957b32599bf73bc"},
+    # given-logits row kernel (768 threads, two rows per SM): 5.370 GB read
+    # + 4.893 GB written at 16,384 rows, scaled to the workload's 262,144
+    # rows (x16)
+    "moe30b_logits": {"bytes": 16 * (5.370281728e9 + 4.892990208e9), "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "7cc3d34b71cc5948"},
 }
 
 

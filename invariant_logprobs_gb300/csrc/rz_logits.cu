@@ -4,9 +4,10 @@
 //
 // Purely bandwidth-bound (no contraction): one CTA streams one row with
 // 16-byte loads, four in flight per thread.  Pass 1 computes (max, sum exp)
-// online and keeps the first 64 KB of the row in shared memory; pass 2
-// re-reads the rest (mostly from L2) and overwrites the row with dz.  Three
-// CTAs per SM keep ~456 rows in flight, their re-read parts inside the L2.
+// online and keeps the first 96 KB of the row in shared memory; pass 2
+// re-reads the rest (mostly from L2) and overwrites the row with dz.  Two
+// CTAs of 768 threads per SM keep ~304 rows in flight, their re-read parts
+// inside the L2.
 // The loss and D3 over all rows are then reduced by the same fixed-order
 // kernels as the hidden-state path.
 #include <cuda_runtime.h>
@@ -23,18 +24,23 @@ namespace rz {
 
 namespace {
 
-constexpr int kRowThreads = 512;
-// 64 KB of each row kept in shared memory: three rows per SM in flight, and
-// the rest of their rows (re-read in pass 2, ~240 KB each at V = 151936,
-// ~109 MB over 456 rows) still fits the L2.  (96 KB and two rows per SM:
-// 30.6 ms per 262,144-row step; 64 KB and three: 27.5 ms; 72 KB no longer
-// fits three per SM.)
-constexpr int kStashVec = 4096;
+constexpr int kRowThreads = 768;
+constexpr int kRowsPerSm = 2;
+// 96 KB of each row kept in shared memory: two rows per SM in flight, and
+// the rest of their rows (re-read in pass 2, ~208 KB each at V = 151936,
+// ~63 MB over 304 rows) stays in the L2.  Measured per 262,144-row step at
+// V = 151936: 512 threads, 64 KB stash, three rows per SM: 27.5 ms; 768
+// threads, 96 KB, two rows: 26.2 ms.  With 768 threads the time is touchy
+// in the stash size: 80 KB 30.0 ms, 88 KB 27.5 ms, 104 KB 30.2 ms; forcing
+// the shared-memory carveout to its maximum makes 96 KB take 30.5 ms, and
+// predicating the last four-wide round instead of finishing with single
+// loads 30.4 ms.
+constexpr int kStashVec = 6144;
 constexpr size_t kRowSmem = kStashVec * sizeof(uint4);
 
 // L2 eviction priorities: the part of a row that pass 2 will read again from
 // L2 is loaded evict-last; everything read for the last time, and the dz
-// written back, is evict-first, so ~300 rows in flight keep their second
+// written back, is evict-first, so the rows in flight keep their second
 // halves resident in the 129 MB L2.
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
@@ -92,7 +98,7 @@ __device__ __forceinline__ uint4 dz8(const uint4& q, float M, float nl2s, float 
   return o;
 }
 
-__global__ void __launch_bounds__(kRowThreads, 3)  // three rows per SM (<= 42 registers)
+__global__ void __launch_bounds__(kRowThreads, kRowsPerSm)  // <= 42 registers
     logits_row_kernel(uint16_t* __restrict__ logits, long long T, int V,
                       const int32_t* __restrict__ tokens, const float* __restrict__ logmu,
                       const int64_t* __restrict__ cu, const float2* __restrict__ fac,
