@@ -696,7 +696,7 @@ def run_e2e(args, b, rz, dev, stream, ws, dH, dW, lp, loss, d3, adv, err, B_tota
         torch.cuda.synchronize()
 
     run(2)
-    K = max(2, min(args.steps, 4))
+    K = max(2, min(args.steps, 8))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     run(K, e0, e1)

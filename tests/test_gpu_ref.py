@@ -192,3 +192,38 @@ def test_ref_sharded_equals_unsharded(rz):
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(dHs).view(torch.int16), full["dH"].view(torch.int16))
     assert rel_l2(f64(dW), f64(full["dW"])) <= 1e-4
+
+
+@pytest.mark.parametrize("cuts,d,V,seed", [([0, 0, 3, 3, 10, 10], 200, 777, 5),
+                                           ([0, 1], 64, 1000, 6)])
+def test_ref_empty_responses_and_single_row(rz, cuts, d, V, seed):
+    """Empty responses (first, middle and last) and a one-row batch on the
+    reference route, against the oracle and the plain route."""
+    g = torch.Generator().manual_seed(seed)
+    T = cuts[-1]
+    H = _rand_bf16((T, d), 1.0, g)
+    W = _rand_bf16((V, d), 0.05, g)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    cu = torch.tensor(cuts, dtype=torch.int64)
+    adv = torch.randn(len(cuts) - 1, generator=g)
+    lm, R = _rollout(rz, H.to(DEV), W.to(DEV), tok.to(DEV))
+    lm = lm + 0.05 * torch.randn(T, generator=g).to(DEV)
+    out = _both(rz, H.to(DEV), W.to(DEV), tok.to(DEV), lm, R, cu.to(DEV), adv.to(DEV))
+    ref = oracle.loss_fwd_bwd(f64(H), f64(W), f64(tok), f64(lm), f64(cu), f64(adv))
+    _check(out, ref)
+
+
+def test_ref_nan_reference_sets_the_range_flag(rz):
+    g = torch.Generator().manual_seed(8)
+    T, d, V = 200, 64, 1500
+    H = _rand_bf16((T, d), 1.0, g).to(DEV)
+    W = _rand_bf16((V, d), 0.1, g).to(DEV)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32).to(DEV)
+    cu = torch.tensor([0, 120, T], dtype=torch.int64, device=DEV)
+    adv = torch.tensor([0.5, -0.5], device=DEV)
+    lm, R = _rollout(rz, H, W, tok)
+    R[37] = float("nan")
+    err = rz.new_err_flag(DEV)
+    rz.rz_loss_fwd_bwd_ref(H, W, tok, lm, R, cu, adv, err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() & rz.RZ_DEVERR_RANGE
