@@ -133,14 +133,32 @@ def _zero_mismatch(rz, T, d, V, seed):
                     torch.full((1,), T, dtype=torch.int64, device=DEV)])
     adv = rz.rz_group_advantage(torch.rand(n_resp, generator=g, device=DEV), 8)
     err = rz.new_err_flag(DEV)
-    # the rollout records log mu with the same weights the learner holds
-    logmu, _ = rz.rz_token_logprob(H, W, tokens, err_flag=err)
+    # the rollout records log mu (and each row's log-sum-exp) with the same
+    # weights the learner holds
+    lse = torch.empty(T, dtype=torch.float32, device=DEV)
+    logmu, _ = rz.rz_token_logprob(H, W, tokens, err_flag=err, lse_out=lse)
     ws_bytes = rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, n_resp)
     out = rz.rz_loss_fwd_bwd(H, W, tokens, logmu, cu, adv, err_flag=err)
     torch.cuda.synchronize()
     assert err.item() == 0
     assert np.array_equal(bits(out["logprob"]), bits(logmu))
     assert out["d3"].item() == 0.0
+    # the reference route over the same chunks: the same log pi, loss and D3
+    # bits, gradients to rounding.  The routes round in different places
+    # (bf16 terms against the reference and a scaled H, against bf16 dz), and
+    # a dH element here sums up to 2^24 rounded terms before its own bf16
+    # rounding; each route is held to rel L2 1e-2 against the oracle
+    # (test_two_chunk_full_vocab_gradients_vs_oracle), and so is their
+    # difference here (measured 5.9e-3 for dH at V = 2^24).
+    out_r = rz.rz_loss_fwd_bwd_ref(H, W, tokens, logmu, lse, cu, adv, err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(bits(out_r["logprob"]), bits(logmu))
+    assert out_r["d3"].item() == 0.0
+    assert np.array_equal(bits(out_r["loss"]), bits(out["loss"]))
+    assert rel_l2(f64(out_r["dH"]), f64(out["dH"])) <= TOL_GRAD_REL_L2
+    assert rel_l2(f64(out_r["dW"]), f64(out["dW"])) <= TOL_GRAD_REL_L2
+    del out_r
     # w == 1 exactly: the loss is -(1/B) sum_i A_i, the same as rz_is_loss
     # gives for log pi == log mu
     loss2, d32, _ = rz.rz_is_loss(logmu, logmu, cu, adv)
