@@ -105,10 +105,11 @@ RZ_API const char* rz_status_string(int status);
  *   tokens  [T] int32     sampled token ids
  *   logprob_out [T] fp32  log pi(a_t|h_t) = z_{t,a_t} - logsumexp_v z_tv,
  *                         z = H W^T (fp32 accumulation, temperature 1)
- *   lse_out [T] fp32      logsumexp_v z_tv (nullable)
+ *   lse_out [T] fp32      logsumexp_v z_tv (nullable); the reference that
+ *                         rz_loss_fwd_bwd_ref takes for each row
  * Rows whose token is out of range get NaN and set RZ_DEVERR_TOKEN_RANGE.
  * Rows are processed in blocks of 38,912 (one GEMM launch each).  The learner
- * side (rz_loss_fwd_bwd) runs this very computation -- the same tiles, K
+ * side (rz_loss_fwd_bwd, rz_loss_fwd_bwd_ref) runs this very computation -- the same tiles, K
  * order, vocab splits and log-sum-exp fold, only keeping more of it for its
  * backward pass -- so both sides agree bit for bit at equal weights
  * [vLLM-zh s.5 "diff 0"].
@@ -124,14 +125,22 @@ RZ_API int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* t
  * z = H W^T at temperature 1, and records log mu(a_t) in the same pass over
  * the logits [vLLM-zh s.4 item 2: the rollout records the logprob of every
  * token it samples; the pages do not say how it samples].
- * Sampling rule (a reading, exact in law): Gumbel-max,
- *   a_t = argmax_v z_tv + G_tv,  G = -log(-log U),  ties -> smaller v,
- * with U_tv = ((x >> 9) + 1/2) 2^-23 and x = word (v mod 4) of
- * Philox4x32-10 (Salmon et al., SC 2011) at counter
- * (v / 4, row_id low 32 bits, row_id high 32 bits, 0) under key
- * (seed low, seed high).  row_ids [T] int64 (nullable: the row index t)
- * makes a row's sample depend only on its own id, hidden state and W --
- * never on the batch it sits in.
+ * Sampling rule (a reading, exact in law): a two-level weighted reservoir
+ * over the row's vocabulary in ascending order, q_v = exp(z_tv - max z_t).
+ * Inside each vocab split (the log-sum-exp's splits: whole 256-column
+ * tiles, a function of V only) the 32-column chunks c come in order; chunk
+ * c becomes the split's candidate when U1 R < Q, Q its sum of q and R the
+ * running sum including it, and the token inside the chunk is the first
+ * column, visited by class (column mod 4) then by column, at which the
+ * running sum of q passes U2 Q.  The splits are taken in order the same
+ * way with U3 against the running sum of their totals.  Every token is drawn
+ * with probability exactly q_v / sum q.  U = ((x >> 9) + 1/2) 2^-23 for a
+ * word x of Philox4x32-10 (Salmon et al., SC 2011) under key (seed low,
+ * seed high): U1, U2 = words 0, 1 at counter (c, row_id low 32 bits,
+ * row_id high 32 bits, 0); U3 = word 0 at counter (split, row_id low,
+ * row_id high, 1).  row_ids [T] int64 (nullable: the row index t) makes a
+ * row's sample depend only on its own id, hidden state and W -- never on
+ * the batch it sits in.
  *   tokens_out [T] int32, logprob_out [T] fp32 (log mu of the sampled
  *   token), lse_out [T] fp32 (nullable).
  * logprob_out is bitwise equal to what rz_token_logprob (and the learner in

@@ -1,6 +1,6 @@
 """Pins for the sampler oracle: the generator against its published
-known-answer vectors, and the Gumbel-max rule against the closed-form
-softmax probabilities it must reproduce."""
+known-answer vectors, and the two-level weighted reservoir against the
+closed-form softmax probabilities it must reproduce."""
 
 import math
 import os
