@@ -44,21 +44,27 @@ TRAFFIC_CAPTURES = {
     # 9,728 rows (one raster group of 76 m-blocks); a 38,912-row chunk is four
     # such groups (x4)
     "qwen4b_lag64": {"bytes": 4 * (1.939186688e9 + 2.946383872e9), "sources": GEMM_SOURCES,
-                     "sources_sha256_16": "2b95a6e69c093685"},
+                     "sources_sha256_16": "4e911367721b954a"},
     # given-logits row kernel (768 threads, two rows per SM): 5.370 GB read
     # + 4.893 GB written at 16,384 rows, scaled to the workload's 262,144
     # rows (x16)
     "moe30b_logits": {"bytes": 16 * (5.370281728e9 + 4.892990208e9), "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "7cc3d34b71cc5948"},
+                      "sources_sha256_16": "26417f2cefb70ada"},
 }
 
 
 def sources_hash(files):
+    """Hash of the kernel sources with comments and blank space removed, so a
+    comment edit does not retire a capture of unchanged code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "invariant_logprobs_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "invariant_logprobs_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

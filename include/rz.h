@@ -448,7 +448,8 @@ RZ_API size_t rz_noalloc_scratch_bytes(void);
 #define RZ_PROF_LOGPROB_GEMM 0  /* rollout logprob GEMM; fused-sampling GEMM */
 #define RZ_PROF_KEEP_GEMM    1  /* learner logits + log-sum-exp GEMM keeping the terms */
 #define RZ_PROF_MERGE        2  /* split merges: log pi, lse, c_t, sampled token */
-#define RZ_PROF_DZ           3  /* dz pass over the kept terms */
+#define RZ_PROF_DZ           3  /* dz pass over the kept terms; on the reference route
+                                   the scaling of H's rows by sigma_t */
 #define RZ_PROF_DH_GEMM      4  /* dH = dz W */
 #define RZ_PROF_DW_GEMM      5  /* dW = dz^T H, accumulated over chunks */
 #define RZ_PROF_LOGITS_ROWS  6  /* given-logits row kernel */

@@ -36,8 +36,10 @@ bool device_ok() {
 }
 
 int64_t chunk_rows(int32_t V) {
-  // one chunk keeps rows x round_up(V, 8) fp16 terms (then bf16 dz) and a
-  // running max per 32 columns, at most 40 GiB together.
+  // one chunk keeps rows x round_up(V, 8) terms (fp16 then bf16 dz on the
+  // plain route, bf16 on the reference route) and, on the plain route, a
+  // running max per 32 columns: at most 40 GiB together.  Both routes use
+  // the plain route's (larger) bytes per row, so they chunk alike.
   const int64_t per_row = dz_ld(V) * 2 + emax_ld(V) * 4;
   int64_t rows = kChunkRowsMax;
   const int64_t cap = (int64_t(40) << 30) / (per_row > 0 ? per_row : 1);

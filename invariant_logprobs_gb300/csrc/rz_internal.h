@@ -28,8 +28,9 @@ inline int vocab_splits(int V) {
   return (nt + tps - 1) / tps;
 }
 
-// Rows per backward chunk: the chunk's kept fp16 terms (overwritten in place
-// by bf16 dz) and one fp32 running max per 32 columns live in the workspace.
+// Rows per backward chunk: the chunk's kept terms (fp16, overwritten in place
+// by bf16 dz, with one fp32 running max per 32 columns; or bf16 against the
+// reference) live in the workspace.
 constexpr int64_t kChunkRowsMax = 38912;  // 256 * 152
 int64_t chunk_rows(int32_t V);
 inline int64_t dz_ld(int32_t V) { return (static_cast<int64_t>(V) + 7) / 8 * 8; }
