@@ -20,7 +20,8 @@ def _inputs(g, T, d, V):
     return H, W, tok
 
 
-def test_rollout_and_learner_replay_bitwise(rz):
+@pytest.mark.parametrize("route", ["plain", "ref"])
+def test_rollout_and_learner_replay_bitwise(rz, route):
     T, d, V, B = 1500, 256, 5003, 6
     g = torch.Generator(device=DEV)
     g.manual_seed(31)
@@ -28,10 +29,12 @@ def test_rollout_and_learner_replay_bitwise(rz):
     cu = torch.tensor([0, 100, 400, 401, 900, 1200, 1500], dtype=torch.int64, device=DEV)
     adv = torch.randn(B, generator=g, device=DEV)
     logmu = torch.empty(T, device=DEV)
+    lse = torch.empty(T, device=DEV)  # the rollout's log-sum-exp (the reference route's input)
 
     # buffers the graph will own
     ws_r = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, DEV)
-    ws_l = rz.alloc_workspace(rz.RZ_OP_LOSS_FWD_BWD, T, d, V, B, DEV)
+    op = rz.RZ_OP_LOSS_FWD_BWD_REF if route == "ref" else rz.RZ_OP_LOSS_FWD_BWD
+    ws_l = rz.alloc_workspace(op, T, d, V, B, DEV)
     lp = torch.empty(T, device=DEV)
     dH = torch.empty(T, d, dtype=torch.bfloat16, device=DEV)
     dW = torch.empty(V, d, device=DEV)
@@ -39,10 +42,14 @@ def test_rollout_and_learner_replay_bitwise(rz):
     d3 = torch.empty(1, device=DEV)
 
     def work():
-        rz.rz_token_logprob(H, W, tok, logprob_out=logmu, ws=ws_r)
+        rz.rz_token_logprob(H, W, tok, logprob_out=logmu, lse_out=lse, ws=ws_r)
         logmu.add_(-0.01)  # a small recorded-vs-learner gap, inside the graph too
-        rz.rz_loss_fwd_bwd(H, W, tok, logmu, cu, adv, logprob_out=lp, dH=dH, dW=dW,
-                           loss_out=loss, d3_out=d3, ws=ws_l)
+        if route == "ref":
+            rz.rz_loss_fwd_bwd_ref(H, W, tok, logmu, lse, cu, adv, logprob_out=lp, dH=dH, dW=dW,
+                                   loss_out=loss, d3_out=d3, ws=ws_l)
+        else:
+            rz.rz_loss_fwd_bwd(H, W, tok, logmu, cu, adv, logprob_out=lp, dH=dH, dW=dW,
+                               loss_out=loss, d3_out=d3, ws=ws_l)
 
     def snapshot():
         torch.cuda.synchronize()
