@@ -330,7 +330,48 @@ def other_workloads(args, rank, dev, peaks, peak_src):
                                            "algorithmic_frac_of_sustained_bf16", "roofline",
                                            "step_breakdown", "config")}
         torch.cuda.empty_cache()
+    res["invariance_d2048_rollout"] = rollout_batch_sizes(dev, peaks)
+    torch.cuda.empty_cache()
     return res
+
+
+def rollout_batch_sizes(dev, peaks, d=2048, V=151936, sizes=(1, 7, 64, 513, 4096), reps=15):
+    """rz_token_logprob at the batch sizes of the invariance sweep (d = 2048,
+    V = 151936; bitwise batch invariance is a test, this is its speed):
+    median device time per call over `reps` calls, each after a 256 MB write
+    that pushes W out of L2.  Small batches are bound by reading W
+    (V d 2 bytes), so the line gives that rate against the measured copy
+    bandwidth; large ones by the tensor cores (2 d V flop per row)."""
+    import torch
+    import invariant_logprobs_gb300 as rz
+    g = torch.Generator(device=dev).manual_seed(2004)
+    W = (torch.randn(V, d, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    Hb = torch.randn(max(sizes), d, generator=g, device=dev).to(torch.bfloat16)
+    tok = torch.randint(0, V, (max(sizes),), generator=g, device=dev, dtype=torch.int32)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for T in sizes:
+        lp = torch.empty(T, device=dev)
+        ws = rz.alloc_workspace(rz.RZ_OP_TOKEN_LOGPROB, T, d, V, 0, dev)
+        for _ in range(3):
+            rz.rz_token_logprob(Hb[:T], W, tok[:T], logprob_out=lp, ws=ws)
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rz.rz_token_logprob(Hb[:T], W, tok[:T], logprob_out=lp, ws=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        m = statistics.median(ms)
+        w_gbs = V * d * 2 / (m / 1e3) / 1e9
+        out["T=%d" % T] = {"ms": m, "W_read_GBs": w_gbs, "W_read_frac_of_hbm": w_gbs / peaks["hbm_gbs"],
+                           "tflops": 2.0 * d * V * T / (m / 1e3) / 1e12}
+    out["note"] = ("median of %d calls after a 256 MB L2 flush each; d = %d, V = %d; "
+                   "W_read_* counts W once per call" % (reps, d, V))
+    return out
 
 
 def measure_learner(args, world, rank, local, dev, peaks, peak_src, name=None, steps=None,
