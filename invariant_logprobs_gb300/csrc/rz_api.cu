@@ -133,7 +133,7 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
                  cudaStream_t st) {
   if (T == 0) return RZ_OK;
   CUtensorMap tmH, tmW;
-  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   const FwdLayout L = fwd_layout(T, V);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
@@ -141,7 +141,7 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
   {
     ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax),
                  st);
-    RZ_TRY(launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err, st));
+    RZ_TRY(launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err, st, a_box_rows(T)));
   }
   ProfScope ps(RZ_PROF_MERGE, 1, st);
   RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse_ws, err, st));
@@ -200,7 +200,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
   const int64_t ldz = dz_ld(V);
   const int64_t ldm = emax_ld(V);
   CUtensorMap tmH, tmW, tmWmn, tmHmn;
-  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmWmn, W, d, V, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmHmn, H, d, T, uint64_t(d) * 2, 64, 64)) return RZ_ERR_UNSUPPORTED;
@@ -232,7 +232,7 @@ int learner_step(bool sc, const rz_bf16* H, const rz_bf16* W, const int32_t* tok
     {
       ProfScope ps(RZ_PROF_KEEP_GEMM, 1, st);
       RZ_TRY(launch_lse_keep(tmH, tmW, r0, rows, d, V, tokens + r0, part, zg, tmE16, emax, ldm,
-                             ref ? ref_lse + r0 : nullptr, err_flag, st));
+                             ref ? ref_lse + r0 : nullptr, err_flag, st, a_box_rows(T)));
     }
     {
       ProfScope ps(RZ_PROF_MERGE, 1, st);
@@ -334,7 +334,7 @@ int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids
   if (!ws || ws_bytes < L.total || !a256(ws)) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   CUtensorMap tmH, tmW;
-  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax) + 1,
@@ -342,7 +342,8 @@ int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids
   return cuda_status(launch_sample(tmH, tmW, T, d, V, row_ids, seed,
                                    reinterpret_cast<float4*>(w8 + L.part),
                                    reinterpret_cast<int*>(w8 + L.idx), tokens_out, logprob_out,
-                                   lse_out, err_flag, reinterpret_cast<cudaStream_t>(stream)));
+                                   lse_out, err_flag, reinterpret_cast<cudaStream_t>(stream),
+                                   a_box_rows(T)));
 }
 
 int rz_group_advantage(const float* rewards, int32_t B, int32_t G, float* adv_out,
@@ -515,10 +516,10 @@ int rz_lmhead_logits(const rz_bf16* H, const rz_bf16* W, int64_t T, int32_t d, i
   if (!a16(H) || !a16(W)) return RZ_ERR_UNSUPPORTED;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   CUtensorMap tmH, tmW;
-  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   return cuda_status(launch_logits_f32(tmH, tmW, T, d, V, logits_out, err_flag,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+                                       reinterpret_cast<cudaStream_t>(stream), a_box_rows(T)));
 }
 
 }  // extern "C"

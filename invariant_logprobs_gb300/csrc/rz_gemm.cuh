@@ -61,6 +61,10 @@ struct GemmSched {
   int a_k_off;          // added to the K coordinate of MN-major A loads
   int b_k_off;          // added to the K coordinate of B loads
   int* err;             // device error word (nullable)
+  uint32_t a_bytes;     // bytes one A load brings (0: a full 128-row box).  A
+                        // K-major A box of fewer rows (a batch of < 128 rows)
+                        // fills the first rows of the stage; the kernel keeps
+                        // the rest of its A stages zero
 };
 
 template <bool kAMN, bool kBMN>
@@ -178,6 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  if (sched.a_bytes != 0 && sched.a_bytes < kTileABytes) {
+    // rows past the A box stay zero for the whole kernel, as a full box
+    // would have filled them past the last row
+    uint4* a4 = reinterpret_cast<uint4*>(sA);
+    for (uint32_t i = threadIdx.x; i < kStages * kTileABytes / 16; i += kThreads)
+      a4[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // visible to the tensor cores' reads
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -205,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], kTileABytes + kTileBBytes);
+            mbar_arrive_expect_tx(&full[stage],
+                                  (sched.a_bytes != 0 ? sched.a_bytes : kTileABytes) + kTileBBytes);
             const int k0 = kb * kBK;
             Ops::load_a(sA + stage * kTileABytes, &tmA, &full[stage], m0, k0 + sched.a_k_off);
             Ops::load_b(sB + stage * kTileBBytes, &tmB, &full[stage], n * kBN,

@@ -85,22 +85,31 @@ cudaError_t check_read_lmhead(unsigned int* count, int* site);
 cudaError_t check_read_logits(unsigned int* count, int* site);
 
 // ---- lm-head kernels (rz_lmhead.cu)
+// Rows of the K-major A box (the hidden states) of a call over T rows: a
+// batch of fewer than 128 rows loads only its own rows, rounded up to 8 (a
+// box lying mostly past the last row is slow to fill: 0.23 vs 0.18 ms for
+// one row at d = 2560).  The tensor map of H and the launch take the same
+// value.
+inline uint32_t a_box_rows(int64_t T) {
+  return T < kBM ? static_cast<uint32_t>((T + 7) / 8 * 8) : static_cast<uint32_t>(kBM);
+}
 cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                                int V, const int32_t* tokens, float2* part, float* zgather,
-                               int* err, cudaStream_t st);
+                               int* err, cudaStream_t st, uint32_t a_rows);
 cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const float2* part,
                              const float* zgather, float* logprob, float* lse, float* lse_ws,
                              int* err, cudaStream_t st);
 cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
-                          int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st);
+                          int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st,
+                          uint32_t a_rows);
 // tmE16: the chunk's kept terms [rows, V] (row stride dz_ld(V)), box 64 x 32:
 // fp16 with running maxima in emax, or (ref != null) bf16 against the
 // per-row reference ref [rows] (chunk-local), no maxima.
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
                             float* zgather, const CUtensorMap& tmE16, float* emax, int64_t ldm,
-                            const float* ref, int* err, cudaStream_t st);
+                            const float* ref, int* err, cudaStream_t st, uint32_t a_rows);
 // Hs[r, :] = sigma[r] H[row0 + r, :] (bf16) for one chunk's rows.
 cudaError_t launch_scale_rows(const uint16_t* H, int64_t row0, int64_t rows, int d,
                               const float* sigma, uint16_t* Hs, cudaStream_t st);
@@ -114,7 +123,7 @@ cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t
                            int64_t rows, int V, const int32_t* tokens, const float* lse,
                            const float* coef, const float* logpi, cudaStream_t st);
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
-                              int V, float* out, int* err, cudaStream_t st);
+                              int V, float* out, int* err, cudaStream_t st, uint32_t a_rows);
 // rowscale (nullable, [rows]): dH rows multiplied by it before rounding.
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
                       int64_t rows, int d, int V, uint16_t* dH, const float* rowscale, int* err,

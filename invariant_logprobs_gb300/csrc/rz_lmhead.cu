@@ -840,7 +840,7 @@ GemmSched sched_of(long long m_rows, int n_cols, int n_groups, long long k_depth
 // power cap a lower clock).  A row's result does not depend on the block.
 cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                                int V, const int32_t* tokens, float2* part, float* zgather,
-                               int* err, cudaStream_t st) {
+                               int* err, cudaStream_t st, uint32_t a_rows) {
   const int S = vocab_splits(V);
   for (int64_t r0 = 0; r0 < T; r0 += kChunkRowsMax) {
     const int64_t rows = (T - r0) < kChunkRowsMax ? (T - r0) : kChunkRowsMax;
@@ -848,6 +848,7 @@ cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, i
     s.tiles_per_group = vocab_tiles_per_split(V);
     s.m_group = vocab_raster_group();
     s.a_m_off = static_cast<int>(r0);
+    s.a_bytes = a_rows * kBK * 2u;
     EpiLsePartial::Params p{tokens + r0, part + r0 * S, zgather + r0,
                             static_cast<long long>(rows), V, S};
     cudaError_t e = run_gemm<EpiLsePartial, false, false>(tmH, tmW, s, p, st);
@@ -869,7 +870,8 @@ cudaError_t launch_lse_merge(int64_t T, int V, const int32_t* tokens, const floa
 
 cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d, int V,
                           const int64_t* row_ids, uint64_t seed, float4* part, int* part_idx,
-                          int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st) {
+                          int32_t* tokens, float* logprob, float* lse, int* err, cudaStream_t st,
+                          uint32_t a_rows) {
   const int S = vocab_splits(V);
   for (int64_t r0 = 0; r0 < T; r0 += kChunkRowsMax) {  // row blocks as in launch_lse_partial
     const int64_t rows = (T - r0) < kChunkRowsMax ? (T - r0) : kChunkRowsMax;
@@ -877,6 +879,7 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
     s.tiles_per_group = vocab_tiles_per_split(V);
     s.m_group = vocab_raster_group();
     s.a_m_off = static_cast<int>(r0);
+    s.a_bytes = a_rows * kBK * 2u;
     EpiSample::Params p{row_ids ? row_ids + r0 : nullptr,
                         part + r0 * S,
                         part_idx + r0 * S,
@@ -900,12 +903,13 @@ cudaError_t launch_sample(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_
 cudaError_t launch_lse_keep(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t row0,
                             int64_t rows, int d, int V, const int32_t* tokens, float2* part,
                             float* zgather, const CUtensorMap& tmE16, float* emax, int64_t ldm,
-                            const float* ref, int* err, cudaStream_t st) {
+                            const float* ref, int* err, cudaStream_t st, uint32_t a_rows) {
   const int S = vocab_splits(V);
   GemmSched s = sched_of(rows, V, S, d, err);
   s.tiles_per_group = vocab_tiles_per_split(V);
   s.m_group = vocab_raster_group();
   s.a_m_off = static_cast<int>(row0);
+  s.a_bytes = a_rows * kBK * 2u;
   const EpiLsePartial::Params lp{tokens, part, zgather, static_cast<long long>(rows), V, S};
   if (ref) {
     EpiLseKeepRef::Params p{tmE16, lp, nullptr, ldm, ref, err};
@@ -947,7 +951,7 @@ cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t
 }
 
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
-                              int V, float* out, int* err, cudaStream_t st) {
+                              int V, float* out, int* err, cudaStream_t st, uint32_t a_rows) {
   const int S = vocab_splits(V);
   for (int64_t r0 = 0; r0 < T; r0 += kChunkRowsMax) {  // row blocks as in launch_lse_partial
     const int64_t rows = (T - r0) < kChunkRowsMax ? (T - r0) : kChunkRowsMax;
@@ -955,6 +959,7 @@ cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, in
     s.tiles_per_group = vocab_tiles_per_split(V);
     s.m_group = vocab_raster_group();
     s.a_m_off = static_cast<int>(r0);
+    s.a_bytes = a_rows * kBK * 2u;
     EpiStore<1>::Params p{out, V, r0, rows, V, 0};
     cudaError_t e = run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
     if (e != cudaSuccess) return e;

@@ -78,12 +78,13 @@ int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const int32_t* 
   if (!scratch) return RZ_ERR_CUDA;
 
   CUtensorMap tmH, tmW;
-  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, kBM)) return RZ_ERR_UNSUPPORTED;
+  if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   float2* part = reinterpret_cast<float2*>(scratch + L.part);
   float* zg = reinterpret_cast<float*>(scratch + L.zg);
-  if (launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err_flag, st) != cudaSuccess)
+  if (launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err_flag, st, a_box_rows(T)) !=
+      cudaSuccess)
     return RZ_ERR_CUDA;
   if (launch_lse_merge(T, V, tokens, part, zg, logprob_out, lse_out, nullptr, err_flag, st) !=
       cudaSuccess)
