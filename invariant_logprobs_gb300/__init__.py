@@ -202,7 +202,8 @@ def new_err_flag(device):
 def rz_token_logprob(H, W, tokens, logprob_out=None, lse_out=None, ws=None, err_flag=None,
                      stream=None):
     """Rollout-side per-token logprob (see include/rz.h).  Returns
-    (logprob [T] fp32, lse [T] fp32 or None)."""
+    (logprob [T] fp32, lse [T] fp32): lse is each row's log-sum-exp, the
+    reference rz_loss_fwd_bwd_ref takes (allocated here unless given)."""
     torch = _torch()
     lib = load()
     _need(H, torch.bfloat16, "H")
@@ -221,9 +222,11 @@ def rz_token_logprob(H, W, tokens, logprob_out=None, lse_out=None, ws=None, err_
     _same_device(H, W, tokens, logprob_out, lse_out, ws, err_flag)
     if ws is None:
         ws = alloc_workspace(RZ_OP_TOKEN_LOGPROB, T, d, V, 0, H.device)
+    ws_bytes, strm = _ws_bytes(ws), _stream(stream)  # checked before allocating lse
+    if lse_out is None:
+        lse_out = torch.empty(T, dtype=torch.float32, device=H.device)
     st = lib.rz_token_logprob(_ptr(H), _ptr(W), _ptr(tokens), T, d, V, _ptr(logprob_out),
-                              _ptr(lse_out), _ptr(ws), _ws_bytes(ws), _ptr(err_flag),
-                              _stream(stream))
+                              _ptr(lse_out), _ptr(ws), ws_bytes, _ptr(err_flag), strm)
     _check("rz_token_logprob", st)
     return logprob_out, lse_out
 

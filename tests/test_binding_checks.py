@@ -109,6 +109,11 @@ def test_valid_calls_reach_the_library(lib):
                 loss_out=zeros(1), ws=learn_ws, err_flag=err, stream=S,
                 action_mask=zeros(T, dtype=torch.uint8))
     _unsupported(rz.rz_loss_fwd_bwd, H, W, tok, logmu, cu, adv, d3_out=zeros(1), **outs)
+    ref_outs = dict(outs, ws=workspace(rz.workspace_size(rz.RZ_OP_LOSS_FWD_BWD_REF, T, d, V, B)))
+    _unsupported(rz.rz_loss_fwd_bwd_ref, H, W, tok, logmu, zeros(T), cu, adv, d3_out=zeros(1),
+                 **ref_outs)
+    _unsupported(rz.rz_loss_fwd_bwd_shard, H, W, tok, logmu, cu, adv, 2 * B, d3_out=zeros(1),
+                 ref_lse=zeros(T), **ref_outs)
     _unsupported(rz.rz_sc_loss_fwd_bwd, H, W, tok, cu, adv, **outs)
     _unsupported(rz.rz_logits_loss_fwd_bwd, zeros(T, V, dtype=torch.bfloat16), tok, logmu, cu,
                  adv, logprob_out=lp, loss_out=zeros(1), d3_out=zeros(1),
