@@ -227,3 +227,27 @@ def test_ref_nan_reference_sets_the_range_flag(rz):
     rz.rz_loss_fwd_bwd_ref(H, W, tok, lm, R, cu, adv, err_flag=err)
     torch.cuda.synchronize()
     assert err.item() & rz.RZ_DEVERR_RANGE
+
+
+@pytest.mark.parametrize("V", [1, 8, 264])
+def test_ref_tiny_vocabularies(rz, V):
+    """One-column, one-tile and ragged-tile vocabularies on the reference
+    route: against the oracle and the plain route (V = 1: log pi = 0 and the
+    gradients vanish)."""
+    g = torch.Generator().manual_seed(V)
+    T, d = 37, 64
+    H = _rand_bf16((T, d), 1.0, g)
+    W = _rand_bf16((V, d), 0.3, g)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    cu = torch.tensor([0, 20, T], dtype=torch.int64)
+    adv = torch.tensor([0.8, -0.3])
+    lm, R = _rollout(rz, H.to(DEV), W.to(DEV), tok.to(DEV))
+    lm = lm - 0.02
+    out = _both(rz, H.to(DEV), W.to(DEV), tok.to(DEV), lm, R, cu.to(DEV), adv.to(DEV))
+    ref = oracle.loss_fwd_bwd(f64(H), f64(W), f64(tok), f64(lm), f64(cu), f64(adv))
+    if V == 1:
+        assert float(out["logprob"].abs().max()) == 0.0
+        assert float(out["dH"].float().abs().max()) == 0.0
+        assert float(out["dW"].abs().max()) == 0.0
+    else:
+        _check(out, ref)
