@@ -62,9 +62,9 @@ struct GemmSched {
   int b_k_off;          // added to the K coordinate of B loads
   int* err;             // device error word (nullable)
   uint32_t a_bytes;     // bytes one A load brings (0: a full 128-row box).  A
-                        // K-major A box of fewer rows (a batch of < 128 rows)
-                        // fills the first rows of the stage; the kernel keeps
-                        // the rest of its A stages zero
+                        // K-major A box of fewer rows (a batch of < 128 rows:
+                        // exactly its rows) fills the first rows of the
+                        // stage; the kernel keeps the rest of its A stages zero
 };
 
 template <bool kAMN, bool kBMN>

@@ -86,12 +86,12 @@ cudaError_t check_read_logits(unsigned int* count, int* site);
 
 // ---- lm-head kernels (rz_lmhead.cu)
 // Rows of the K-major A box (the hidden states) of a call over T rows: a
-// batch of fewer than 128 rows loads only its own rows, rounded up to 8 (a
-// box lying mostly past the last row is slow to fill: 0.23 vs 0.18 ms for
-// one row at d = 2560).  The tensor map of H and the launch take the same
-// value.
+// batch of fewer than 128 rows loads exactly its own rows (a box lying past
+// the last row is slow to fill: 0.23-0.26 vs 0.15-0.18 ms for one row), the
+// GEMM keeps the rest of its A stages zero.  The tensor map of H and the
+// launch take the same value.
 inline uint32_t a_box_rows(int64_t T) {
-  return T < kBM ? static_cast<uint32_t>((T + 7) / 8 * 8) : static_cast<uint32_t>(kBM);
+  return T < 1 ? 1u : (T < kBM ? static_cast<uint32_t>(T) : static_cast<uint32_t>(kBM));
 }
 cudaError_t launch_lse_partial(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                                int V, const int32_t* tokens, float2* part, float* zgather,
