@@ -128,9 +128,12 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RZ_OK : RZ_ERR
   } while (0)
 
 // log pi for all T rows: identical launch sequence for rollout and learner.
+// A decode-sized batch (decode_mode) given the scratch after the pass's own
+// workspace takes the logits through it and folds them there (the same
+// bits as the fused pass, which runs otherwise).
 int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int64_t T, int32_t d,
                  int32_t V, float* logprob, float* lse, float* lse_ws, uint8_t* ws, int* err,
-                 cudaStream_t st) {
+                 cudaStream_t st, bool scratch) {
   if (T == 0) return RZ_OK;
   CUtensorMap tmH, tmW;
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
@@ -138,6 +141,17 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
   const FwdLayout L = fwd_layout(T, V);
   float2* part = reinterpret_cast<float2*>(ws + L.part);
   float* zg = reinterpret_cast<float*>(ws + L.zg);
+  if (scratch && decode_mode(T, V)) {
+    float* z = reinterpret_cast<float*>(ws + L.total);
+    {
+      ProfScope ps(RZ_PROF_LOGPROB_GEMM, 1, st);
+      RZ_TRY(launch_decode_logits(tmH, tmW, T, d, V, z, err, st, a_box_rows(T)));
+    }
+    ProfScope ps(RZ_PROF_MERGE, 2, st);
+    RZ_TRY(launch_decode_fold(z, T, V, tokens, part, zg, st));
+    RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse_ws, err, st));
+    return RZ_OK;
+  }
   {
     ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax),
                  st);
@@ -295,7 +309,8 @@ const char* rz_status_string(int status) {
 size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
   if (T < 0) T = 0;
   switch (op) {
-    case RZ_OP_TOKEN_LOGPROB: return fwd_layout(T, V > 0 ? V : 1).total;
+    case RZ_OP_TOKEN_LOGPROB:
+      return fwd_layout(T, V > 0 ? V : 1).total + decode_bytes(T, V > 0 ? V : 1);
     case RZ_OP_LOSS_FWD_BWD:
     case RZ_OP_SC_LOSS_FWD_BWD: return learn_layout(T, V > 0 ? V : 1, B).total;
     case RZ_OP_LOSS_FWD_BWD_REF: return learn_layout(T, V > 0 ? V : 1, B, true, d).total;
@@ -314,11 +329,12 @@ int rz_token_logprob(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, 
   if (d % 8 != 0) return RZ_ERR_UNSUPPORTED;
   if (T == 0) return RZ_OK;
   if (!a16(H) || !a16(W)) return RZ_ERR_UNSUPPORTED;
-  const size_t need = rz_workspace_size(RZ_OP_TOKEN_LOGPROB, T, d, V, 0);
+  const size_t need = fwd_layout(T, V).total;
   if (!ws || ws_bytes < need || !a256(ws)) return RZ_ERR_WORKSPACE;
   if (!device_ok()) return RZ_ERR_UNSUPPORTED;
   return logprob_pass(H, W, tokens, T, d, V, logprob_out, lse_out, nullptr,
-                      static_cast<uint8_t*>(ws), err_flag, reinterpret_cast<cudaStream_t>(stream));
+                      static_cast<uint8_t*>(ws), err_flag, reinterpret_cast<cudaStream_t>(stream),
+                      ws_bytes >= need + decode_bytes(T, V));
 }
 
 int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids, int64_t T,

@@ -56,6 +56,27 @@ inline FwdLayout fwd_layout(int64_t T, int32_t V) {
   return L;
 }
 
+// Decode-sized batches (at most kDecodeRows rows, with a logits scratch of
+// at most kDecodeBytes): the logprob pass first computes the fp32 logits
+// with one 256-column tile per task -- every SM streams W, where one task
+// per (row block, vocab split) keeps only 60 SMs busy -- into the
+// workspace, then a fold kernel takes the fused epilogue's per-row fold over
+// them with the same operations in the same order: the same bits.
+// (1-7 rows: 0.175 -> 0.150 ms at d = 2560; 64 rows about even; 128 rows
+// slower, as the fold grows with the rows while the GEMM does not)
+constexpr int64_t kDecodeRows = 64;
+constexpr size_t kDecodeBytes = size_t(256) << 20;
+inline int64_t decode_ld(int32_t V) { return (static_cast<int64_t>(V) + 63) / 64 * 64; }
+inline bool decode_mode(int64_t T, int32_t V) {
+  return T > 0 && T <= kDecodeRows &&
+         static_cast<size_t>(T) * static_cast<size_t>(decode_ld(V)) * 4 <= kDecodeBytes;
+}
+// the logits scratch, appended to the pass's workspace (0 outside decode mode)
+inline size_t decode_bytes(int64_t T, int32_t V) {
+  return decode_mode(T, V) ? al256(static_cast<size_t>(T) * static_cast<size_t>(decode_ld(V)) * 4)
+                           : 0;
+}
+
 int num_sms();
 bool device_ok();  // current device is sm_103 (or newer family member we compiled for)
 
@@ -124,6 +145,13 @@ cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t
                            const float* coef, const float* logpi, cudaStream_t st);
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                               int V, float* out, int* err, cudaStream_t st, uint32_t a_rows);
+// Decode mode (decode_mode(T, V)): z [T, decode_ld(V)] fp32 with one tile per
+// task, then the fused epilogue's fold over it: split states and gathered
+// logit (then launch_lse_merge).
+cudaError_t launch_decode_logits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
+                                 int V, float* z, int* err, cudaStream_t st, uint32_t a_rows);
+cudaError_t launch_decode_fold(const float* z, int64_t T, int V, const int32_t* tokens,
+                               float2* part, float* zgather, cudaStream_t st);
 // rowscale (nullable, [rows]): dH rows multiplied by it before rounding.
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
                       int64_t rows, int d, int V, uint16_t* dH, const float* rowscale, int* err,

@@ -794,6 +794,91 @@ __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict
   if (lse) lse[t] = lse_from(M, sum);
 }
 
+// ============================================================== decode mode
+// The logprob pass's split states over stored logits, one warp per (split,
+// row).  The fused epilogue folds the split's 32-column chunks one after the
+// other; here its three steps are taken apart: every lane takes the maxima
+// of its chunks (lane l holds chunk l of each round of 32), a running
+// maximum over the chunks in order gives each chunk the m its terms are
+// summed against, every lane sums its chunks against that m, and the
+// rescales and additions of s then run in chunk order.  The same operations
+// on the same values (fold32_max, fold32_rescale, fold32_sum), so the same
+// bits as the fused pass.  z: [T, ldz] fp32, ldz a multiple of 64 (>= V):
+// a chunk's 32 loads stay inside its row.
+__global__ void __launch_bounds__(32)
+    decode_lse_kernel(const float* __restrict__ z, long long ldz, int V, int S, int tps,
+                      int n_tiles, const int32_t* __restrict__ tokens, float2* __restrict__ part,
+                      float* __restrict__ zgather) {
+  const int grp = blockIdx.x;
+  const long long g = blockIdx.y;
+  const int lane = threadIdx.x;
+  const float* zr = z + g * ldz;
+  const int c0 = grp * tps * kBN;
+  int c_end = (grp + 1) * tps * kBN;
+  if (c_end > n_tiles * kBN) c_end = n_tiles * kBN;
+  if (c_end > V) c_end = V;
+  const int C = (c_end - c0 + 31) / 32;  // the split's chunks that start below V
+  const int a = __ldg(tokens + g);
+  float m_run = -INFINITY;  // the maximum over the chunks of earlier rounds
+  float s = 0.f;
+  for (int base = 0; base < C; base += 32) {
+    const int k = base + lane;
+    const bool have = k < C;
+    const int cs = c0 + 32 * k;
+    float v[32];
+    if (have) {
+      const float4* src = reinterpret_cast<const float4*>(zr + cs);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 q = __ldg(src + i);
+        v[4 * i] = q.x;
+        v[4 * i + 1] = q.y;
+        v[4 * i + 2] = q.z;
+        v[4 * i + 3] = q.w;
+      }
+      if (cs + 32 > V) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (cs + j >= V) v[j] = -INFINITY;
+      }
+      const unsigned rel = static_cast<unsigned>(a - cs);
+      if (rel < 32u) {
+        float za = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (rel == static_cast<unsigned>(j)) za = v[j];
+        zgather[g] = za;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+    }
+    const float cm = have ? fold32_max(v) : -INFINITY;
+    // M_k: the running maximum after chunk k (max is exact in any order)
+    float incl = cm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl = fmaxf(incl, t);
+    }
+    incl = fmaxf(incl, m_run);
+    float prev = __shfl_up_sync(0xffffffffu, incl, 1);  // M_{k-1}
+    if (lane == 0) prev = m_run;
+    float e[32], acc[4];
+    const float w = have ? fold32_sum<false>(v, incl, e, acc) : 0.f;
+    const int nk = C - base < 32 ? C - base : 32;
+    for (int j = 0; j < nk; ++j) {
+      const float cmj = __shfl_sync(0xffffffffu, cm, j);
+      float mj = __shfl_sync(0xffffffffu, prev, j);
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      fold32_rescale(mj, s, cmj);
+      s = __fadd_rn(s, wj);
+    }
+    m_run = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0 && RZ_DCHECK(grp < S, 14)) part[g * S + grp] = make_float2(m_run, s);
+}
+
 // ============================================================== launchers
 namespace {
 
@@ -978,6 +1063,26 @@ cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t
   }
   EpiStore<0>::Params p{dH, d, row0, rows, d, 0, nullptr};
   return run_gemm<EpiStore<0>, false, true>(tmDz, tmWmn, s, p, st);
+}
+
+cudaError_t launch_decode_logits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
+                                 int V, float* z, int* err, cudaStream_t st, uint32_t a_rows) {
+  const int nt = vocab_tiles(V);
+  GemmSched s = sched_of(T, V, nt, d, err);  // one 256-column tile per task
+  s.m_group = s.m_blocks;                    // a tile's row blocks run together
+  s.a_bytes = a_rows * kBK * 2u;
+  EpiStore<1>::Params p{z, decode_ld(V), 0, static_cast<long long>(T), V, 0};
+  return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
+}
+
+cudaError_t launch_decode_fold(const float* z, int64_t T, int V, const int32_t* tokens,
+                               float2* part, float* zgather, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int S = vocab_splits(V);
+  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(T));
+  decode_lse_kernel<<<grid, 32, 0, st>>>(z, decode_ld(V), V, S, vocab_tiles_per_split(V),
+                                         vocab_tiles(V), tokens, part, zgather);
+  return cudaGetLastError();
 }
 
 cudaError_t check_read_lmhead(unsigned int* count, int* site) {

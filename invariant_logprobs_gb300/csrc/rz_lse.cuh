@@ -19,10 +19,11 @@ namespace rz {
 // the maximum itself, whose term is exactly 1.  The caller guarantees at
 // least one finite logit.  With kKeep the 32 terms 2^((z - m) log2 e), taken
 // against the updated m, are also returned in e (0 past V); the state is
-// computed by the very same operations either way.
-template <bool kKeep>
-__device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float (&v)[32],
-                                                float (&e)[32], float (&acc)[4], float& w) {
+// computed by the very same operations either way.  The three steps are
+// also used one by one, over many chunks at once, by the decode-mode fold:
+// the chunk's maximum, the rescale of s when the maximum grows, and the
+// chunk's sum against the updated maximum.
+__device__ __forceinline__ float fold32_max(const float (&v)[32]) {
   float mx[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
   for (int j = 4; j < 32; j += 4) {
@@ -31,11 +32,19 @@ __device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float 
     mx[2] = fmaxf(mx[2], v[j + 2]);
     mx[3] = fmaxf(mx[3], v[j + 3]);
   }
-  const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+__device__ __forceinline__ void fold32_rescale(float& m, float& s, float cm) {
   if (cm > m) {
     s = __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, cm), kLog2e)));
     m = cm;
   }
+}
+
+template <bool kKeep>
+__device__ __forceinline__ float fold32_sum(const float (&v)[32], float m, float (&e)[32],
+                                            float (&acc)[4]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = 0.f;
 #pragma unroll
@@ -44,7 +53,14 @@ __device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float 
     if (kKeep) e[j] = t;
     acc[j & 3] = __fadd_rn(acc[j & 3], t);
   }
-  w = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+  return __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+}
+
+template <bool kKeep>
+__device__ __forceinline__ void lse_fold32_impl(float& m, float& s, const float (&v)[32],
+                                                float (&e)[32], float (&acc)[4], float& w) {
+  fold32_rescale(m, s, fold32_max(v));
+  w = fold32_sum<kKeep>(v, m, e, acc);
   s = __fadd_rn(s, w);
 }
 

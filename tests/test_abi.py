@@ -251,9 +251,11 @@ def test_vocab_splits_depend_on_v_only(lib):
     what fixes each row's reduction order whatever batch it is in."""
     import invariant_logprobs_gb300 as rz
 
-    def splits(V, T=32):
+    def splits(V, T=512):
+        # past the decode-sized batches (at most 64 rows), which also hold
+        # their logits
         ws = rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, T, 64, V, 0)
-        return (ws - 256) // (T * 8)  # T * 4 bytes of gathered logits -> one 256-byte block
+        return (ws - 2048) // (T * 8)  # T * 4 bytes of gathered logits -> 2048 bytes at T = 512
 
     def rule(V):
         tiles = -(-V // 256)
@@ -263,8 +265,13 @@ def test_vocab_splits_depend_on_v_only(lib):
     for V, want in [(1, 1), (256, 1), (257, 2), (16384, 64), (16385, 33), (151936, 60),
                     (1 << 24, 64)]:
         assert splits(V) == want == rule(V), V
-    for T in (32, 64, 320):
+    for T in (512, 1024, 4096):
         assert splits(151936, T) == 60
+    # a decode-sized batch's workspace adds its logits, [T, V rounded up to 64] fp32
+    for T in (1, 7, 64):
+        extra = rz.workspace_size(rz.RZ_OP_TOKEN_LOGPROB, T, 64, 151936, 0) - \
+            (-(-T * 60 * 8 // 256) * 256 + -(-T * 4 // 256) * 256)
+        assert extra == -(-T * 151936 * 4 // 256) * 256, T
 
 
 def test_profile_classes_and_host_side_behaviour(lib):

@@ -30,7 +30,11 @@ def test_batch_invariance_sweep(rz):
         for rep in range(2):
             H, tok, pos, pidx = synth.make_invariance_batch(pH, ptok, batch, g, DEV)
             lp, _ = rz.rz_token_logprob(H, W, tok, ws=ws)
+            # a workspace sized for this batch: decode-sized batches (<= 64
+            # rows) then take the logits through it and fold them apart
+            lp2, _ = rz.rz_token_logprob(H, W, tok)
             torch.cuda.synchronize()
+            assert np.array_equal(bits(lp), bits(lp2)), batch
             idx = pidx.cpu().numpy()
             b = bits(lp[pos])
             seen = known[idx]

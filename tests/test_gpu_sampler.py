@@ -69,15 +69,19 @@ def test_sampler_batch_invariant_and_learner_zero_mismatch(rz):
     torch.cuda.synchronize()
     g = torch.Generator(device=DEV)
     g.manual_seed(17)
+    ws_big = rz.alloc_workspace(rz.RZ_OP_SAMPLE, 4096, d, V, 0, DEV)
     for batch in synth.INVARIANCE_BATCH_SIZES:
         H, _, pos, pidx = synth.make_invariance_batch(pH, torch.zeros_like(pid, dtype=torch.int32),
                                                       batch, g, DEV)
         rid = torch.randint(0, 2**40, (batch,), generator=g, device=DEV, dtype=torch.int64) + 10**6
         rid[pos] = pid[pidx]
         tok, lmu = rz.rz_sample_logprob(H, W, seed, row_ids=rid)
+        # the same call on a workspace sized for 4,096 rows: the same bits
+        tok2, lmu2 = rz.rz_sample_logprob(H, W, seed, row_ids=rid, ws=ws_big)
         torch.cuda.synchronize()
         assert torch.equal(tok[pos], ref_tok[pidx])
         assert np.array_equal(bits(lmu[pos]), bits(ref_lmu[pidx]))
+        assert torch.equal(tok, tok2) and np.array_equal(bits(lmu), bits(lmu2)), batch
     # learner at the sampling weights: w == 1, D3 == 0 exactly
     cu = torch.tensor([0, 32, 64], dtype=torch.int64, device=DEV)
     adv = torch.tensor([0.5, -0.5], device=DEV)
