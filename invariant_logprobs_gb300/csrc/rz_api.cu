@@ -316,7 +316,8 @@ size_t rz_workspace_size(int op, int64_t T, int32_t d, int32_t V, int32_t B) {
     case RZ_OP_LOSS_FWD_BWD_REF: return learn_layout(T, V > 0 ? V : 1, B, true, d).total;
     case RZ_OP_LOGITS_LOSS: return is_loss_ws_bytes(B) + resp_factors_ws_bytes(B);
     case RZ_OP_IS_LOSS: return is_loss_ws_bytes(B);
-    case RZ_OP_SAMPLE: return sample_layout(T, V > 0 ? V : 1).total;
+    case RZ_OP_SAMPLE:
+      return sample_layout(T, V > 0 ? V : 1).total + decode_bytes(T, V > 0 ? V : 1);
     default: return 0;
   }
 }
@@ -353,6 +354,21 @@ int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (decode_mode(T, V) && ws_bytes >= L.total + decode_bytes(T, V)) {
+    // decode-sized batch: logits through the workspace, then the sampler's
+    // fold apart (the same bits)
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* z = reinterpret_cast<float*>(w8 + L.total);
+    {
+      ProfScope ps(RZ_PROF_LOGPROB_GEMM, 1, st);
+      RZ_TRY(launch_decode_logits(tmH, tmW, T, d, V, z, err_flag, st, a_box_rows(T)));
+    }
+    ProfScope ps(RZ_PROF_MERGE, 2, st);
+    return cuda_status(launch_decode_sample(z, T, V, row_ids, seed,
+                                            reinterpret_cast<float4*>(w8 + L.part),
+                                            reinterpret_cast<int*>(w8 + L.idx), tokens_out,
+                                            logprob_out, lse_out, st));
+  }
   ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax) + 1,
                reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(launch_sample(tmH, tmW, T, d, V, row_ids, seed,

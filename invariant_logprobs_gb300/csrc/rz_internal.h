@@ -152,6 +152,10 @@ cudaError_t launch_decode_logits(const CUtensorMap& tmH, const CUtensorMap& tmW,
                                  int V, float* z, int* err, cudaStream_t st, uint32_t a_rows);
 cudaError_t launch_decode_fold(const float* z, int64_t T, int V, const int32_t* tokens,
                                float2* part, float* zgather, cudaStream_t st);
+// ... or the fused sampler's split states, then its merge
+cudaError_t launch_decode_sample(const float* z, int64_t T, int V, const int64_t* row_ids,
+                                 uint64_t seed, float4* part, int* part_idx, int32_t* tokens,
+                                 float* logprob, float* lse, cudaStream_t st);
 // rowscale (nullable, [rows]): dH rows multiplied by it before rounding.
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
                       int64_t rows, int d, int V, uint16_t* dH, const float* rowscale, int* err,

@@ -405,9 +405,22 @@ struct EpiSample {
     st.rng.words(static_cast<uint32_t>(cbase) >> 5, x);
     const bool rep = __fmul_rn(uniform_of(x[0]), st.s) < W;
     if (!__any_sync(0xffffffffu, rep)) return;  // the warp stays converged
-    // draw from this chunk: the class (column mod 4) by the class sums, then
-    // the member inside it; on rounding past the end, the last positive one
-    const float tgt = __fmul_rn(uniform_of(x[1]), W);
+    float zsel;
+    const int off = draw_in_chunk(v, e, acc, W, x[1], zsel);
+    if (rep && off >= 0) {
+      st.bi = cbase + off;
+      st.bz = zsel;
+    }
+  }
+
+  // The draw inside a chunk that replaces the split's candidate: the class
+  // (column mod 4) by the class sums, then the member inside it; on
+  // rounding past the end, the last positive one.  Returns the column inside
+  // the chunk (-1: none) and its logit in zsel_out.
+  static __device__ __forceinline__ int draw_in_chunk(const float (&v)[32], const float (&e)[32],
+                                                      const float (&acc)[4], float W, uint32_t x1,
+                                                      float& zsel_out) {
+    const float tgt = __fmul_rn(uniform_of(x1), W);
     int k = -1, lastk = 0;
     float cum = 0.f, base = 0.f, lastbase = 0.f;
 #pragma unroll
@@ -453,10 +466,8 @@ struct EpiSample {
       sel = last;
       zsel = zlast;
     }
-    if (rep && sel >= 0) {
-      st.bi = cbase + 4 * sel + k;
-      st.bz = zsel;
-    }
+    zsel_out = zsel;
+    return sel >= 0 ? 4 * sel + k : -1;
   }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, int, int n_tile,
@@ -879,6 +890,105 @@ __global__ void __launch_bounds__(32)
   if (lane == 0 && RZ_DCHECK(grp < S, 14)) part[g * S + grp] = make_float2(m_run, s);
 }
 
+// The fused sampler's split states over stored logits, one warp per (split,
+// row): the fold as in decode_lse_kernel (every chunk's terms kept while its
+// round is in registers), the running sum after each chunk recorded by the
+// chunk's lane, then each lane's replace decision (the epilogue's test, on
+// the same Philox words) and, for a replacing chunk, the same in-chunk draw
+// (EpiSample::draw_in_chunk).  The split's sample is the draw of the last
+// chunk that replaced, as in the epilogue's walk: the same bits.
+__global__ void __launch_bounds__(32)
+    decode_sample_kernel(const float* __restrict__ z, long long ldz, int V, int S, int tps,
+                         int n_tiles, const int64_t* __restrict__ row_ids, uint32_t k0,
+                         uint32_t k1, float4* __restrict__ part, int* __restrict__ part_idx) {
+  const int grp = blockIdx.x;
+  const long long g = blockIdx.y;
+  const int lane = threadIdx.x;
+  const float* zr = z + g * ldz;
+  const int c0 = grp * tps * kBN;
+  int c_end = (grp + 1) * tps * kBN;
+  if (c_end > n_tiles * kBN) c_end = n_tiles * kBN;
+  if (c_end > V) c_end = V;
+  const int C = (c_end - c0 + 31) / 32;
+  const long long rid = row_ids ? __ldg(row_ids + g) : g;
+  PhiloxRow rng;
+  rng.init(static_cast<uint32_t>(static_cast<unsigned long long>(rid) & 0xffffffffull),
+           static_cast<uint32_t>(static_cast<unsigned long long>(rid) >> 32), k0, k1);
+  float m_run = -INFINITY;
+  float s = 0.f;
+  int bi = -1;
+  float bz = 0.f;
+  for (int base = 0; base < C; base += 32) {
+    const int k = base + lane;
+    const bool have = k < C;
+    const int cs = c0 + 32 * k;
+    float v[32];
+    if (have) {
+      const float4* src = reinterpret_cast<const float4*>(zr + cs);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 q = __ldg(src + i);
+        v[4 * i] = q.x;
+        v[4 * i + 1] = q.y;
+        v[4 * i + 2] = q.z;
+        v[4 * i + 3] = q.w;
+      }
+      if (cs + 32 > V) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (cs + j >= V) v[j] = -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+    }
+    const float cm = have ? fold32_max(v) : -INFINITY;
+    float incl = cm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl = fmaxf(incl, t);
+    }
+    incl = fmaxf(incl, m_run);
+    float prev = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) prev = m_run;
+    float e[32], acc[4];
+    const float w = have ? fold32_sum<true>(v, incl, e, acc) : 0.f;
+    const int nk = C - base < 32 ? C - base : 32;
+    float s_mine = 0.f;  // the running sum after this lane's chunk
+    for (int j = 0; j < nk; ++j) {
+      const float cmj = __shfl_sync(0xffffffffu, cm, j);
+      float mj = __shfl_sync(0xffffffffu, prev, j);
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      fold32_rescale(mj, s, cmj);
+      s = __fadd_rn(s, wj);
+      if (lane == j) s_mine = s;
+    }
+    m_run = __shfl_sync(0xffffffffu, incl, 31);
+    bool rep = false;
+    int off = -1;
+    float zs = 0.f;
+    if (have) {
+      uint32_t x[4];
+      rng.words(static_cast<uint32_t>(cs) >> 5, x);
+      rep = __fmul_rn(uniform_of(x[0]), s_mine) < w;
+      if (rep) off = EpiSample::draw_in_chunk(v, e, acc, w, x[1], zs);
+    }
+    const unsigned take = __ballot_sync(0xffffffffu, rep && off >= 0);
+    if (take) {
+      const int src_lane = 31 - __clz(static_cast<int>(take));
+      const int off_l = __shfl_sync(0xffffffffu, off, src_lane);
+      const float zs_l = __shfl_sync(0xffffffffu, zs, src_lane);
+      bi = c0 + 32 * (base + src_lane) + off_l;
+      bz = zs_l;
+    }
+  }
+  if (lane == 0 && RZ_DCHECK(grp < S, 15)) {
+    part[g * S + grp] = make_float4(m_run, s, bz, 0.f);
+    part_idx[g * S + grp] = bi;
+  }
+}
+
 // ============================================================== launchers
 namespace {
 
@@ -1082,6 +1192,25 @@ cudaError_t launch_decode_fold(const float* z, int64_t T, int V, const int32_t* 
   const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(T));
   decode_lse_kernel<<<grid, 32, 0, st>>>(z, decode_ld(V), V, S, vocab_tiles_per_split(V),
                                          vocab_tiles(V), tokens, part, zgather);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_sample(const float* z, int64_t T, int V, const int64_t* row_ids,
+                                 uint64_t seed, float4* part, int* part_idx, int32_t* tokens,
+                                 float* logprob, float* lse, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int S = vocab_splits(V);
+  const uint32_t k0 = static_cast<uint32_t>(seed & 0xffffffffull);
+  const uint32_t k1 = static_cast<uint32_t>(seed >> 32);
+  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(T));
+  decode_sample_kernel<<<grid, 32, 0, st>>>(z, decode_ld(V), V, S, vocab_tiles_per_split(V),
+                                            vocab_tiles(V), row_ids, k0, k1, part, part_idx);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  const long long blocks = (T + threads - 1) / threads;
+  sample_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      T, S, part, part_idx, row_ids, k0, k1, tokens, logprob, lse);
   return cudaGetLastError();
 }
 
