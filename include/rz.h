@@ -91,10 +91,11 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
 /*
  * Bytes of scratch the operation needs for these sizes (0 if none).  Pure
  * host function; arguments an operation does not use are ignored.  For
- * RZ_OP_TOKEN_LOGPROB with at most 64 rows (a decode-sized batch; logits
- * scratch at most 256 MB) the size includes the batch's fp32 logits, [T, V
- * rounded up to 64]: with it the call spreads the LM-head GEMM over every SM
- * and folds the stored logits with the fused pass's own operations.  A
+ * RZ_OP_TOKEN_LOGPROB and RZ_OP_SAMPLE with at most 64 rows (a decode-sized
+ * batch; logits scratch at most 256 MB) the size includes the batch's fp32
+ * logits, [T, V rounded up to 64]: with it the call spreads the LM-head GEMM
+ * over every SM and folds the stored logits with the fused pass's own
+ * operations.  A
  * workspace sized for any larger T serves a smaller batch too (without the
  * logits scratch the call keeps the fused pass); the results are the same
  * bits either way.
