@@ -28,7 +28,12 @@ def _case(T, d, V, seed):
     return H, W, tok
 
 
-@pytest.mark.parametrize("shapes", [((3000, 512, 151936), (7777, 256, 5000))])
+@pytest.mark.parametrize("shapes", [((3000, 512, 151936), (7777, 256, 5000)),
+                                    # decode-sized batches: the logits fit the
+                                    # scratch up to 55 rows at V = 151936 (56:
+                                    # the fused pass, against the workspace
+                                    # entry point's decode path)
+                                    ((1, 2560, 151936), (55, 2048, 151936), (56, 2048, 151936))])
 def test_noalloc_matches_workspace_entry_point_twice(rz, shapes):
     for i, (T, d, V) in enumerate(shapes):
         H, W, tok = _case(T, d, V, 11 + i)
