@@ -40,16 +40,16 @@ GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_m
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 TRAFFIC_CAPTURES = {
     # learner keep GEMM taking the terms against the recorded log-sum-exp, one
-    # 38,912-row chunk at the 4B shape: 2.310 GB read + 2.932 GB written at
+    # 38,912-row chunk at the 4B shape: 1.942 GB read + 2.946 GB written at
     # 9,728 rows (one raster group of 76 m-blocks); a 38,912-row chunk is four
     # such groups (x4)
-    "qwen4b_lag64": {"bytes": 4 * (2.309682688e9 + 2.931859456e9), "sources": GEMM_SOURCES,
-                     "sources_sha256_16": "65d39e06c858ccb0"},
-    # given-logits row kernel (768 threads, two rows per SM): 5.401 GB read
+    "qwen4b_lag64": {"bytes": 4 * (1.941773312e9 + 2.946048000e9), "sources": GEMM_SOURCES,
+                     "sources_sha256_16": "0410dcbebf52a621"},
+    # given-logits row kernel (768 threads, two rows per SM): 5.389 GB read
     # + 4.893 GB written at 16,384 rows, scaled to the workload's 262,144
     # rows (x16)
-    "moe30b_logits": {"bytes": 16 * (5.400610304e9 + 4.892825600e9), "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "01c101b8cf62e5bd"},
+    "moe30b_logits": {"bytes": 16 * (5.388791296e9 + 4.893217536e9), "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "d0f1549642c2e583"},
 }
 
 
