@@ -342,9 +342,13 @@ def rollout_batch_sizes(dev, peaks, d=2048, V=151936, sizes=(1, 7, 64, 513, 4096
     """rz_token_logprob at the batch sizes of the invariance sweep (d = 2048,
     V = 151936; bitwise batch invariance is a test, this is its speed):
     median device time per call over `reps` calls, each after a 256 MB write
-    that pushes W out of L2.  Small batches are bound by reading W
-    (V d 2 bytes), so the line gives that rate against the measured copy
-    bandwidth; large ones by the tensor cores (2 d V flop per row)."""
+    that pushes W out of L2 (the write-back of the dirty lines it leaves
+    behind falls inside the timed call), and the mean over 10 calls issued
+    back to back (W, 622 MB, is larger than L2, so each call reads it from
+    DRAM again; what one call leaves in L2 is the part of W the next call
+    reads last).  Small batches are bound by reading W (V d 2 bytes), so the
+    line gives that rate against the measured copy bandwidth; large ones by
+    the tensor cores (2 d V flop per row)."""
     import torch
     import invariant_logprobs_gb300 as rz
     g = torch.Generator(device=dev).manual_seed(2004)
@@ -369,11 +373,26 @@ def rollout_batch_sizes(dev, peaks, d=2048, V=151936, sizes=(1, 7, 64, 513, 4096
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
         m = statistics.median(ms)
+        bb = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                rz.rz_token_logprob(Hb[:T], W, tok[:T], logprob_out=lp, ws=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            bb.append(e0.elapsed_time(e1) / 10)
+        mb = statistics.median(bb)
         w_gbs = V * d * 2 / (m / 1e3) / 1e9
+        wb_gbs = V * d * 2 / (mb / 1e3) / 1e9
         out["T=%d" % T] = {"ms": m, "W_read_GBs": w_gbs, "W_read_frac_of_hbm": w_gbs / peaks["hbm_gbs"],
-                           "tflops": 2.0 * d * V * T / (m / 1e3) / 1e12}
-    out["note"] = ("median of %d calls after a 256 MB L2 flush each; d = %d, V = %d; "
-                   "W_read_* counts W once per call" % (reps, d, V))
+                           "tflops": 2.0 * d * V * T / (m / 1e3) / 1e12,
+                           "ms_back_to_back": mb,
+                           "W_read_frac_of_hbm_back_to_back": wb_gbs / peaks["hbm_gbs"]}
+    out["note"] = ("ms: median of %d calls after a 256 MB L2 flush each; ms_back_to_back: "
+                   "median over 5 runs of the mean of 10 calls issued back to back (W is "
+                   "larger than L2); d = %d, V = %d; W_read_* counts W once per call"
+                   % (reps, d, V))
     return out
 
 

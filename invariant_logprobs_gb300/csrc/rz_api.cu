@@ -147,9 +147,8 @@ int logprob_pass(const rz_bf16* H, const rz_bf16* W, const int32_t* tokens, int6
       ProfScope ps(RZ_PROF_LOGPROB_GEMM, 1, st);
       RZ_TRY(launch_decode_logits(tmH, tmW, T, d, V, z, err, st, a_box_rows(T)));
     }
-    ProfScope ps(RZ_PROF_MERGE, 2, st);
-    RZ_TRY(launch_decode_fold(z, T, V, tokens, part, zg, st));
-    RZ_TRY(launch_lse_merge(T, V, tokens, part, zg, logprob, lse, lse_ws, err, st));
+    ProfScope ps(RZ_PROF_MERGE, 1, st);
+    RZ_TRY(launch_decode_logprob(z, T, V, tokens, logprob, lse, lse_ws, err, st));
     return RZ_OK;
   }
   {
@@ -356,18 +355,16 @@ int rz_sample_logprob(const rz_bf16* H, const rz_bf16* W, const int64_t* row_ids
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   if (decode_mode(T, V) && ws_bytes >= L.total + decode_bytes(T, V)) {
     // decode-sized batch: logits through the workspace, then the sampler's
-    // fold apart (the same bits)
+    // fold and merge over them (the same bits)
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* z = reinterpret_cast<float*>(w8 + L.total);
     {
       ProfScope ps(RZ_PROF_LOGPROB_GEMM, 1, st);
       RZ_TRY(launch_decode_logits(tmH, tmW, T, d, V, z, err_flag, st, a_box_rows(T)));
     }
-    ProfScope ps(RZ_PROF_MERGE, 2, st);
-    return cuda_status(launch_decode_sample(z, T, V, row_ids, seed,
-                                            reinterpret_cast<float4*>(w8 + L.part),
-                                            reinterpret_cast<int*>(w8 + L.idx), tokens_out,
-                                            logprob_out, lse_out, st));
+    ProfScope ps(RZ_PROF_MERGE, 1, st);
+    return cuda_status(
+        launch_decode_sample(z, T, V, row_ids, seed, tokens_out, logprob_out, lse_out, st));
   }
   ProfScope ps(RZ_PROF_LOGPROB_GEMM, static_cast<int>((T + kChunkRowsMax - 1) / kChunkRowsMax) + 1,
                reinterpret_cast<cudaStream_t>(stream));

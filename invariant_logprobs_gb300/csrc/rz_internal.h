@@ -146,16 +146,18 @@ cudaError_t launch_dz_rows(uint16_t* ez, int64_t lde, const float* emax, int64_t
 cudaError_t launch_logits_f32(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                               int V, float* out, int* err, cudaStream_t st, uint32_t a_rows);
 // Decode mode (decode_mode(T, V)): z [T, decode_ld(V)] fp32 with one tile per
-// task, then the fused epilogue's fold over it: split states and gathered
-// logit (then launch_lse_merge).
+// task, then the fused epilogue's fold over it and the merge of the split
+// states in one launch: log pi, lse (nullable) and lse_ws (nullable) as
+// launch_lse_merge gives them ...
 cudaError_t launch_decode_logits(const CUtensorMap& tmH, const CUtensorMap& tmW, int64_t T, int d,
                                  int V, float* z, int* err, cudaStream_t st, uint32_t a_rows);
-cudaError_t launch_decode_fold(const float* z, int64_t T, int V, const int32_t* tokens,
-                               float2* part, float* zgather, cudaStream_t st);
-// ... or the fused sampler's split states, then its merge
+cudaError_t launch_decode_logprob(const float* z, int64_t T, int V, const int32_t* tokens,
+                                  float* logprob, float* lse, float* lse_ws, int* err,
+                                  cudaStream_t st);
+// ... or the fused sampler's fold and merge (sampled tokens, log mu, lse)
 cudaError_t launch_decode_sample(const float* z, int64_t T, int V, const int64_t* row_ids,
-                                 uint64_t seed, float4* part, int* part_idx, int32_t* tokens,
-                                 float* logprob, float* lse, cudaStream_t st);
+                                 uint64_t seed, int32_t* tokens, float* logprob, float* lse,
+                                 cudaStream_t st);
 // rowscale (nullable, [rows]): dH rows multiplied by it before rounding.
 cudaError_t launch_dH(const CUtensorMap& tmDz, const CUtensorMap& tmWmn, int64_t row0,
                       int64_t rows, int d, int V, uint16_t* dH, const float* rowscale, int* err,

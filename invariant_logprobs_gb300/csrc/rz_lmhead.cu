@@ -18,6 +18,7 @@
 // logprob, "REINFORCE Zero" project page s.02 and the vLLM post s.4 item 1);
 // dz from differentiating the loss through the numerator pi only (project
 // page s.02, "A minimal REINFORCE objective").
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -32,6 +33,8 @@
 #include "rz_ptx.cuh"
 
 namespace rz {
+
+namespace cg = cooperative_groups;
 
 // ============================================================== epilogues
 // Online log-sum-exp: state (m, s) with m = max z so far and
@@ -588,10 +591,8 @@ struct EpiStore {
 // ============================================================== merge kernels
 // Merge one row's S split states in split order; log pi = z[t, a_t] - lse.
 // An out-of-range token gives NaN for both and raises RZ_DEVERR_TOKEN_RANGE.
-__device__ __forceinline__ float merge_row(const float2* pp, int S, int V, int a,
-                                           const float* zg, float* l_out, int* err) {
-  float sum;
-  const float M = lse_merge_parts(pp, S, &sum);
+__device__ __forceinline__ float merge_finish(float M, float sum, int V, int a, const float* zg,
+                                              float* l_out, int* err) {
   if (a < 0 || a >= V) {
     if (err) atomicOr(err, 1);
     *l_out = __int_as_float(0x7fc00000);
@@ -599,6 +600,12 @@ __device__ __forceinline__ float merge_row(const float2* pp, int S, int V, int a
   }
   *l_out = lse_from(M, sum);
   return logprob_from(*zg, M, sum);
+}
+__device__ __forceinline__ float merge_row(const float2* pp, int S, int V, int a,
+                                           const float* zg, float* l_out, int* err) {
+  float sum;
+  const float M = lse_merge_parts(pp, S, &sum);
+  return merge_finish(M, sum, V, a, zg, l_out, err);
 }
 
 // One thread per row.
@@ -770,10 +777,38 @@ __global__ void __launch_bounds__(kDzThreads)
   }
 }
 
-// One thread per row: the log-sum-exp exactly as lse_merge_kernel, and the
-// split level of the sampler's reservoir: splits in order, the running sum R
-// of their totals (scaled to the row's maximum as the log-sum-exp scales
-// them), the sample replaced by split g's candidate when U3 R < its total.
+// The split level of the sampler's reservoir for one row, given the row's
+// maximum M and the splits' factors f(g) = e^(m_g - M) (lse_merge_factor):
+// splits in order, the running sum R of their totals (scaled to the row's
+// maximum as the log-sum-exp scales them), the sample replaced by split g's
+// candidate when U3 R < its total (u(g) = U3 of split g).
+template <class F, class U>
+__device__ __forceinline__ int sample_merge_pick(const float4* pp, const int* pidx, int S,
+                                                 const F& f, const U& u, float* bz_out) {
+  float R = 0.f, bz = 0.f;
+  int bi = 0;
+  for (int g = 0; g < S; ++g) {
+    const float w = __fmul_rn(pp[g].y, f(g));
+    R = __fadd_rn(R, w);
+    if (__fmul_rn(u(g), R) < w && pidx[g] >= 0) {
+      bi = pidx[g];
+      bz = pp[g].z;
+    }
+  }
+  *bz_out = bz;
+  return bi;
+}
+
+// U3 of split g: word 0 of Philox at counter (split, row id lo, row id hi, 1).
+__device__ __forceinline__ float split_uniform(int g, uint32_t rlo, uint32_t rhi, uint32_t k0,
+                                               uint32_t k1) {
+  uint32_t x[4];
+  philox4x32_10(static_cast<uint32_t>(g), rlo, rhi, 1u, k0, k1, x);
+  return uniform_of(x[0]);
+}
+
+// One thread per row: the log-sum-exp exactly as lse_merge_kernel, then the
+// split level of the reservoir (sample_merge_pick).
 __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict__ part,
                                     const int* __restrict__ part_idx,
                                     const int64_t* __restrict__ row_ids, uint32_t k0, uint32_t k1,
@@ -788,205 +823,251 @@ __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict
       static_cast<unsigned long long>(row_ids ? row_ids[t] : static_cast<int64_t>(t));
   const uint32_t rlo = static_cast<uint32_t>(rid & 0xffffffffull);
   const uint32_t rhi = static_cast<uint32_t>(rid >> 32);
-  float R = 0.f, bz = 0.f;
-  int bi = 0;
-  for (int g = 0; g < S; ++g) {
-    const float w = __fmul_rn(pp[g].y, exp2f(__fmul_rn(__fsub_rn(pp[g].x, M), kLog2e)));
-    R = __fadd_rn(R, w);
-    uint32_t x[4];
-    philox4x32_10(static_cast<uint32_t>(g), rlo, rhi, 1u, k0, k1, x);
-    if (__fmul_rn(uniform_of(x[0]), R) < w && part_idx[t * S + g] >= 0) {
-      bi = part_idx[t * S + g];
-      bz = pp[g].z;
-    }
-  }
-  tokens[t] = bi;
+  float bz;
+  tokens[t] = sample_merge_pick(
+      pp, part_idx + t * S, S, [&](int g) { return lse_merge_factor(pp[g].x, M); },
+      [&](int g) { return split_uniform(g, rlo, rhi, k0, k1); }, &bz);
   logprob[t] = logprob_from(bz, M, sum);
   if (lse) lse[t] = lse_from(M, sum);
 }
 
 // ============================================================== decode mode
-// The logprob pass's split states over stored logits, one warp per (split,
-// row).  The fused epilogue folds the split's 32-column chunks one after the
-// other; here its three steps are taken apart: every lane takes the maxima
-// of its chunks (lane l holds chunk l of each round of 32), a running
+// The logprob pass over stored logits z ([T, ldz] fp32, ldz a multiple of 64
+// and >= V, so a chunk's 32 loads stay inside its row): one warp per
+// (vocabulary split, row), one cluster of kDecCluster CTAs per row.  The
+// fused epilogue folds a split's 32-column chunks one after the other; here
+// its steps are taken apart, a round of 32 chunks at a time (lane l holding
+// chunk l of the round): every lane takes its chunk's maximum, a running
 // maximum over the chunks in order gives each chunk the m its terms are
-// summed against, every lane sums its chunks against that m, and the
-// rescales and additions of s then run in chunk order.  The same operations
-// on the same values (fold32_max, fold32_rescale, fold32_sum), so the same
-// bits as the fused pass.  z: [T, ldz] fp32, ldz a multiple of 64 (>= V):
-// a chunk's 32 loads stay inside its row.
-__global__ void __launch_bounds__(32)
-    decode_lse_kernel(const float* __restrict__ z, long long ldz, int V, int S, int tps,
-                      int n_tiles, const int32_t* __restrict__ tokens, float2* __restrict__ part,
-                      float* __restrict__ zgather) {
-  const int grp = blockIdx.x;
-  const long long g = blockIdx.y;
-  const int lane = threadIdx.x;
-  const float* zr = z + g * ldz;
-  const int c0 = grp * tps * kBN;
+// summed against and the factor that rescales s when the maximum grows,
+// every lane sums its chunk against that m, and the rescales and additions
+// of s then run in chunk order.  The same operations on the same values
+// (fold32_max, fold32_scale, fold32_sum), so the same bits as the fused
+// pass.  The split states then go through distributed shared memory to the
+// cluster's first CTA, which merges them in split order as the merge
+// kernels do (lse_merge_max, lse_merge_factor, the same sums in the same
+// order), with the splits' factors evaluated on the lanes of one warp.
+constexpr int kDecWarps = 8;    // warps per CTA, one vocabulary split each
+constexpr int kDecCluster = 8;  // CTAs per row
+static_assert(kDecWarps * kDecCluster >= kMaxVocabSplits, "one warp per split");
+
+// Columns [c0, c0 + 32 C) of split grp (C: its chunks that start below V).
+__device__ __forceinline__ int dec_split_chunks(int grp, int tps, int n_tiles, int V, int* c0) {
+  *c0 = grp * tps * kBN;
   int c_end = (grp + 1) * tps * kBN;
   if (c_end > n_tiles * kBN) c_end = n_tiles * kBN;
   if (c_end > V) c_end = V;
-  const int C = (c_end - c0 + 31) / 32;  // the split's chunks that start below V
-  const int a = __ldg(tokens + g);
-  float m_run = -INFINITY;  // the maximum over the chunks of earlier rounds
-  float s = 0.f;
-  for (int base = 0; base < C; base += 32) {
-    const int k = base + lane;
-    const bool have = k < C;
-    const int cs = c0 + 32 * k;
-    float v[32];
-    if (have) {
-      const float4* src = reinterpret_cast<const float4*>(zr + cs);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 q = __ldg(src + i);
-        v[4 * i] = q.x;
-        v[4 * i + 1] = q.y;
-        v[4 * i + 2] = q.z;
-        v[4 * i + 3] = q.w;
-      }
-      if (cs + 32 > V) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (cs + j >= V) v[j] = -INFINITY;
-      }
-      const unsigned rel = static_cast<unsigned>(a - cs);
-      if (rel < 32u) {
-        float za = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (rel == static_cast<unsigned>(j)) za = v[j];
-        zgather[g] = za;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
-    }
-    const float cm = have ? fold32_max(v) : -INFINITY;
-    // M_k: the running maximum after chunk k (max is exact in any order)
-    float incl = cm;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl = fmaxf(incl, t);
-    }
-    incl = fmaxf(incl, m_run);
-    float prev = __shfl_up_sync(0xffffffffu, incl, 1);  // M_{k-1}
-    if (lane == 0) prev = m_run;
-    float e[32], acc[4];
-    const float w = have ? fold32_sum<false>(v, incl, e, acc) : 0.f;
-    const int nk = C - base < 32 ? C - base : 32;
-    for (int j = 0; j < nk; ++j) {
-      const float cmj = __shfl_sync(0xffffffffu, cm, j);
-      float mj = __shfl_sync(0xffffffffu, prev, j);
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      fold32_rescale(mj, s, cmj);
-      s = __fadd_rn(s, wj);
-    }
-    m_run = __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0 && RZ_DCHECK(grp < S, 14)) part[g * S + grp] = make_float2(m_run, s);
+  return (c_end - *c0 + 31) / 32;
 }
 
-// The fused sampler's split states over stored logits, one warp per (split,
-// row): the fold as in decode_lse_kernel (every chunk's terms kept while its
-// round is in registers), the running sum after each chunk recorded by the
-// chunk's lane, then each lane's replace decision (the epilogue's test, on
-// the same Philox words) and, for a replacing chunk, the same in-chunk draw
-// (EpiSample::draw_in_chunk).  The split's sample is the draw of the last
-// chunk that replaced, as in the epilogue's walk: the same bits.
-__global__ void __launch_bounds__(32)
-    decode_sample_kernel(const float* __restrict__ z, long long ldz, int V, int S, int tps,
-                         int n_tiles, const int64_t* __restrict__ row_ids, uint32_t k0,
-                         uint32_t k1, float4* __restrict__ part, int* __restrict__ part_idx) {
-  const int grp = blockIdx.x;
-  const long long g = blockIdx.y;
-  const int lane = threadIdx.x;
-  const float* zr = z + g * ldz;
-  const int c0 = grp * tps * kBN;
-  int c_end = (grp + 1) * tps * kBN;
-  if (c_end > n_tiles * kBN) c_end = n_tiles * kBN;
-  if (c_end > V) c_end = V;
-  const int C = (c_end - c0 + 31) / 32;
-  const long long rid = row_ids ? __ldg(row_ids + g) : g;
-  PhiloxRow rng;
-  rng.init(static_cast<uint32_t>(static_cast<unsigned long long>(rid) & 0xffffffffull),
-           static_cast<uint32_t>(static_cast<unsigned long long>(rid) >> 32), k0, k1);
-  float m_run = -INFINITY;
-  float s = 0.f;
-  int bi = -1;
-  float bz = 0.f;
-  for (int base = 0; base < C; base += 32) {
-    const int k = base + lane;
-    const bool have = k < C;
-    const int cs = c0 + 32 * k;
-    float v[32];
-    if (have) {
-      const float4* src = reinterpret_cast<const float4*>(zr + cs);
+// The lane's chunk (columns cs .. cs + 31) of row zr; -inf past V and for a
+// lane without a chunk.
+__device__ __forceinline__ void dec_load(const float* zr, int cs, bool have, int V,
+                                         float (&v)[32]) {
+  if (have) {
+    const float4* src = reinterpret_cast<const float4*>(zr + cs);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 q = __ldg(src + i);
-        v[4 * i] = q.x;
-        v[4 * i + 1] = q.y;
-        v[4 * i + 2] = q.z;
-        v[4 * i + 3] = q.w;
-      }
-      if (cs + 32 > V) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (cs + j >= V) v[j] = -INFINITY;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+    for (int i = 0; i < 8; ++i) {
+      const float4 q = __ldg(src + i);
+      v[4 * i] = q.x;
+      v[4 * i + 1] = q.y;
+      v[4 * i + 2] = q.z;
+      v[4 * i + 3] = q.w;
     }
-    const float cm = have ? fold32_max(v) : -INFINITY;
-    float incl = cm;
+    if (cs + 32 > V) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl = fmaxf(incl, t);
+      for (int j = 0; j < 32; ++j)
+        if (cs + j >= V) v[j] = -INFINITY;
     }
-    incl = fmaxf(incl, m_run);
-    float prev = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) prev = m_run;
-    float e[32], acc[4];
-    const float w = have ? fold32_sum<true>(v, incl, e, acc) : 0.f;
-    const int nk = C - base < 32 ? C - base : 32;
-    float s_mine = 0.f;  // the running sum after this lane's chunk
-    for (int j = 0; j < nk; ++j) {
-      const float cmj = __shfl_sync(0xffffffffu, cm, j);
-      float mj = __shfl_sync(0xffffffffu, prev, j);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+  }
+}
+
+// One round of nk chunks (lane l: the round's chunk l, loaded in v): the
+// fold's state (m_run, s) carried through them in order.  Returns the lane's
+// chunk sum w (against the running maximum after its chunk); e and acc get
+// its terms and class sums (kKeep); s_mine gets s right after the lane's own
+// chunk.
+template <bool kKeep>
+__device__ __forceinline__ float dec_round(const float (&v)[32], bool have, int nk, int lane,
+                                           float& m_run, float& s, float (&e)[32],
+                                           float (&acc)[4], float& s_mine) {
+  const float cm = have ? fold32_max(v) : -INFINITY;
+  // M_k: the running maximum after chunk k (max is exact in any order)
+  float incl = cm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = fmaxf(incl, t);
+  }
+  incl = fmaxf(incl, m_run);
+  float prev = __shfl_up_sync(0xffffffffu, incl, 1);  // M_{k-1}
+  if (lane == 0) prev = m_run;
+  const float w = have ? fold32_sum<kKeep>(v, incl, e, acc) : 0.f;
+  // fold32_rescale(M_{k-1}, s, cm) of every chunk: the factors first, on
+  // all lanes at once, then s through the chunks in order
+  const bool up = cm > prev;
+  const float f = up ? fold32_scale(prev, cm) : 1.f;
+  const unsigned upm = __ballot_sync(0xffffffffu, up);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < nk) {  // warp-uniform
+      const float fj = __shfl_sync(0xffffffffu, f, j);
       const float wj = __shfl_sync(0xffffffffu, w, j);
-      fold32_rescale(mj, s, cmj);
+      if ((upm >> j) & 1u) s = __fmul_rn(s, fj);
       s = __fadd_rn(s, wj);
       if (lane == j) s_mine = s;
     }
-    m_run = __shfl_sync(0xffffffffu, incl, 31);
-    bool rep = false;
-    int off = -1;
-    float zs = 0.f;
-    if (have) {
-      uint32_t x[4];
-      rng.words(static_cast<uint32_t>(cs) >> 5, x);
-      rep = __fmul_rn(uniform_of(x[0]), s_mine) < w;
-      if (rep) off = EpiSample::draw_in_chunk(v, e, acc, w, x[1], zs);
+  }
+  m_run = __shfl_sync(0xffffffffu, incl, 31);
+  return w;
+}
+
+// The row's maximum over the split states in order (every lane) and the
+// splits' factors against it (fs[g], written by lane g % 32).
+template <class P>
+__device__ __forceinline__ float dec_merge_factors(const P* parts, int S, int lane, float* fs) {
+  const float M = lse_merge_max(parts, S);
+  for (int g = lane; g < S; g += 32) fs[g] = lse_merge_factor(parts[g].x, M);
+  __syncwarp();
+  return M;
+}
+
+__global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kDecWarps * 32, 1)
+    decode_logprob_kernel(const float* __restrict__ z, long long ldz, int V, int S, int tps,
+                          int n_tiles, const int32_t* __restrict__ tokens,
+                          float* __restrict__ logprob, float* __restrict__ lse,
+                          float* __restrict__ lse_ws, int* err) {
+  __shared__ float2 parts[kDecWarps * kDecCluster];
+  __shared__ float fs[kDecWarps * kDecCluster];
+  __shared__ float za;
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int grp = static_cast<int>(rank) * kDecWarps + warp;
+  const long long g = blockIdx.y;
+  const int a = __ldg(tokens + g);
+  if (grp < S) {
+    const float* zr = z + g * ldz;
+    int c0;
+    const int C = dec_split_chunks(grp, tps, n_tiles, V, &c0);
+    float m_run = -INFINITY, s = 0.f;
+    for (int base = 0; base < C; base += 32) {
+      const int k = base + lane;
+      const bool have = k < C;
+      const int cs = c0 + 32 * k;
+      float v[32], e[32], acc[4], s_mine;
+      dec_load(zr, cs, have, V, v);
+      const unsigned rel = static_cast<unsigned>(a - cs);
+      if (have && rel < 32u) {
+        float zv = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (rel == static_cast<unsigned>(j)) zv = v[j];
+        *cluster.map_shared_rank(&za, 0) = zv;
+      }
+      dec_round<false>(v, have, C - base < 32 ? C - base : 32, lane, m_run, s, e, acc, s_mine);
     }
-    const unsigned take = __ballot_sync(0xffffffffu, rep && off >= 0);
-    if (take) {
-      const int src_lane = 31 - __clz(static_cast<int>(take));
-      const int off_l = __shfl_sync(0xffffffffu, off, src_lane);
-      const float zs_l = __shfl_sync(0xffffffffu, zs, src_lane);
-      bi = c0 + 32 * (base + src_lane) + off_l;
-      bz = zs_l;
+    if (lane == 0 && RZ_DCHECK(grp < kDecWarps * kDecCluster, 14))
+      *cluster.map_shared_rank(&parts[grp], 0) = make_float2(m_run, s);
+  }
+  cluster.sync();
+  if (rank != 0 || warp != 0) return;
+  const float M = dec_merge_factors(parts, S, lane, fs);
+  if (lane != 0) return;
+  float sum = 0.f;
+  for (int q = 0; q < S; ++q) sum = fmaf(parts[q].y, fs[q], sum);
+  float l;
+  const float lp = merge_finish(M, sum, V, a, &za, &l, err);
+  logprob[g] = lp;
+  if (lse) lse[g] = l;
+  if (lse_ws) lse_ws[g] = l;
+}
+
+// The fused sampler over stored logits: each warp folds its split as above,
+// every chunk's terms kept while its round is in registers, the running sum
+// after each chunk recorded by the chunk's lane; then each lane's replace
+// decision (the epilogue's test, on the same Philox words) and, for a
+// replacing chunk, the same in-chunk draw (EpiSample::draw_in_chunk).  The
+// split's sample is the draw of the last chunk that replaced, as in the
+// epilogue's walk.  The merge takes the split level of the reservoir as
+// sample_merge_kernel does (sample_merge_pick), the Philox words of the
+// splits drawn on the lanes of one warp.  The same bits as the fused pass.
+__global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kDecWarps * 32, 1)
+    decode_sample_kernel(const float* __restrict__ z, long long ldz, int V, int S, int tps,
+                         int n_tiles, const int64_t* __restrict__ row_ids, uint32_t k0,
+                         uint32_t k1, int32_t* __restrict__ tokens, float* __restrict__ logprob,
+                         float* __restrict__ lse) {
+  __shared__ float4 parts[kDecWarps * kDecCluster];
+  __shared__ int pidx[kDecWarps * kDecCluster];
+  __shared__ float fs[kDecWarps * kDecCluster];
+  __shared__ float us[kDecWarps * kDecCluster];
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int grp = static_cast<int>(rank) * kDecWarps + warp;
+  const long long g = blockIdx.y;
+  const unsigned long long rid =
+      static_cast<unsigned long long>(row_ids ? __ldg(row_ids + g) : static_cast<int64_t>(g));
+  const uint32_t rlo = static_cast<uint32_t>(rid & 0xffffffffull);
+  const uint32_t rhi = static_cast<uint32_t>(rid >> 32);
+  if (grp < S) {
+    const float* zr = z + g * ldz;
+    int c0;
+    const int C = dec_split_chunks(grp, tps, n_tiles, V, &c0);
+    PhiloxRow rng;
+    rng.init(rlo, rhi, k0, k1);
+    float m_run = -INFINITY, s = 0.f;
+    int bi = -1;
+    float bz = 0.f;
+    for (int base = 0; base < C; base += 32) {
+      const int k = base + lane;
+      const bool have = k < C;
+      const int cs = c0 + 32 * k;
+      float v[32], e[32], acc[4];
+      float s_mine = 0.f;
+      dec_load(zr, cs, have, V, v);
+      const float w =
+          dec_round<true>(v, have, C - base < 32 ? C - base : 32, lane, m_run, s, e, acc, s_mine);
+      bool rep = false;
+      int off = -1;
+      float zs = 0.f;
+      if (have) {
+        uint32_t x[4];
+        rng.words(static_cast<uint32_t>(cs) >> 5, x);
+        rep = __fmul_rn(uniform_of(x[0]), s_mine) < w;
+        if (rep) off = EpiSample::draw_in_chunk(v, e, acc, w, x[1], zs);
+      }
+      const unsigned take = __ballot_sync(0xffffffffu, rep && off >= 0);
+      if (take) {
+        const int src_lane = 31 - __clz(static_cast<int>(take));
+        const int off_l = __shfl_sync(0xffffffffu, off, src_lane);
+        const float zs_l = __shfl_sync(0xffffffffu, zs, src_lane);
+        bi = c0 + 32 * (base + src_lane) + off_l;
+        bz = zs_l;
+      }
+    }
+    if (lane == 0 && RZ_DCHECK(grp < kDecWarps * kDecCluster, 15)) {
+      *cluster.map_shared_rank(&parts[grp], 0) = make_float4(m_run, s, bz, 0.f);
+      *cluster.map_shared_rank(&pidx[grp], 0) = bi;
     }
   }
-  if (lane == 0 && RZ_DCHECK(grp < S, 15)) {
-    part[g * S + grp] = make_float4(m_run, s, bz, 0.f);
-    part_idx[g * S + grp] = bi;
-  }
+  cluster.sync();
+  if (rank != 0 || warp != 0) return;
+  for (int q = lane; q < S; q += 32) us[q] = split_uniform(q, rlo, rhi, k0, k1);
+  const float M = dec_merge_factors(parts, S, lane, fs);  // ends with __syncwarp
+  if (lane != 0) return;
+  float sum = 0.f;
+  for (int q = 0; q < S; ++q) sum = fmaf(parts[q].y, fs[q], sum);
+  float bz;
+  tokens[g] = sample_merge_pick(
+      parts, pidx, S, [&](int q) { return fs[q]; }, [&](int q) { return us[q]; }, &bz);
+  logprob[g] = logprob_from(bz, M, sum);
+  if (lse) lse[g] = lse_from(M, sum);
 }
 
 // ============================================================== launchers
@@ -1185,32 +1266,27 @@ cudaError_t launch_decode_logits(const CUtensorMap& tmH, const CUtensorMap& tmW,
   return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
 }
 
-cudaError_t launch_decode_fold(const float* z, int64_t T, int V, const int32_t* tokens,
-                               float2* part, float* zgather, cudaStream_t st) {
+cudaError_t launch_decode_logprob(const float* z, int64_t T, int V, const int32_t* tokens,
+                                  float* logprob, float* lse, float* lse_ws, int* err,
+                                  cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  const int S = vocab_splits(V);
-  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(T));
-  decode_lse_kernel<<<grid, 32, 0, st>>>(z, decode_ld(V), V, S, vocab_tiles_per_split(V),
-                                         vocab_tiles(V), tokens, part, zgather);
+  const dim3 grid(kDecCluster, static_cast<unsigned>(T));
+  decode_logprob_kernel<<<grid, kDecWarps * 32, 0, st>>>(
+      z, decode_ld(V), V, vocab_splits(V), vocab_tiles_per_split(V), vocab_tiles(V), tokens,
+      logprob, lse, lse_ws, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_sample(const float* z, int64_t T, int V, const int64_t* row_ids,
-                                 uint64_t seed, float4* part, int* part_idx, int32_t* tokens,
-                                 float* logprob, float* lse, cudaStream_t st) {
+                                 uint64_t seed, int32_t* tokens, float* logprob, float* lse,
+                                 cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  const int S = vocab_splits(V);
   const uint32_t k0 = static_cast<uint32_t>(seed & 0xffffffffull);
   const uint32_t k1 = static_cast<uint32_t>(seed >> 32);
-  const dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(T));
-  decode_sample_kernel<<<grid, 32, 0, st>>>(z, decode_ld(V), V, S, vocab_tiles_per_split(V),
-                                            vocab_tiles(V), row_ids, k0, k1, part, part_idx);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int threads = 256;
-  const long long blocks = (T + threads - 1) / threads;
-  sample_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      T, S, part, part_idx, row_ids, k0, k1, tokens, logprob, lse);
+  const dim3 grid(kDecCluster, static_cast<unsigned>(T));
+  decode_sample_kernel<<<grid, kDecWarps * 32, 0, st>>>(
+      z, decode_ld(V), V, vocab_splits(V), vocab_tiles_per_split(V), vocab_tiles(V), row_ids, k0,
+      k1, tokens, logprob, lse);
   return cudaGetLastError();
 }
 

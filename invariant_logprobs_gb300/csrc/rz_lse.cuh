@@ -19,10 +19,10 @@ namespace rz {
 // the maximum itself, whose term is exactly 1.  The caller guarantees at
 // least one finite logit.  With kKeep the 32 terms 2^((z - m) log2 e), taken
 // against the updated m, are also returned in e (0 past V); the state is
-// computed by the very same operations either way.  The three steps are
-// also used one by one, over many chunks at once, by the decode-mode fold:
-// the chunk's maximum, the rescale of s when the maximum grows, and the
-// chunk's sum against the updated maximum.
+// computed by the very same operations either way.  The steps are also
+// used one by one, over many chunks at once, by the decode-mode fold: the
+// chunk's maximum, the factor that rescales s when the maximum grows, and
+// the chunk's sum against the updated maximum.
 __device__ __forceinline__ float fold32_max(const float (&v)[32]) {
   float mx[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
@@ -35,9 +35,14 @@ __device__ __forceinline__ float fold32_max(const float (&v)[32]) {
   return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
+// The factor s is multiplied by when the maximum grows from m to cm.
+__device__ __forceinline__ float fold32_scale(float m, float cm) {
+  return ex2_approx(__fmul_rn(__fsub_rn(m, cm), kLog2e));
+}
+
 __device__ __forceinline__ void fold32_rescale(float& m, float& s, float cm) {
   if (cm > m) {
-    s = __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, cm), kLog2e)));
+    s = __fmul_rn(s, fold32_scale(m, cm));
     m = cm;
   }
 }
@@ -86,13 +91,23 @@ __device__ __forceinline__ void lse_fold32_terms(float& m, float& s, const float
 // Merge the partial states of a row in a fixed order.  P is any struct with
 // .x = m and .y = s (float2, float4).  Returns M = max m and sets *sum to the
 // row's sum 2^((z - M) log2 e) over the whole vocabulary.
+// The merge's two steps are also taken apart by the decode-mode kernels,
+// which evaluate the splits' factors on the lanes of a warp at once: the
+// maximum over the states in order, and the factor of a state against it.
 template <class P>
-__device__ __forceinline__ float lse_merge_parts(const P* pp, int S, float* sum) {
+__device__ __forceinline__ float lse_merge_max(const P* pp, int S) {
   float M = -INFINITY;
   for (int g = 0; g < S; ++g) M = fmaxf(M, pp[g].x);
+  return M;
+}
+__device__ __forceinline__ float lse_merge_factor(float m, float M) {
+  return exp2f(__fmul_rn(__fsub_rn(m, M), kLog2e));
+}
+template <class P>
+__device__ __forceinline__ float lse_merge_parts(const P* pp, int S, float* sum) {
+  const float M = lse_merge_max(pp, S);
   float acc = 0.f;
-  for (int g = 0; g < S; ++g)
-    acc = fmaf(pp[g].y, exp2f(__fmul_rn(__fsub_rn(pp[g].x, M), kLog2e)), acc);
+  for (int g = 0; g < S; ++g) acc = fmaf(pp[g].y, lse_merge_factor(pp[g].x, M), acc);
   *sum = acc;
   return M;
 }

@@ -81,21 +81,22 @@ int rz_token_logprob_noalloc(const rz_bf16* H, const rz_bf16* W, const int32_t* 
   if (!make_tmap_bf16(&tmH, H, d, T, uint64_t(d) * 2, kBK, a_box_rows(T))) return RZ_ERR_UNSUPPORTED;
   if (!make_tmap_bf16(&tmW, W, d, V, uint64_t(d) * 2, kBK, kBN)) return RZ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  float2* part = reinterpret_cast<float2*>(scratch + L.part);
-  float* zg = reinterpret_cast<float*>(scratch + L.zg);
   if (decode_mode(T, V) && L.total + decode_bytes(T, V) <= kNoAllocScratchBytes) {
-    // a decode-sized batch whose logits fit the scratch (up to 52 rows at
+    // a decode-sized batch whose logits fit the scratch (up to 55 rows at
     // V = 151936): as rz_token_logprob does, the same bits
     float* z = reinterpret_cast<float*>(scratch + L.total);
     if (launch_decode_logits(tmH, tmW, T, d, V, z, err_flag, st, a_box_rows(T)) != cudaSuccess ||
-        launch_decode_fold(z, T, V, tokens, part, zg, st) != cudaSuccess)
+        launch_decode_logprob(z, T, V, tokens, logprob_out, lse_out, nullptr, err_flag, st) !=
+            cudaSuccess)
       return RZ_ERR_CUDA;
-  } else if (launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err_flag, st,
-                                a_box_rows(T)) != cudaSuccess) {
-    return RZ_ERR_CUDA;
+    return RZ_OK;
   }
-  if (launch_lse_merge(T, V, tokens, part, zg, logprob_out, lse_out, nullptr, err_flag, st) !=
-      cudaSuccess)
+  float2* part = reinterpret_cast<float2*>(scratch + L.part);
+  float* zg = reinterpret_cast<float*>(scratch + L.zg);
+  if (launch_lse_partial(tmH, tmW, T, d, V, tokens, part, zg, err_flag, st, a_box_rows(T)) !=
+          cudaSuccess ||
+      launch_lse_merge(T, V, tokens, part, zg, logprob_out, lse_out, nullptr, err_flag, st) !=
+          cudaSuccess)
     return RZ_ERR_CUDA;
   return RZ_OK;
 }
