@@ -984,17 +984,18 @@ def run_profile(args):
     per = max(1, args.rows // wl.B)
     wl = dataclasses.replace(wl, len_lo=per, len_hi=per, tokens="uniform")
     b = synth.make_batch(wl, device=dev)
-    if args.profile == "sample":
+    if args.profile in ("sample", "rollout"):
+        # fewer rows than the workload has responses: its first rows (a
+        # decode-sized batch takes the logits through the workspace)
+        n = min(args.rows, b["T"])
+        H, tok = b["H"][:n].contiguous(), b["tokens"][:n].contiguous()
         for k in range(args.steps):
-            rz.rz_sample_logprob(b["H"], b["W_mu"], 77 + k)
+            if args.profile == "sample":
+                rz.rz_sample_logprob(H, b["W_mu"], 77 + k)
+            else:
+                rz.rz_token_logprob(H, b["W_mu"], tok)
         torch.cuda.synchronize()
-        print("profile sample rows=%d ok" % b["T"])
-        return 0
-    if args.profile == "rollout":
-        for _ in range(args.steps):
-            rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"])
-        torch.cuda.synchronize()
-        print("profile rollout rows=%d ok" % b["T"])
+        print("profile %s rows=%d ok" % (args.profile, n))
         return 0
     lse = torch.empty(b["T"], dtype=torch.float32, device=dev)
     logmu, _ = rz.rz_token_logprob(b["H"], b["W_mu"], b["tokens"], lse_out=lse)
