@@ -40,16 +40,16 @@ GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_m
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 TRAFFIC_CAPTURES = {
     # learner keep GEMM taking the terms against the recorded log-sum-exp, one
-    # 38,912-row chunk at the 4B shape: 1.942 GB read + 2.946 GB written at
+    # 38,912-row chunk at the 4B shape: 1.941 GB read + 2.947 GB written at
     # 9,728 rows (one raster group of 76 m-blocks); a 38,912-row chunk is four
     # such groups (x4)
-    "qwen4b_lag64": {"bytes": 4 * (1.941773312e9 + 2.946048000e9), "sources": GEMM_SOURCES,
-                     "sources_sha256_16": "0410dcbebf52a621"},
-    # given-logits row kernel (768 threads, two rows per SM): 5.389 GB read
+    "qwen4b_lag64": {"bytes": 4 * (1.940542976e9 + 2.947392000e9), "sources": GEMM_SOURCES,
+                     "sources_sha256_16": "3ddca55261d78b91"},
+    # given-logits row kernel (768 threads, two rows per SM): 5.383 GB read
     # + 4.893 GB written at 16,384 rows, scaled to the workload's 262,144
     # rows (x16)
-    "moe30b_logits": {"bytes": 16 * (5.388791296e9 + 4.893217536e9), "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "d0f1549642c2e583"},
+    "moe30b_logits": {"bytes": 16 * (5.383338240e9 + 4.892902144e9), "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "435a4beb49e72b78"},
 }
 
 
