@@ -14,7 +14,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 pytestmark = pytest.mark.gpu
 SUITES = ["tests/test_gpu_parity.py", "tests/test_gpu_random_shapes.py",
-          "tests/test_gpu_sampler.py", "tests/test_gpu_profile.py"]
+          "tests/test_gpu_sampler.py", "tests/test_gpu_decode.py", "tests/test_gpu_profile.py"]
 
 
 def test_normal_build_has_no_checks(rz):
