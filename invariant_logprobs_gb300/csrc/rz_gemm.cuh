@@ -194,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up done: the next kernel may be scheduled, and this one waits for
+  // the kernel ahead of it (when launched to overlap its tail) before its
+  // first global access.
+  grid_dep_launch();
+  grid_dep_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer

@@ -846,7 +846,10 @@ __global__ void sample_merge_kernel(long long T, int S, const float4* __restrict
 // pass.  The split states then go through distributed shared memory to the
 // cluster's first CTA, which merges them in split order as the merge
 // kernels do (lse_merge_max, lse_merge_factor, the same sums in the same
-// order), with the splits' factors evaluated on the lanes of one warp.
+// order), with the splits' factors evaluated on the lanes of one warp.  The
+// logits GEMM and this kernel are launched with programmatic stream
+// serialization, so each starts while the kernel ahead of it finishes and
+// waits (griddepcontrol) only before touching memory.
 constexpr int kDecWarps = 8;    // warps per CTA, one vocabulary split each
 constexpr int kDecCluster = 8;  // CTAs per row
 static_assert(kDecWarps * kDecCluster >= kMaxVocabSplits, "one warp per split");
@@ -940,6 +943,8 @@ __global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kDecWarps 
                           int n_tiles, const int32_t* __restrict__ tokens,
                           float* __restrict__ logprob, float* __restrict__ lse,
                           float* __restrict__ lse_ws, int* err) {
+  grid_dep_launch();  // a following call's GEMM may start its set-up
+  grid_dep_wait();    // the logits GEMM ahead of this kernel has finished
   __shared__ float2 parts[kDecWarps * kDecCluster];
   __shared__ float fs[kDecWarps * kDecCluster];
   __shared__ float za;
@@ -1001,6 +1006,8 @@ __global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kDecWarps 
                          int n_tiles, const int64_t* __restrict__ row_ids, uint32_t k0,
                          uint32_t k1, int32_t* __restrict__ tokens, float* __restrict__ logprob,
                          float* __restrict__ lse) {
+  grid_dep_launch();  // a following call's GEMM may start its set-up
+  grid_dep_wait();    // the logits GEMM ahead of this kernel has finished
   __shared__ float4 parts[kDecWarps * kDecCluster];
   __shared__ int pidx[kDecWarps * kDecCluster];
   __shared__ float fs[kDecWarps * kDecCluster];
@@ -1076,14 +1083,47 @@ namespace {
 // Launch a GEMM: one persistent CTA per SM (or per task, if fewer).
 template <class Epi, bool kAMN, bool kBMN>
 cudaError_t run_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmSched& s,
-                     const typename Epi::Params& p, cudaStream_t st) {
+                     const typename Epi::Params& p, cudaStream_t st, bool overlap = false) {
   if (s.num_tasks <= 0) return cudaSuccess;
   auto kern = gemm_kernel<Epi, kAMN, kBMN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = s.num_tasks < num_sms() ? s.num_tasks : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, st>>>(a, b, s, p);
+  if (!overlap) {
+    kern<<<grid, kThreads, kSmemBytes, st>>>(a, b, s, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a, b, s, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// A small kernel launched to overlap the tail of the kernel ahead of it
+// (it starts with grid_dep_wait).
+template <class K, class... Args>
+cudaError_t launch_overlapped(K kern, dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1263,7 +1303,7 @@ cudaError_t launch_decode_logits(const CUtensorMap& tmH, const CUtensorMap& tmW,
   s.m_group = s.m_blocks;                    // a tile's row blocks run together
   s.a_bytes = a_rows * kBK * 2u;
   EpiStore<1>::Params p{z, decode_ld(V), 0, static_cast<long long>(T), V, 0};
-  return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st);
+  return run_gemm<EpiStore<1>, false, false>(tmH, tmW, s, p, st, true);
 }
 
 cudaError_t launch_decode_logprob(const float* z, int64_t T, int V, const int32_t* tokens,
@@ -1271,10 +1311,10 @@ cudaError_t launch_decode_logprob(const float* z, int64_t T, int V, const int32_
                                   cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const dim3 grid(kDecCluster, static_cast<unsigned>(T));
-  decode_logprob_kernel<<<grid, kDecWarps * 32, 0, st>>>(
-      z, decode_ld(V), V, vocab_splits(V), vocab_tiles_per_split(V), vocab_tiles(V), tokens,
-      logprob, lse, lse_ws, err);
-  return cudaGetLastError();
+  return launch_overlapped(decode_logprob_kernel, grid, dim3(kDecWarps * 32), st,
+                           z, static_cast<long long>(decode_ld(V)), V, vocab_splits(V),
+                           vocab_tiles_per_split(V), vocab_tiles(V), tokens, logprob, lse,
+                           lse_ws, err);
 }
 
 cudaError_t launch_decode_sample(const float* z, int64_t T, int V, const int64_t* row_ids,
@@ -1284,10 +1324,10 @@ cudaError_t launch_decode_sample(const float* z, int64_t T, int V, const int64_t
   const uint32_t k0 = static_cast<uint32_t>(seed & 0xffffffffull);
   const uint32_t k1 = static_cast<uint32_t>(seed >> 32);
   const dim3 grid(kDecCluster, static_cast<unsigned>(T));
-  decode_sample_kernel<<<grid, kDecWarps * 32, 0, st>>>(
-      z, decode_ld(V), V, vocab_splits(V), vocab_tiles_per_split(V), vocab_tiles(V), row_ids, k0,
-      k1, tokens, logprob, lse);
-  return cudaGetLastError();
+  return launch_overlapped(decode_sample_kernel, grid, dim3(kDecWarps * 32), st,
+                           z, static_cast<long long>(decode_ld(V)), V, vocab_splits(V),
+                           vocab_tiles_per_split(V), vocab_tiles(V), row_ids, k0, k1, tokens,
+                           logprob, lse);
 }
 
 cudaError_t check_read_lmhead(unsigned int* count, int* site) {
