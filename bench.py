@@ -40,16 +40,17 @@ GEMM_SOURCES = ["rz_gemm.cuh", "rz_lmhead.cu", "rz_lse.cuh", "rz_ptx.cuh", "rz_m
 LOGITS_SOURCES = ["rz_logits.cu", "rz_ptx.cuh", "rz_math.cuh", "rz_internal.h"]
 TRAFFIC_CAPTURES = {
     # learner keep GEMM taking the terms against the recorded log-sum-exp, one
-    # 38,912-row chunk at the 4B shape: 1.941 GB read + 2.947 GB written at
+    # 38,912-row chunk at the 4B shape: 2.321 GB read + 2.932 GB written at
     # 9,728 rows (one raster group of 76 m-blocks); a 38,912-row chunk is four
-    # such groups (x4)
-    "qwen4b_lag64": {"bytes": 4 * (1.940542976e9 + 2.947392000e9), "sources": GEMM_SOURCES,
-                     "sources_sha256_16": "3ddca55261d78b91"},
-    # given-logits row kernel (768 threads, two rows per SM): 5.383 GB read
+    # such groups (x4).  Its operand re-reads vary from capture to capture
+    # (1.94-2.36 GB read at 9,728 rows on the same kernel code).
+    "qwen4b_lag64": {"bytes": 4 * (2.320705536e9 + 2.931853824e9), "sources": GEMM_SOURCES,
+                     "sources_sha256_16": "c6598b72eec7cb31"},
+    # given-logits row kernel (768 threads, two rows per SM): 5.414 GB read
     # + 4.893 GB written at 16,384 rows, scaled to the workload's 262,144
     # rows (x16)
-    "moe30b_logits": {"bytes": 16 * (5.383338240e9 + 4.892902144e9), "sources": LOGITS_SOURCES,
-                      "sources_sha256_16": "435a4beb49e72b78"},
+    "moe30b_logits": {"bytes": 16 * (5.414485504e9 + 4.892578816e9), "sources": LOGITS_SOURCES,
+                      "sources_sha256_16": "47be4dfd2aa2d274"},
 }
 
 
