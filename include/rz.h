@@ -95,7 +95,10 @@ typedef struct CUstream_st* rz_stream_t;  /* == cudaStream_t */
  * batch; logits scratch at most 256 MB) the size includes the batch's fp32
  * logits, [T, V rounded up to 64]: with it the call spreads the LM-head GEMM
  * over every SM and folds the stored logits with the fused pass's own
- * operations.  A
+ * operations.  Those two kernels are launched with programmatic stream
+ * serialization: each may begin its set-up while the kernel ahead of it in
+ * the stream finishes, and waits for that kernel before any memory access,
+ * so stream order is kept.  A
  * workspace sized for any larger T serves a smaller batch too (without the
  * logits scratch the call keeps the fused pass); the results are the same
  * bits either way.
